@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for the W8A8 block-FP8 linear path.
+
+This module only draws random numbers and shapes them into the workloads'
+value distributions; it holds none of the quantisation or GEMM arithmetic.
+It is the one module that both the CUDA path's tests/benchmark and the CPU
+oracle's tests read their inputs from.
+
+All draws use numpy's PCG64 generator (``numpy.random.default_rng(seed)``),
+which gives the same stream on x86_64 and aarch64.  Activations are returned
+as bf16/fp16 bit patterns (uint16) rounded to nearest-even from fp32;
+weights as fp32 or bf16 bits.
+
+Workload recipes (the shapes the pages benchmark; DeepSeek-V3 projection
+N/K, "vLLM 量化 Kernel 配置机制" §3.2 and "vLLM DeepGEMM FP8 Block GEMM 基准测试"
+§3.2):
+  small      M=16, N=K=1536: act N(0,1) seed 0; weight fp32 N(0,0.02) seed 1
+  decode     act N(0,1), 1% of K-channels x30; weight N(0,0.02)
+  prefill    act Student-t(nu=3) scaled to unit RMS; weight N(0,0.02)
+  quant      act N(0,1); every 8th row (m % 8 == 3) holds one +-1000 spike per
+             128-group (position and sign seeded)
+  full grid  act N(0,1), 0.5% of K-channels x50; weight N(0,0.02)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SEED_ACT = 0
+SEED_WEIGHT = 1
+SEED_STRUCT = 2  # outlier channels / spike positions
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> fp16 bit patterns (numpy's cast rounds to nearest even)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def normal(shape, seed: int, std: float = 1.0) -> np.ndarray:
+    x = _rng(seed).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def student_t_unit_rms(shape, seed: int, nu: float = 3.0) -> np.ndarray:
+    t = _rng(seed).standard_t(nu, size=shape)
+    rms = np.sqrt(np.mean(np.square(t, dtype=np.float64)))
+    return (t / rms).astype(np.float32)
+
+
+def outlier_channels(K: int, frac: float, seed: int) -> np.ndarray:
+    """A seeded set of round(frac*K) (at least 1) distinct K-channel indices."""
+    n = max(1, int(round(frac * K)))
+    return np.sort(_rng(seed).choice(K, size=n, replace=False))
+
+
+def scale_channels(x: np.ndarray, channels: np.ndarray, factor: float) -> np.ndarray:
+    x[:, channels] *= np.float32(factor)
+    return x
+
+
+def group_spikes(x: np.ndarray, group: int, seed: int, value: float = 1000.0,
+                 row_period: int = 8, row_phase: int = 3) -> np.ndarray:
+    """In rows m % row_period == row_phase put one +-value per group of `group`
+    columns, at a seeded position with a seeded sign."""
+    M, K = x.shape
+    rows = np.arange(row_phase, M, row_period)
+    if rows.size == 0:
+        return x
+    G = K // group
+    rng = _rng(seed)
+    pos = rng.integers(0, group, size=(rows.size, G))
+    sign = np.where(rng.integers(0, 2, size=(rows.size, G)) == 0, -1.0, 1.0).astype(np.float32)
+    cols = np.arange(G)[None, :] * group + pos
+    x[rows[:, None], cols] = sign * np.float32(value)
+    return x
+
+
+# ------------------------------------------------------------ workloads --
+
+def act_small(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    return f32_to_bf16_bits(normal((M, K), seed))
+
+
+def act_decode(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal((M, K), seed)
+    scale_channels(x, outlier_channels(K, 0.01, SEED_STRUCT), 30.0)
+    return f32_to_bf16_bits(x)
+
+
+def act_prefill(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    return f32_to_bf16_bits(student_t_unit_rms((M, K), seed))
+
+
+def act_quant(M: int, K: int, group: int = 128, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal((M, K), seed)
+    group_spikes(x, group, SEED_STRUCT)
+    return f32_to_bf16_bits(x)
+
+
+def act_full_grid(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal((M, K), seed)
+    scale_channels(x, outlier_channels(K, 0.005, SEED_STRUCT), 50.0)
+    return f32_to_bf16_bits(x)
+
+
+def weight_f32(N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
+    return normal((N, K), seed, std=0.02)
+
+
+def weight_bf16(N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
+    return f32_to_bf16_bits(weight_f32(N, K, seed))
+
+
+# The pages' M grid ("vLLM 量化 Kernel 配置机制" §2) and the workload shape sets.
+M_GRID = (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128, 256, 512, 1024, 1536, 2048, 3072, 4096)
+DECODE_M = (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128)
+DECODE_NK = ((7168, 18432), (18432, 7168), (4096, 7168))
+PREFILL_M = (256, 512, 1024, 1536, 2048, 3072, 4096)
+PREFILL_NK = ((24576, 7168), (4096, 7168), (7168, 18432))
+QUANT_M = (1, 64, 1024, 4096, 16384)
+QUANT_K = (1536, 7168, 18432)
+FULL_NK = ((1536, 7168), (7168, 1536), (4096, 7168), (7168, 18432), (18432, 7168), (24576, 7168))

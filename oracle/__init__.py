@@ -1,0 +1,188 @@
+"""CPU oracle of the W8A8 block-FP8 linear path (ctypes binding of oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the benchmark's ``cpu_baseline`` / ``--impl reference`` legs.  The product
+package never imports it, and it shares no code with the CUDA path.
+
+Every function takes and returns numpy arrays; the C source states which page
+and section each step follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+
+BF16, FP16, FP32 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, no CUDA)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "oracle.h"))
+    ):
+        return _LIB
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        l = ctypes.CDLL(build())
+        i64, i32, vp, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
+        l.oracle_e4m3_decode.restype = dp
+        l.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        l.oracle_e4m3_encode.restype = ctypes.c_uint8
+        l.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        l.oracle_bf16_to_f32.restype = ctypes.c_float
+        l.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        l.oracle_f16_to_f32.restype = ctypes.c_float
+        l.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        l.oracle_group_scale.restype = ctypes.c_float
+        l.oracle_group_scale.argtypes = [ctypes.c_float, i32]
+        l.oracle_quant_value.restype = ctypes.c_uint8
+        l.oracle_quant_value.argtypes = [ctypes.c_float, ctypes.c_float]
+        l.oracle_act_scale_bytes.restype = i64
+        l.oracle_act_scale_bytes.argtypes = [i64, i64, i32, i32]
+        l.oracle_quant_act.restype = i32
+        l.oracle_quant_act.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp]
+        l.oracle_quant_weight.restype = i32
+        l.oracle_quant_weight.argtypes = [vp, i32, i64, i64, i32, i32, i32, vp, vp]
+        l.oracle_act_scale.restype = dp
+        l.oracle_act_scale.argtypes = [vp, i32, i64, i64, i32, i64, i64]
+        l.oracle_gemm.restype = i32
+        l.oracle_gemm.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, i32, i32, i64, i64, vp]
+        l.oracle_gemm_elem.restype = dp
+        l.oracle_gemm_elem.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, i32, i32, i64, i64]
+        l.oracle_calc_diff.restype = dp
+        l.oracle_calc_diff.argtypes = [vp, vp, i64]
+        _lib = l
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ------------------------------------------------------------------ codecs --
+
+def e4m3_decode(code: int) -> float:
+    return lib().oracle_e4m3_decode(int(code))
+
+
+def e4m3_decode_all() -> np.ndarray:
+    """Decoded value of all 256 codes (NaN for 0x7F, 0xFF)."""
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(y: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(y)))
+
+
+def group_scale(amax: float, ue8m0: bool) -> np.float32:
+    return np.float32(lib().oracle_group_scale(float(amax), int(bool(ue8m0))))
+
+
+def quant_value(x: float, s: float) -> int:
+    return int(lib().oracle_quant_value(float(x), float(s)))
+
+
+def bf16_to_f32(bits: int) -> np.float32:
+    return np.float32(lib().oracle_bf16_to_f32(int(bits)))
+
+
+def f16_to_f32(bits: int) -> np.float32:
+    return np.float32(lib().oracle_f16_to_f32(int(bits)))
+
+
+# ------------------------------------------------------------------- quant --
+
+def act_scale_bytes(M: int, K: int, group: int, ue8m0: bool) -> int:
+    return int(lib().oracle_act_scale_bytes(M, K, group, int(bool(ue8m0))))
+
+
+def quant_act(x_bits: np.ndarray, x_dtype: int, group: int, ue8m0: bool):
+    """x_bits: uint16 [M,K] (bf16 or fp16 bit patterns).
+
+    Returns (q uint8 [M,K], s) with s float32 [G, Mp] (fp32 mode) or uint32
+    [ceil(G/4), Mp] (UE8M0 packed mode), both column-major in the sense
+    that a group's scales for consecutive rows are contiguous.
+    """
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    G = K // group
+    Mp = (M + 3) // 4 * 4
+    q = np.empty((M, K), dtype=np.uint8)
+    if ue8m0:
+        s = np.empty(((G + 3) // 4, Mp), dtype=np.uint32)
+    else:
+        s = np.empty((G, Mp), dtype=np.float32)
+    rc = lib().oracle_quant_act(_ptr(x_bits), x_dtype, M, K, group, int(bool(ue8m0)),
+                                _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quant_act: bad arguments")
+    return q, s
+
+
+def quant_weight(w: np.ndarray, w_dtype: int, bn: int = 128, bk: int = 128, ue8m0: bool = False):
+    """w: [N,K] float32 (w_dtype FP32) or uint16 bit patterns (BF16/FP16)."""
+    w = np.ascontiguousarray(w)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.uint8)
+    s = np.empty(((N + bn - 1) // bn, K // bk), dtype=np.float32)
+    rc = lib().oracle_quant_weight(_ptr(w), w_dtype, N, K, bn, bk, int(bool(ue8m0)),
+                                   _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quant_weight: bad arguments")
+    return q, s
+
+
+def act_scale(s: np.ndarray, ue8m0: bool, M: int, K: int, group: int, m: int, g: int) -> float:
+    return lib().oracle_act_scale(_ptr(s), int(bool(ue8m0)), M, K, group, m, g)
+
+
+# -------------------------------------------------------------------- GEMM --
+
+def gemm(qa, sa, qw, sw, ue8m0: bool, group: int = 128, bn: int = 128, bk: int = 128,
+         rows=None) -> np.ndarray:
+    """fp64 reference [M,N] (or the row range ``rows=(row0, count)``)."""
+    M, K = qa.shape
+    N = qw.shape[0]
+    row0, cnt = (0, M) if rows is None else rows
+    out = np.empty((cnt, N), dtype=np.float64)
+    rc = lib().oracle_gemm(M, N, K, _ptr(qa), _ptr(sa), int(bool(ue8m0)), _ptr(qw), _ptr(sw),
+                           group, bn, bk, row0, cnt, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_gemm: bad arguments")
+    return out
+
+
+def gemm_elem(qa, sa, qw, sw, ue8m0: bool, m: int, n: int, group: int = 128, bn: int = 128,
+              bk: int = 128) -> float:
+    M, K = qa.shape
+    N = qw.shape[0]
+    return lib().oracle_gemm_elem(M, N, K, _ptr(qa), _ptr(sa), int(bool(ue8m0)), _ptr(qw),
+                                  _ptr(sw), group, bn, bk, m, n)
+
+
+def calc_diff(x: np.ndarray, y: np.ndarray) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float64).ravel()
+    y = np.ascontiguousarray(y, dtype=np.float64).ravel()
+    return lib().oracle_calc_diff(_ptr(x), _ptr(y), x.size)

@@ -1,0 +1,103 @@
+/*
+ * oracle.h -- plain, slow, single-threaded CPU reference of the W8A8 block-FP8
+ * linear path (per-token-group activation quant, 128x128 weight block quant,
+ * block-scaled GEMM accumulated in fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or
+ * calls this code; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant generator with
+ * the CUDA path.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [DG]  "vLLM DeepGEMM FP8 Block GEMM 基准测试：DeepSeek DeepGEMM 对比 Triton 与
+ *          CUTLASS 的块量化 GEMM 内核解析" (blog.gitcode.com), §4.1 (quant layouts:
+ *          per_block_cast_to_fp8, per_token_group_quant_fp8), §4.2 (the Triton
+ *          kernel's per-K-block scale multiply), §4.3 (metrics), §4.4 (calc_diff).
+ *   [PR]  "vllm-project/vllm PR 42153" (prhub.com.cn), 实现拆解 (the packed
+ *          UE8M0 per-token-group quant kernel: eps, min/max 8-bit bounds,
+ *          packed int32 scales, TMA-aligned rows).
+ *   [CFG] "vLLM 量化 Kernel 配置机制" (blog.gitcode.com), §2 (M grid).
+ * Readings of points the pages leave open (eps = 1e-10, fp8 max = 448,
+ * IEEE division x/s, ceil on the fp32-rounded scale, biased-exponent UE8M0
+ * byte, little-endian packing, zero padding) are listed in the design notes;
+ * each function below states the one it uses.
+ *
+ * Parity status: every function here is pinned by tests under tests/ that do
+ * not call the function's own formula (brute force, exact rationals, closed
+ * forms, invariants, library special cases).  calc_diff is pinned only by its
+ * closed-form special cases; the pages' printed 0.000684 depends on their RNG
+ * and is not reproducible (parity unpinned for that one number).
+ */
+#ifndef FP8BQ_ORACLE_H
+#define FP8BQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes for raw 16/32-bit inputs */
+enum { ORACLE_BF16 = 0, ORACLE_FP16 = 1, ORACLE_FP32 = 2 };
+
+/* OCP FP8 E4M3 ("e4m3fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, largest finite 448.  decode() returns the
+ * exact value (NaN for 0x7F/0xFF). */
+double oracle_e4m3_decode(uint8_t code);
+/* Round-to-nearest-even of a finite fp32 value with |y| <= 448 (callers clamp
+ * first, see oracle_quant_value); the sign of zero is kept (-0 -> 0x80). */
+uint8_t oracle_e4m3_encode(float y);
+
+float oracle_bf16_to_f32(uint16_t bits);
+float oracle_f16_to_f32(uint16_t bits);
+
+/* Scale of one group/block from its amax: s = fp32(max(amax, 1e-10) / 448);
+ * with ue8m0 != 0, s is rounded up to the next power of two (2^ceil(log2 s)),
+ * computed on the fp32 bits of s.  [DG §4.1], [PR 实现拆解]. */
+float oracle_group_scale(float amax, int ue8m0);
+/* code of one element: e4m3_rne(clamp(fp32(x / s), -448, 448)). */
+uint8_t oracle_quant_value(float x, float s);
+
+/* Bytes of the activation-scale buffer: Mp = ceil(M/4)*4 rows;
+ * fp32: 4*G*Mp; ue8m0 packed: 4*ceil(G/4)*Mp.  G = K/group. */
+int64_t oracle_act_scale_bytes(int64_t M, int64_t K, int group, int ue8m0);
+
+/* Per-token-group activation quant.  x: [M,K] row-major bf16/fp16 bits.
+ * q: [M,K] e4m3 codes.  s: column-major scales, element (g, m) at g*Mp + m
+ * (fp32 mode) or byte (g%4) of u32 word (g/4)*Mp + m (ue8m0 mode; byte =
+ * biased fp32 exponent of the power-of-two scale).  Rows m in [M, Mp) and
+ * unused bytes of the last word are 0.  Returns 0, or -1 on bad arguments. */
+int oracle_quant_act(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int group,
+                     int ue8m0, uint8_t* q, void* s);
+
+/* 128x128 weight block quant.  w: [N,K] row-major (fp32, bf16 or fp16).
+ * q: [N,K] codes; s: fp32 [ceil(N/bn)][K/bk] row-major.  A partial last row
+ * block takes its amax over the rows that exist.  [DG §4.1] */
+int oracle_quant_weight(const void* w, int w_dtype, int64_t N, int64_t K, int bn, int bk,
+                        int ue8m0, uint8_t* q, float* s);
+
+/* Activation scale (m, g) decoded to a double (fp32 value or 2^(byte-127)). */
+double oracle_act_scale(const void* s, int ue8m0, int64_t M, int64_t K, int group,
+                        int64_t m, int64_t g);
+
+/* Block-scaled GEMM, exact-in-fp64 slab sums:
+ *   ref[m,n] = sum_kb sa[m,kb] * sw[n/bn,kb] * S_kb,
+ *   S_kb     = sum_{k in slab kb} dec(qa[m,k]) * dec(qw[n,k])
+ * accumulated in fp64 in the order kb = 0..G-1 ([DG §4.2]: each K block's
+ * dot product is multiplied by the two scales and added to the accumulator).
+ * Rows [row0, row0+rows) of the [M,N] result are written to out (rows x N). */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const void* sa, int ue8m0,
+                const uint8_t* qw, const float* sw, int group, int bn, int bk,
+                int64_t row0, int64_t rows, double* out);
+/* One element of the same result. */
+double oracle_gemm_elem(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const void* sa,
+                        int ue8m0, const uint8_t* qw, const float* sw, int group, int bn, int bk,
+                        int64_t m, int64_t n);
+
+/* calc_diff of [DG §4.4]: 1 - 2*sum(x*y) / sum(x*x + y*y), in fp64. */
+double oracle_calc_diff(const double* x, const double* y, int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
