@@ -2,14 +2,5 @@
 
 The compute path is the C-ABI library ``libfp8bq.so`` (hand-written CUDA);
 ``block_scaled_fp8_group_gb300.fp8bq`` is its thin Python binding.  This file
-imports nothing heavy so that ``synth`` can be used without the library.
+imports nothing heavy, so ``synth`` can be used without the library.
 """
-
-__all__ = ["fp8bq", "synth"]
-
-
-def __getattr__(name):
-    if name == "fp8bq":
-        from . import fp8bq as _m
-        return _m
-    raise AttributeError(name)

@@ -1,0 +1,571 @@
+// api.cu -- the extern "C" entry points of libfp8bq: argument checks, the
+// per-shape variant table, the device status word, and the launches.
+#include <dlfcn.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <string>
+#include <tuple>
+
+#include "internal.h"
+
+namespace fp8bq {
+
+// ------------------------------------------------------- device state
+
+// Status word the kernels' bounded waits write on time-out.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int ready = 0;
+    int supported = 0;
+    int num_sms = 0;
+    int* status = nullptr;  // device address of g_status_word
+    std::string name;       // spaces replaced by '_'
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+fp8bq_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BQ_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return FP8BQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BQ_ERR_CUDA;
+        }
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BQ_ERR_CUDA;
+        }
+        d.status = static_cast<int*>(p);
+        d.num_sms = prop.multiProcessorCount;
+        d.supported = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+        d.name = prop.name;
+        for (char& c : d.name)
+            if (c == ' ') c = '_';
+        d.ready = 1;
+    }
+    *out = &d;
+    return d.supported ? FP8BQ_OK : FP8BQ_ERR_UNSUPPORTED;
+}
+
+uint64_t wait_timeout_ns() {
+    static uint64_t ns = [] {
+        const char* e = std::getenv("FP8BQ_WAIT_TIMEOUT_MS");
+        double ms = e ? std::atof(e) : 2000.0;
+        if (!(ms > 0.0)) ms = 2000.0;
+        return static_cast<uint64_t>(ms * 1e6);
+    }();
+    return ns;
+}
+
+fp8bq_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return FP8BQ_OK;
+    cudaGetLastError();  // clear the sticky-free error state for the next call
+    return FP8BQ_ERR_LAUNCH;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// ------------------------------------------------------- variant table
+//
+// Text file, one entry per line:  N K fmt out M kind block_n split grid
+// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap).  Per
+// (N, K, fmt, out) the entries form an M grid; a lookup takes the grid point
+// nearest to M, the smaller one on a tie ("vLLM 量化 Kernel 配置机制" §4.2:
+// configs[min(keys, key=|x - M|)], e.g. M=37 -> 32, M=2050 -> 2048).
+
+using TableKey = std::tuple<int64_t, int64_t, int, int>;  // N, K, fmt, out
+
+struct Table {
+    bool loaded = false;
+    std::string path;
+    std::map<TableKey, std::map<int64_t, fp8bq_variant>> rows;
+    std::set<TableKey> logged;
+};
+
+std::mutex g_table_mutex;
+Table g_table;
+
+std::string library_dir() {
+    Dl_info info;
+    if (dladdr(reinterpret_cast<void*>(&library_dir), &info) && info.dli_fname) {
+        std::string p = info.dli_fname;
+        size_t cut = p.find_last_of('/');
+        if (cut != std::string::npos) return p.substr(0, cut);
+    }
+    return ".";
+}
+
+std::string table_path(const std::string& device_name) {
+    const char* e = std::getenv("FP8BQ_TABLE");
+    if (e && *e) return e;
+    if (device_name.empty()) return std::string();
+    return library_dir() + "/../tables/" + device_name + ".tbl";
+}
+
+int parse_fmt(const char* s) {
+    if (!std::strcmp(s, "fp32")) return FP8BQ_SCALE_FP32;
+    if (!std::strcmp(s, "ue8m0")) return FP8BQ_SCALE_UE8M0;
+    return -1;
+}
+int parse_out(const char* s) {
+    if (!std::strcmp(s, "bf16")) return FP8BQ_BF16;
+    if (!std::strcmp(s, "fp16")) return FP8BQ_FP16;
+    if (!std::strcmp(s, "fp32")) return FP8BQ_FP32;
+    return -1;
+}
+int parse_kind(const char* s) {
+    if (!std::strcmp(s, "normal")) return FP8BQ_KIND_NORMAL;
+    if (!std::strcmp(s, "swap")) return FP8BQ_KIND_SWAP_AB;
+    return -1;
+}
+
+void load_table_locked(const std::string& device_name) {
+    g_table.rows.clear();
+    g_table.logged.clear();
+    g_table.path = table_path(device_name);
+    g_table.loaded = true;
+    if (g_table.path.empty()) return;
+    FILE* f = std::fopen(g_table.path.c_str(), "r");
+    if (!f) return;  // a missing table only costs speed
+    char line[512];
+    while (std::fgets(line, sizeof line, f)) {
+        char* hash = std::strchr(line, '#');
+        if (hash) *hash = 0;
+        long long N, K, M;
+        char fmt[16], out[16], kind[16];
+        int bn, split, grid;
+        if (std::sscanf(line, "%lld %lld %15s %15s %lld %15s %d %d %d", &N, &K, fmt, out, &M, kind,
+                        &bn, &split, &grid) != 9)
+            continue;  // blank or malformed line: skipped
+        const int ifmt = parse_fmt(fmt), iout = parse_out(out), ikind = parse_kind(kind);
+        if (ifmt < 0 || iout < 0 || ikind < 0 || M < 0) continue;
+        fp8bq_variant v = {};
+        v.kind = ikind;
+        v.block_n = bn;
+        v.split = split;
+        v.grid = grid;
+        v.from_table = 1;
+        g_table.rows[TableKey(N, K, ifmt, iout)][M] = v;
+    }
+    std::fclose(f);
+}
+
+// Default variant when the table has no entry (speed only, never correctness;
+// "vLLM 量化 Kernel 配置机制" §4.1).  Swap-AB below 129 tokens, otherwise the
+// normal orientation with 256-wide weight tiles; the K split is the one that
+// minimises (slabs on the busiest CTA) + a small per-split penalty.
+fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
+    fp8bq_variant v = {};
+    const int64_t G = K / 128;
+    int64_t tiles;
+    if (M <= 128) {
+        v.kind = FP8BQ_KIND_SWAP_AB;
+        v.block_n = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        tiles = ((N + 127) / 128) * ((M + v.block_n - 1) / v.block_n);
+    } else {
+        v.kind = FP8BQ_KIND_NORMAL;
+        v.block_n = N >= 256 ? 256 : 128;
+        tiles = ((N + v.block_n - 1) / v.block_n) * ((M + 127) / 128);
+    }
+    const int64_t max_split = G < 16 ? G : 16;
+    double best = 1e300;
+    int best_s = 1;
+    for (int s = 1; s <= max_split; ++s) {
+        const int64_t items = tiles * s;
+        const int64_t waves = (items + num_sms - 1) / num_sms;
+        const double slabs = static_cast<double>(waves) * static_cast<double>((G + s - 1) / s);
+        const double penalty = (s > 1 ? 1.0 : 0.0) * (M <= 128 ? 0.5 : 4.0) * s;
+        if (slabs + penalty < best) {
+            best = slabs + penalty;
+            best_s = s;
+        }
+    }
+    v.split = best_s;
+    v.grid = 0;
+    v.from_table = 0;
+    return v;
+}
+
+fp8bq_variant select_variant(int64_t M, int64_t N, int64_t K, int fmt, int out,
+                             const std::string& device_name, int num_sms) {
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    if (!g_table.loaded) load_table_locked(device_name);
+    const TableKey key(N, K, fmt, out);
+    auto it = g_table.rows.find(key);
+    if (it != g_table.rows.end() && !it->second.empty()) {
+        const fp8bq_variant* best = nullptr;
+        int64_t best_d = 0;
+        for (const auto& kv : it->second) {  // ascending M: strict '<' keeps the smaller on ties
+            const int64_t d = kv.first > M ? kv.first - M : M - kv.first;
+            if (!best || d < best_d) {
+                best = &kv.second;
+                best_d = d;
+            }
+        }
+        return *best;
+    }
+    if (g_table.logged.insert(key).second) {
+        const char* e = std::getenv("FP8BQ_LOG");
+        if (e && std::atoi(e) == 1)
+            std::fprintf(stderr,
+                         "fp8bq: no table entry for N=%lld K=%lld fmt=%d out=%d (table %s); "
+                         "using the default variant\n",
+                         static_cast<long long>(N), static_cast<long long>(K), fmt, out,
+                         g_table.path.empty() ? "<none>" : g_table.path.c_str());
+    }
+    return default_variant(M, N, K, num_sms);
+}
+
+// ------------------------------------------------------- argument checks
+
+constexpr int64_t kMaxDim = (1LL << 31) - 4096;
+
+fp8bq_status check_gemm_args(int64_t M, int64_t N, int64_t K, int fmt, int out_dtype) {
+    if (M < 0 || N < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (fmt != FP8BQ_SCALE_FP32 && fmt != FP8BQ_SCALE_UE8M0) return FP8BQ_ERR_INVALID_ARG;
+    if (out_dtype != FP8BQ_BF16 && out_dtype != FP8BQ_FP16 && out_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_INVALID_ARG;
+    if (K == 0 || K % 128 != 0 || N % 64 != 0) return FP8BQ_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    return FP8BQ_OK;
+}
+
+fp8bq_status check_gemm_ptrs(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
+                             const void* out) {
+    if (!a_q || !a_s || !w_q || !w_s || !out) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(w_q) || !aligned16(w_s) ||
+        !aligned16(out))
+        return FP8BQ_ERR_ALIGNMENT;
+    return FP8BQ_OK;
+}
+
+fp8bq_status check_ws(const GemmPlan& plan, const void* ws, size_t ws_bytes) {
+    if (plan.ws_bytes == 0) return FP8BQ_OK;
+    if (!ws || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return FP8BQ_ERR_WORKSPACE;
+    return FP8BQ_OK;
+}
+
+fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, const void* a_q,
+                      const void* a_s, const void* w_q, const float* w_s, int fmt, int out_dtype,
+                      void* out, void* ws, size_t ws_data_offset, DeviceInfo* d, int pdl,
+                      cudaStream_t stream) {
+    GemmLaunch g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.a_q = a_q;
+    g.a_s = a_s;
+    g.w_q = w_q;
+    g.w_s = w_s;
+    g.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    g.out_dtype = out_dtype;
+    g.out = out;
+    g.workspace = ws;
+    g.ws_data_offset = ws_data_offset;
+    g.status = d->status;
+    g.timeout_ns = wait_timeout_ns();
+    g.pdl = pdl;
+    return from_cuda(launch_gemm(plan, g, stream));
+}
+
+}  // namespace
+}  // namespace fp8bq
+
+using namespace fp8bq;
+
+// =========================================================== C ABI
+
+extern "C" {
+
+int fp8bq_abi_version(void) { return 1; }
+
+const char* fp8bq_status_string(fp8bq_status s) {
+    switch (s) {
+        case FP8BQ_OK: return "ok";
+        case FP8BQ_ERR_INVALID_ARG: return "invalid argument";
+        case FP8BQ_ERR_SHAPE: return "unsupported shape (K must be a positive multiple of 128, N of 64)";
+        case FP8BQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case FP8BQ_ERR_UNSUPPORTED: return "unsupported group/block size, dtype or GPU";
+        case FP8BQ_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case FP8BQ_ERR_LAUNCH: return "kernel launch failed";
+        case FP8BQ_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
+        case FP8BQ_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+size_t fp8bq_act_scale_bytes(int64_t M, int64_t K, int group, fp8bq_scale_fmt fmt) {
+    if (M < 0 || K <= 0 || group != kGroup || K % group) return 0;
+    if (fmt != FP8BQ_SCALE_FP32 && fmt != FP8BQ_SCALE_UE8M0) return 0;
+    const int64_t G = K / group;
+    const int64_t cols = fmt == FP8BQ_SCALE_UE8M0 ? (G + 3) / 4 : G;
+    return static_cast<size_t>(4 * cols * pad_rows4(M));
+}
+
+size_t fp8bq_weight_scale_bytes(int64_t N, int64_t K, int block_n, int block_k) {
+    if (N < 0 || K <= 0 || block_n != kGroup || block_k != kGroup || K % block_k) return 0;
+    return static_cast<size_t>(4 * ((N + block_n - 1) / block_n) * (K / block_k));
+}
+
+size_t fp8bq_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, const fp8bq_variant* v) {
+    if (!v || check_gemm_args(M, N, K, FP8BQ_SCALE_FP32, FP8BQ_BF16) != FP8BQ_OK) return 0;
+    if (M == 0 || N == 0) return 0;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *v, 152, &plan)) return 0;
+    return plan.ws_bytes;
+}
+
+fp8bq_status fp8bq_select_variant(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                  fp8bq_dtype out_dtype, fp8bq_variant* variant) {
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    fp8bq_status st = check_gemm_args(M, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    std::string name;
+    int sms = 152;  // GB300 when no GPU is visible (host-only queries)
+    if (device_info(&d) == FP8BQ_OK) {
+        name = d->name;
+        sms = d->num_sms;
+    }
+    *variant = select_variant(M, N, K, fmt, out_dtype, name, sms);
+    return FP8BQ_OK;
+}
+
+fp8bq_status fp8bq_reload_table(void) {
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    g_table.loaded = false;
+    return FP8BQ_OK;
+}
+
+size_t fp8bq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                  fp8bq_dtype out_dtype) {
+    fp8bq_variant v;
+    if (fp8bq_select_variant(M, N, K, fmt, out_dtype, &v) != FP8BQ_OK) return 0;
+    return fp8bq_variant_workspace_bytes(M, N, K, &v);
+}
+
+size_t fp8bq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                    fp8bq_dtype out_dtype) {
+    if (check_gemm_args(M, N, K, fmt, out_dtype) != FP8BQ_OK) return 0;
+    const size_t g = fp8bq_gemm_workspace_bytes(M, N, K, fmt, out_dtype);
+    return kCounterRegion + align256(static_cast<size_t>(M * K)) +
+           align256(fp8bq_act_scale_bytes(M, K, kGroup, fmt)) + (g ? g - kCounterRegion : 0);
+}
+
+fp8bq_status fp8bq_quant_act(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t K, int group,
+                             fp8bq_scale_fmt fmt, void* q, void* s, cudaStream_t stream) {
+    if (M < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (fmt != FP8BQ_SCALE_FP32 && fmt != FP8BQ_SCALE_UE8M0) return FP8BQ_ERR_INVALID_ARG;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (group != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (K == 0 || K % kGroup != 0 || K > kMaxDim || M > kMaxDim) return FP8BQ_ERR_SHAPE;
+    if (M == 0) return FP8BQ_OK;
+    if (!x || !q || !s) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return FP8BQ_ERR_ALIGNMENT;
+    if ((K / kGroup + 3) / 4 > 65535) return FP8BQ_ERR_SHAPE;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    QuantActArgs a;
+    a.x = x;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.M = M;
+    a.Mp = pad_rows4(M);
+    a.K = K;
+    a.G = static_cast<int>(K / kGroup);
+    a.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    a.fp16 = x_dtype == FP8BQ_FP16;
+    a.pdl_trigger = 0;
+    return from_cuda(launch_quant_act(a, stream));
+}
+
+fp8bq_status fp8bq_quant_weight(const void* w, fp8bq_dtype w_dtype, int64_t N, int64_t K,
+                                int block_n, int block_k, fp8bq_scale_fmt fmt, void* q, float* s,
+                                cudaStream_t stream) {
+    if (N < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (fmt != FP8BQ_SCALE_FP32 && fmt != FP8BQ_SCALE_UE8M0) return FP8BQ_ERR_INVALID_ARG;
+    if (w_dtype != FP8BQ_BF16 && w_dtype != FP8BQ_FP16 && w_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_UNSUPPORTED;
+    if (block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (K == 0 || K % kGroup != 0 || K > kMaxDim || N > kMaxDim) return FP8BQ_ERR_SHAPE;
+    if ((N + kGroup - 1) / kGroup > 65535) return FP8BQ_ERR_SHAPE;
+    if (N == 0) return FP8BQ_OK;
+    if (!w || !q || !s) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s)) return FP8BQ_ERR_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    QuantWeightArgs a;
+    a.w = w;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.N = N;
+    a.K = K;
+    a.NB = static_cast<int>((N + kGroup - 1) / kGroup);
+    a.KB = static_cast<int>(K / kGroup);
+    a.dtype = w_dtype;
+    a.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    return from_cuda(launch_quant_weight(a, stream));
+}
+
+fp8bq_status fp8bq_gemm_variant(int64_t M, int64_t N, int64_t K, const void* a_q, const void* a_s,
+                                const void* w_q, const float* w_s, fp8bq_scale_fmt fmt,
+                                fp8bq_dtype out_dtype, void* out, const fp8bq_variant* variant,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_gemm_args(M, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *variant, d->num_sms, &plan)) return FP8BQ_ERR_UNSUPPORTED;
+    st = check_ws(plan, workspace, workspace_bytes);
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, workspace, 0, d, 0,
+                    stream);
+}
+
+fp8bq_status fp8bq_gemm(int64_t M, int64_t N, int64_t K, const void* a_q, const void* a_s,
+                        const void* w_q, const float* w_s, int group, int block_n, int block_k,
+                        fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_gemm_args(M, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = select_variant(M, N, K, fmt, out_dtype, d->name, d->num_sms);
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan)) return FP8BQ_ERR_UNSUPPORTED;
+    st = check_ws(plan, workspace, workspace_bytes);
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, workspace, 0, d, 0,
+                    stream);
+}
+
+fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N, int64_t K,
+                          const void* w_q, const float* w_s, int group, int block_n, int block_k,
+                          fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_gemm_args(M, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    if (!x) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(x)) return FP8BQ_ERR_ALIGNMENT;
+    st = check_gemm_ptrs(x, x, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8BQ_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = select_variant(M, N, K, fmt, out_dtype, d->name, d->num_sms);
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan)) return FP8BQ_ERR_UNSUPPORTED;
+    // workspace: [counter prefix][codes][scales][split-K partials]; the GEMM
+    // sees a workspace whose prefix is the counters and whose partials follow
+    // the scales, so it is passed as a base pointer with the data shifted.
+    const size_t q_bytes = align256(static_cast<size_t>(M * K));
+    const size_t s_bytes = align256(fp8bq_act_scale_bytes(M, K, kGroup, fmt));
+    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
+    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
+        return FP8BQ_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* a_q = base + kCounterRegion;
+    void* a_s = base + kCounterRegion + q_bytes;
+
+    QuantActArgs qa;
+    qa.x = x;
+    qa.q = static_cast<uint8_t*>(a_q);
+    qa.s = a_s;
+    qa.M = M;
+    qa.Mp = pad_rows4(M);
+    qa.K = K;
+    qa.G = static_cast<int>(K / kGroup);
+    qa.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    qa.fp16 = x_dtype == FP8BQ_FP16;
+    qa.pdl_trigger = 1;
+    st = from_cuda(launch_quant_act(qa, stream));
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, base,
+                    q_bytes + s_bytes, d, 1, stream);
+}
+
+fp8bq_status fp8bq_device_status(int* code, cudaStream_t stream) {
+    if (!code) return FP8BQ_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpyAsync(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyAsync(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BQ_ERR_CUDA;
+    }
+    *code = v;
+    return FP8BQ_OK;
+}
+
+fp8bq_status fp8bq_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns == 0 || timeout_ns > 10ull * 1000 * 1000 * 1000) return FP8BQ_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    return from_cuda(launch_wait_selftest(d->status, timeout_ns, stream));
+}
+
+}  // extern "C"
+
+namespace fp8bq {
+
+EncodeTiledFn get_encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<EncodeTiledFn>(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+}  // namespace fp8bq

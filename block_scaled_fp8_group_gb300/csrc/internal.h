@@ -1,0 +1,97 @@
+// internal.h -- declarations shared by the library's translation units (not
+// part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fp8bq.h"
+
+namespace fp8bq {
+
+constexpr int kGroup = 128;  // activation group / weight block edge
+constexpr float kEps = 1e-10f;
+constexpr float kFp8Max = 448.0f;
+
+inline int64_t pad_rows4(int64_t m) { return (m + 3) / 4 * 4; }
+
+// Every workspace starts with this many bytes of split-K tile counters.  The
+// region must be zero before first use and every call leaves it zero, so one
+// workspace can serve calls of any shape in turn (data goes after it).
+constexpr size_t kCounterRegion = 65536;
+
+// ---------------------------------------------------------------- quant
+
+struct QuantActArgs {
+    const void* x;
+    uint8_t* q;
+    void* s;
+    int64_t M;   // rows
+    int64_t Mp;  // rows rounded up to a multiple of 4
+    int64_t K;
+    int G;       // groups per row
+    int ue8m0;
+    int fp16;    // input is fp16 (else bf16)
+    int pdl_trigger;  // signal a programmatic dependent launch early
+};
+cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream);
+
+struct QuantWeightArgs {
+    const void* w;
+    uint8_t* q;
+    float* s;
+    int64_t N, K;
+    int NB, KB;
+    int dtype;  // fp8bq_dtype
+    int ue8m0;
+};
+cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream);
+
+// ----------------------------------------------------------------- GEMM
+
+struct GemmPlan {
+    int kind;      // fp8bq_kind
+    int bn;        // MMA N
+    int split;     // K splits per tile
+    int grid;      // CTAs
+    int tiles_tok; // token tiles
+    int tiles_w;   // weight tiles
+    int num_items; // tiles * split
+    size_t ws_bytes;
+};
+
+// Fills the derived fields of a plan for (M, N, K) and the chosen variant;
+// returns false if the variant is not supported.
+bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
+                    GemmPlan* plan);
+
+struct GemmLaunch {
+    int64_t M, N, K;
+    const void* a_q;
+    const void* a_s;
+    const void* w_q;
+    const float* w_s;
+    int ue8m0;
+    int out_dtype;
+    void* out;
+    void* workspace;        // counter prefix at offset 0
+    size_t ws_data_offset;  // partials start at kCounterRegion + this offset
+    int* status;
+    uint64_t timeout_ns;
+    int pdl;  // launched as a programmatic dependent of the previous kernel
+};
+cudaError_t launch_gemm(const GemmPlan& plan, const GemmLaunch& g, cudaStream_t stream);
+
+// Bounded-wait self test (one CTA, one thread).
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace fp8bq

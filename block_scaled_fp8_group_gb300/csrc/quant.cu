@@ -1,0 +1,265 @@
+// quant.cu -- per-token-group activation quant and 128x128 weight block quant.
+//
+// Method ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.1; "vllm-project/vllm PR
+// 42153" 实现拆解): per group amax, s = max(amax, 1e-10)/448 (rounded up to a
+// power of two for UE8M0), codes = e4m3 round-to-nearest-even of
+// clamp(x/s, +-448).  Both kernels are HBM streams on the CUDA cores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bq {
+
+namespace {
+
+// Power-of-two round-up of a positive normal fp32 scale, on its bits.
+__device__ __forceinline__ float ceil_pow2(float s) {
+    uint32_t u = __float_as_uint(s);
+    uint32_t e = (u >> 23) & 0xFFu;
+    if (u & 0x7FFFFFu) e += 1u;
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ float group_scale(float amax, int ue8m0) {
+    float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+    return ue8m0 ? ceil_pow2(s) : s;
+}
+
+// Two fp32 values -> two e4m3 codes (low byte = first), saturating RNE.
+__device__ __forceinline__ uint32_t cvt2_e4m3(float a, float b) {
+    a = fminf(fmaxf(a, -kFp8Max), kFp8Max);
+    b = fminf(fmaxf(b, -kFp8Max), kFp8Max);
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                          __NV_E4M3));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// -------------------------------------------------------- activation quant
+//
+// One warp owns 4 consecutive groups (512 elements, 1 KB of bf16) of one row:
+// lane l holds elements [16 l, 16 l + 16) of that span, i.e. lanes 8j..8j+7
+// hold group j.  The group amax is a 3-step xor shuffle inside those 8 lanes,
+// and the 4 UE8M0 exponents of the warp form exactly one packed u32 word, so
+// packing needs no traffic between warps.
+//
+// 2D grid without runtime division: blockIdx.x picks kRows rows (one per
+// warp), blockIdx.y picks the 4-group column; every index below is a product
+// or sum of those with compile-time constants.
+constexpr int kQuantRows = 8;  // warps per CTA = rows per CTA
+
+template <bool kFp16>
+__global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantActArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantRows + (threadIdx.x >> 5);
+    const int quad = blockIdx.y;             // 4-group column index
+    const int g = quad * 4 + (lane >> 3);    // this lane's group
+    const bool active = row < a.M && g < a.G;
+
+    if (a.pdl_trigger) pdl_launch_dependents();
+    if (row >= a.Mp) return;
+
+    const int64_t off = row * a.K + static_cast<int64_t>(quad) * 512 + lane * 16;
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + off);
+        v0 = __ldcs(src);
+        v1 = __ldcs(src + 1);
+    }
+    float f[16];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = kFp16 ? f16_lo(w[i]) : bf16_lo(w[i]);
+        f[2 * i + 1] = kFp16 ? f16_hi(w[i]) : bf16_hi(w[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    const float s = group_scale(amax, a.ue8m0);
+
+    if (active) {
+        uint32_t c[8];
+        if (a.ue8m0) {
+            // s = 2^e exactly, so x * (1/s) is the same correctly rounded
+            // value as x / s.
+            const float r = __fdiv_rn(1.0f, s);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = cvt2_e4m3(f[2 * i] * r, f[2 * i + 1] * r);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                c[i] = cvt2_e4m3(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+        }
+        uint4 out;
+        out.x = c[0] | (c[1] << 16);
+        out.y = c[2] | (c[3] << 16);
+        out.z = c[4] | (c[5] << 16);
+        out.w = c[6] | (c[7] << 16);
+        *reinterpret_cast<uint4*>(a.q + off) = out;
+    }
+
+    // Scales: padding rows (row >= M) and groups past G store 0.
+    if (a.ue8m0) {
+        const uint32_t byte = (row < a.M && g < a.G) ? ((__float_as_uint(s) >> 23) & 0xFFu) : 0u;
+        const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, byte, 0);
+        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, 8);
+        const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, 16);
+        const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, 24);
+        if (lane == 0)
+            static_cast<uint32_t*>(a.s)[static_cast<int64_t>(quad) * a.Mp + row] =
+                b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    } else if ((lane & 7) == 0 && g < a.G) {
+        static_cast<float*>(a.s)[static_cast<int64_t>(g) * a.Mp + row] = row < a.M ? s : 0.0f;
+    }
+}
+
+// ------------------------------------------------------------ weight quant
+//
+// One CTA per 128x128 block; 256 threads, thread t covers columns
+// 16*(t%8) .. +16 of rows t/8 + 32*i (i = 0..3).  The block amax is a warp
+// shuffle reduction followed by a shared-memory one across the 8 warps.
+template <typename T>
+__device__ __forceinline__ void load16(const T* p, float (&f)[16]);
+
+template <>
+__device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
+    const float4* s = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float4 v = s[i];
+        f[4 * i] = v.x;
+        f[4 * i + 1] = v.y;
+        f[4 * i + 2] = v.z;
+        f[4 * i + 3] = v.w;
+    }
+}
+
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[16]) {
+    const uint4* s = reinterpret_cast<const uint4*>(p);
+    uint4 v0 = s[0], v1 = s[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+    }
+}
+
+template <>
+__device__ __forceinline__ void load16<__half>(const __half* p, float (&f)[16]) {
+    const uint4* s = reinterpret_cast<const uint4*>(p);
+    uint4 v0 = s[0], v1 = s[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = f16_lo(w[i]);
+        f[2 * i + 1] = f16_hi(w[i]);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs a) {
+    __shared__ float warp_max[8];
+    const int t = threadIdx.x;
+    const int kb = blockIdx.x, nb = blockIdx.y;
+    const int64_t col = static_cast<int64_t>(kb) * kGroup + (t & 7) * 16;
+    const T* w = static_cast<const T*>(a.w);
+
+    float f[4][16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t n = static_cast<int64_t>(nb) * kGroup + (t >> 3) + 32 * i;
+        if (n < a.N) {
+            load16<T>(w + n * a.K + col, f[i]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[i][j]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((t & 31) == 0) warp_max[t >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    const float s = group_scale(amax, a.ue8m0);
+    if (t == 0) a.s[static_cast<int64_t>(nb) * a.KB + kb] = s;
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t n = static_cast<int64_t>(nb) * kGroup + (t >> 3) + 32 * i;
+        if (n >= a.N) continue;
+        uint32_t c[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            c[j] = cvt2_e4m3(__fdiv_rn(f[i][2 * j], s), __fdiv_rn(f[i][2 * j + 1], s));
+        uint4 out;
+        out.x = c[0] | (c[1] << 16);
+        out.y = c[2] | (c[3] << 16);
+        out.z = c[4] | (c[5] << 16);
+        out.w = c[6] | (c[7] << 16);
+        *reinterpret_cast<uint4*>(a.q + n * a.K + col) = out;
+    }
+}
+
+// ------------------------------------------------------ bounded-wait test
+
+__global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        // Nothing ever arrives on `bar`: the wait must give up by itself.
+        mbar_wait_bounded(&bar, 0, &abort_flag, status, timeout_ns,
+                          static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
+    const int quads = (a.G + 3) / 4;
+    dim3 grid(static_cast<unsigned>((a.Mp + kQuantRows - 1) / kQuantRows),
+              static_cast<unsigned>(quads));
+    if (a.fp16)
+        quant_act_kernel<true><<<grid, kQuantRows * 32, 0, stream>>>(a);
+    else
+        quant_act_kernel<false><<<grid, kQuantRows * 32, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream) {
+    dim3 grid(static_cast<unsigned>(a.KB), static_cast<unsigned>(a.NB));
+    if (a.dtype == FP8BQ_FP32)
+        quant_weight_kernel<float><<<grid, 256, 0, stream>>>(a);
+    else if (a.dtype == FP8BQ_BF16)
+        quant_weight_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
+    else
+        quant_weight_kernel<__half><<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bq

@@ -1,0 +1,214 @@
+/*
+ * fp8bq.h -- C ABI of the W8A8 block-FP8 linear path for GB300 (sm_103a).
+ *
+ * Two steps, as the pages describe them:
+ *   1. per-token-group activation quant: bf16/fp16 rows -> float8_e4m3fn codes
+ *      with one scale per 1x128 group, fp32 or UE8M0 (power of two, four
+ *      exponent bytes packed per int32), in a TMA-aligned column-major layout
+ *      ("vLLM DeepGEMM FP8 Block GEMM 基准测试", §4.1; "vllm-project/vllm PR
+ *      42153", 实现拆解);
+ *   2. a dense GEMM of those codes against weights quantised in 128x128
+ *      blocks, where each 128-wide K slab's partial sum is promoted by
+ *      sa[m,kb]*sw[nb,kb] into an fp32 accumulator and the result is written as
+ *      bf16, fp16 or fp32 ("vLLM DeepGEMM FP8 Block GEMM 基准测试", §4.2 and
+ *      §4.3; split-K and swap-AB variants: "用 Helion 为 vLLM 构建高性能可移植
+ *      线性后端", 内核实现).
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates device memory and never frees anything it is given.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
+ *     synchronise, except fp8bq_device_status.
+ *   - Errors are returned as fp8bq_status, never thrown or aborted on.  All
+ *     argument checks run on the host before any launch; a call that returns
+ *     an argument error has written nothing.
+ *   - Shapes: int64 sizes; M (tokens) >= 0 arbitrary, K a positive multiple of
+ *     128, N a multiple of 64 for the GEMM (the DeepGEMM dispatch predicate of
+ *     "vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.2: bf16 output, N % 64 == 0,
+ *     K % 128 == 0 -- fp16/fp32 outputs are accepted here as well).  M == 0 or
+ *     N == 0 is a no-op that returns FP8BQ_OK.
+ *   - Inputs must hold finite values; outputs for NaN/Inf inputs are
+ *     unspecified.
+ *   - Calls sharing one workspace must not overlap on the GPU (same stream, or
+ *     ordered by events).
+ */
+#ifndef FP8BQ_H
+#define FP8BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BQ_OK = 0,
+    FP8BQ_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum */
+    FP8BQ_ERR_SHAPE = 2,          /* K % 128 != 0 or K <= 0, N % 64 != 0, size overflow */
+    FP8BQ_ERR_ALIGNMENT = 3,      /* a pointer not 16-byte aligned */
+    FP8BQ_ERR_UNSUPPORTED = 4,    /* group/block != 128, dtype not accepted, GPU not sm_103 */
+    FP8BQ_ERR_WORKSPACE = 5,      /* workspace null or smaller than required */
+    FP8BQ_ERR_LAUNCH = 6,         /* the kernel launch itself failed */
+    FP8BQ_ERR_DEVICE_TIMEOUT = 7, /* a kernel's bounded wait gave up (see fp8bq_device_status) */
+    FP8BQ_ERR_CUDA = 8            /* another CUDA runtime error (no device, ...) */
+} fp8bq_status;
+
+typedef enum {
+    FP8BQ_SCALE_FP32 = 0,  /* one fp32 scale per group */
+    FP8BQ_SCALE_UE8M0 = 1  /* power-of-two scales; activation scales packed 4 per u32 */
+} fp8bq_scale_fmt;
+
+typedef enum { FP8BQ_BF16 = 0, FP8BQ_FP16 = 1, FP8BQ_FP32 = 2 } fp8bq_dtype;
+
+/* GEMM variant (kernel shape) -- what the per-shape table stores.
+ * "用 Helion 为 vLLM 构建高性能可移植线性后端", 内核实现: Standard, Split-K and
+ * Swap-AB exposed as tunable choices; "vLLM 量化 Kernel 配置机制" §4.2: per-M
+ * configs, nearest-M lookup. */
+typedef enum {
+    FP8BQ_KIND_NORMAL = 0, /* MMA M = 128 tokens, MMA N = block_n weight rows */
+    FP8BQ_KIND_SWAP_AB = 1 /* D^T = W A^T: MMA M = 128 weight rows, MMA N = block_n tokens */
+} fp8bq_kind;
+
+typedef struct {
+    int32_t kind;       /* fp8bq_kind */
+    int32_t block_n;    /* MMA N: swap-AB {16,32,64,128}; normal {128,256} */
+    int32_t split;      /* K splits per output tile, 1..64 (1 = no split-K) */
+    int32_t grid;       /* CTAs to launch; 0 = one per SM, capped by the work items */
+    int32_t from_table; /* output of fp8bq_select_variant: 1 = measured table, 0 = default */
+    int32_t reserved;
+} fp8bq_variant;
+
+/* ------------------------------------------------------------ size queries */
+
+/* Bytes of the activation scale buffer for an [M,K] input with 1 x `group`
+ * groups (G = K/group): rows are padded to Mp = ceil(M/4)*4 (TMA-aligned);
+ * FP32: 4*G*Mp bytes, element (g, m) at float index g*Mp + m;
+ * UE8M0: 4*ceil(G/4)*Mp bytes, group g of row m in byte (g%4) of the u32 at
+ * index (g/4)*Mp + m (byte = biased fp32 exponent of the scale, 127 = 1.0).
+ * Returns 0 on invalid arguments. */
+size_t fp8bq_act_scale_bytes(int64_t M, int64_t K, int group, fp8bq_scale_fmt fmt);
+
+/* Bytes of the weight scale buffer: fp32 [ceil(N/block_n)][K/block_k]. */
+size_t fp8bq_weight_scale_bytes(int64_t N, int64_t K, int block_n, int block_k);
+
+/* Workspace bytes fp8bq_gemm needs for this shape (0 when none is needed:
+ * no split-K).  Every workspace starts with a 65536-byte prefix of split-K
+ * tile counters, followed by fp32 partial tiles.  The prefix must be zero
+ * before the first use; every successful call leaves it zero again (the
+ * counters reset themselves), so one workspace can serve calls of any shape
+ * in turn.  After an FP8BQ_ERR_DEVICE_TIMEOUT, zero the prefix again. */
+size_t fp8bq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                  fp8bq_dtype out_dtype);
+/* Same for an explicit variant (fp8bq_gemm_variant). */
+size_t fp8bq_variant_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                     const fp8bq_variant* variant);
+/* Workspace bytes of fp8bq_linear: the 65536-byte counter prefix, then the
+ * activation codes (M*K bytes), the activation scales and the split-K
+ * partials, each at a 256-byte aligned offset. */
+size_t fp8bq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                    fp8bq_dtype out_dtype);
+
+/* ------------------------------------------------------------------ quant */
+
+/* Per-token-group activation quant ("vLLM DeepGEMM FP8 Block GEMM 基准测试"
+ * §4.1 per_token_group_quant_fp8 with column_major_scales and
+ * tma_aligned_scales; packed UE8M0 scales as in "vllm-project/vllm PR 42153").
+ * For each row m and group g (128 consecutive k):
+ *   amax = max |x|;  s = fp32(max(amax, 1e-10) / 448);
+ *   UE8M0: s = 2^ceil(log2 s);
+ *   q = e4m3 round-to-nearest-even of clamp(fp32(x / s), -448, 448).
+ * x: [M,K] row-major, x_dtype FP8BQ_BF16 or FP8BQ_FP16, 16-byte aligned.
+ * q: [M,K] e4m3 codes row-major, 16-byte aligned.
+ * s: fp8bq_act_scale_bytes(M,K,group,fmt) bytes, 16-byte aligned; padding rows
+ *    [M, Mp) and unused bytes of the last packed word are written as 0.
+ * group must be 128.  Results are bit-exact functions of the input. */
+fp8bq_status fp8bq_quant_act(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t K,
+                             int group, fp8bq_scale_fmt fmt, void* q, void* s,
+                             cudaStream_t stream);
+
+/* 128x128 weight block quant ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.1
+ * per_block_cast_to_fp8(B, [128,128], use_ue8m0)): per block (nb, kb) the same
+ * scale and rounding rules as fp8bq_quant_act, over the block's 128x128
+ * elements (a partial last row block uses the rows that exist).
+ * w: [N,K] row-major, FP8BQ_FP32, FP8BQ_BF16 or FP8BQ_FP16, 16-byte aligned.
+ * q: [N,K] e4m3 codes, 16-byte aligned.
+ * s: fp32 [ceil(N/128)][K/128] row-major (powers of two in UE8M0 mode).
+ * block_n and block_k must be 128.  Meant for offline use. */
+fp8bq_status fp8bq_quant_weight(const void* w, fp8bq_dtype w_dtype, int64_t N, int64_t K,
+                                int block_n, int block_k, fp8bq_scale_fmt fmt, void* q,
+                                float* s, cudaStream_t stream);
+
+/* ------------------------------------------------------------------- GEMM */
+
+/* out[m,n] = sum_kb sa[m,kb] * sw[n/128,kb] * sum_{k in slab kb} a_q[m,k]*w_q[n,k]
+ * ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.2: fp8_gemm_nt, A [M,K] and W
+ * [N,K] both K-major; the per-K-block scale multiply into the accumulator).
+ * Each slab's FP8 products are summed by the tensor cores in fp32 and the
+ * slab sum is promoted into an fp32 register accumulator; the result is
+ * rounded to nearest even into out_dtype.
+ * a_q: [M,K] e4m3 row-major, 16-byte aligned.
+ * a_s: activation scales in the fp8bq_quant_act layout for `fmt`.
+ * w_q: [N,K] e4m3 row-major, 16-byte aligned.  w_s: fp32 [ceil(N/128)][K/128].
+ * out: [M,N] row-major out_dtype (BF16, FP16 or FP32), 16-byte aligned.
+ * workspace: fp8bq_gemm_workspace_bytes(...) bytes (may be NULL when that is
+ * 0), zero-filled before first use, 256-byte aligned.
+ * group, block_n, block_k must be 128.  The kernel shape comes from the
+ * per-shape table (fp8bq_select_variant). */
+fp8bq_status fp8bq_gemm(int64_t M, int64_t N, int64_t K, const void* a_q, const void* a_s,
+                        const void* w_q, const float* w_s, int group, int block_n, int block_k,
+                        fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* fp8bq_gemm with an explicit kernel shape (used by the tuner and the tests).
+ * The workspace size is fp8bq_variant_workspace_bytes for that variant. */
+fp8bq_status fp8bq_gemm_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                const void* a_s, const void* w_q, const float* w_s,
+                                fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                                const fp8bq_variant* variant, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Activation quant followed by the GEMM, one call, two launches on `stream`
+ * (the whole W8A8 linear layer for a bf16/fp16 input x [M,K]).  The codes and
+ * scales go to the front of `workspace`; see fp8bq_linear_workspace_bytes. */
+fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N, int64_t K,
+                          const void* w_q, const float* w_s, int group, int block_n,
+                          int block_k, fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------ host queries */
+
+/* The variant fp8bq_gemm would run for this shape (host only, no GPU work):
+ * the measured table for (device, N, K, fmt, out_dtype) is searched for the
+ * M grid point nearest to M (a tie goes to the smaller M); without a table
+ * entry a default variant is used and, with FP8BQ_LOG=1 in the environment,
+ * one line is logged per (N, K, fmt, out_dtype) ("vLLM 量化 Kernel 配置机制"
+ * §4.1-§4.2).  The table file is FP8BQ_TABLE if set, else
+ * <package>/tables/<device name, spaces as '_'>.tbl. */
+fp8bq_status fp8bq_select_variant(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                  fp8bq_dtype out_dtype, fp8bq_variant* variant);
+
+/* Reloads the table (after FP8BQ_TABLE changed); host only. */
+fp8bq_status fp8bq_reload_table(void);
+
+/* Synchronises `stream`, reads and clears the library's device status word:
+ * *code = FP8BQ_OK, or FP8BQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
+ * gave up since the last read.  Bounded waits give up after
+ * FP8BQ_WAIT_TIMEOUT_MS milliseconds (environment, default 2000). */
+fp8bq_status fp8bq_device_status(int* code, cudaStream_t stream);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing arrives at, for at most timeout_ns nanoseconds, then
+ * records FP8BQ_ERR_DEVICE_TIMEOUT in the status word and returns.  Never
+ * hangs.  Read the result with fp8bq_device_status. */
+fp8bq_status fp8bq_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+const char* fp8bq_status_string(fp8bq_status status);
+int fp8bq_abi_version(void); /* 1 */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8BQ_H */

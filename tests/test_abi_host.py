@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute launched).
+
+* the library loads and exports every function include/fp8bq.h declares;
+* size queries agree with the oracle's layout arithmetic;
+* invalid arguments are rejected on the host with the documented status;
+* the per-shape table lookup: nearest M, ties to the smaller grid point
+  ("vLLM 量化 Kernel 配置机制" §4.2 worked examples M=37 -> 32, M=2050 -> 2048),
+  a missing entry falls back to the default variant.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from block_scaled_fp8_group_gb300 import build, fp8bq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fp8bq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8bq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(fp8bq.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) == set(fp8bq.EXPORTS)
+
+
+def test_abi_version_and_status_strings():
+    lib = fp8bq.lib()
+    assert lib.fp8bq_abi_version() == 1
+    for code in range(9):
+        assert lib.fp8bq_status_string(code)
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 640), (16, 1536), (37, 7168), (1025, 18432)])
+@pytest.mark.parametrize("ue", [False, True])
+def test_act_scale_bytes_matches_oracle(M, K, ue):
+    assert fp8bq.fp8bq_act_scale_bytes(M, K, 128, "ue8m0" if ue else "fp32") == \
+        oracle.act_scale_bytes(M, K, 128, ue)
+
+
+def test_size_queries_reject_bad_shapes():
+    lib = fp8bq.lib()
+    assert lib.fp8bq_act_scale_bytes(4, 100, 128, 0) == 0
+    assert lib.fp8bq_act_scale_bytes(4, 256, 64, 0) == 0
+    assert lib.fp8bq_weight_scale_bytes(200, 384, 128, 128) == 4 * 2 * 3
+    assert lib.fp8bq_weight_scale_bytes(200, 384, 64, 128) == 0
+
+
+def call_gemm(M=16, N=128, K=256, ptr=4096, group=128, fmt=0, out=0, ws=None, wsb=0):
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(ptr)
+    return lib.fp8bq_gemm(M, N, K, p, p, p, p, group, 128, 128, fmt, out, p, ws, wsb, None)
+
+
+def test_gemm_argument_errors_on_host():
+    assert call_gemm(K=100) == 2          # K % 128
+    assert call_gemm(K=0) == 2            # K == 0
+    assert call_gemm(N=100) == 2          # N % 64
+    assert call_gemm(M=-1) == 1
+    assert call_gemm(fmt=7) == 1
+    assert call_gemm(out=9) == 1
+    assert call_gemm(group=64) == 4
+    assert call_gemm(ptr=4100) == 3       # not 16-byte aligned
+    assert call_gemm(ptr=0) == 1          # null
+    assert call_gemm(M=0) == 0            # empty: no-op
+    assert call_gemm(N=0) == 0
+
+
+def test_quant_argument_errors_on_host():
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(4096)
+    assert lib.fp8bq_quant_act(p, 0, 4, 100, 128, 0, p, p, None) == 2
+    assert lib.fp8bq_quant_act(p, 2, 4, 128, 128, 0, p, p, None) == 4   # fp32 input
+    assert lib.fp8bq_quant_act(p, 0, 4, 128, 32, 0, p, p, None) == 4
+    assert lib.fp8bq_quant_act(ctypes.c_void_p(4104), 0, 4, 128, 128, 0, p, p, None) == 3
+    assert lib.fp8bq_quant_act(p, 0, 0, 128, 128, 0, p, p, None) == 0
+    assert lib.fp8bq_quant_weight(p, 0, 4, 128, 128, 64, 0, p, p, None) == 4
+    assert lib.fp8bq_quant_weight(p, 0, 4, 120, 128, 128, 0, p, p, None) == 2
+
+
+def test_linear_argument_errors_on_host():
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(4096)
+    # workspace not 256-byte aligned
+    assert lib.fp8bq_linear(p, 0, 4, 128, 128, p, p, 128, 128, 128, 1, 0, p,
+                            ctypes.c_void_p(4096 + 16), 1 << 20, None) == 5
+    assert lib.fp8bq_linear(p, 2, 4, 128, 128, p, p, 128, 128, 128, 1, 0, p, p, 1 << 20,
+                            None) == 4
+
+
+@pytest.fixture()
+def fake_table(tmp_path, monkeypatch):
+    t = tmp_path / "t.tbl"
+    t.write_text(
+        "# N K fmt out M kind block_n split grid\n"
+        "4096 7168 ue8m0 bf16 1 swap 16 4 0\n"
+        "4096 7168 ue8m0 bf16 32 swap 32 2 0\n"
+        "4096 7168 ue8m0 bf16 64 swap 64 1 120\n"
+        "4096 7168 ue8m0 bf16 2048 normal 256 1 0\n"
+        "4096 7168 ue8m0 bf16 4096 normal 128 1 0\n"
+        "this line is malformed and skipped\n")
+    monkeypatch.setenv("FP8BQ_TABLE", str(t))
+    fp8bq.fp8bq_reload_table()
+    yield
+    monkeypatch.delenv("FP8BQ_TABLE")
+    fp8bq.fp8bq_reload_table()
+
+
+def test_nearest_m_lookup(fake_table):
+    sel = lambda M: fp8bq.fp8bq_select_variant(M, 4096, 7168, "ue8m0", "bf16")
+    assert sel(37)["block_n"] == 32          # 37 -> 32
+    assert sel(2050)["block_n"] == 256       # 2050 -> 2048
+    assert sel(48)["block_n"] == 32          # tie between 32 and 64 -> smaller
+    v = sel(64)
+    assert v == {"kind": "swap", "block_n": 64, "split": 1, "grid": 120, "from_table": True}
+    assert sel(1)["split"] == 4
+    assert sel(10 ** 6)["block_n"] == 128    # beyond the grid -> largest key
+    assert sel(3072)["block_n"] == 256       # tie 2048/4096 -> smaller
+
+
+def test_table_miss_uses_default(fake_table):
+    v = fp8bq.fp8bq_select_variant(8, 7168, 18432, "ue8m0", "bf16")
+    assert v["from_table"] is False and v["kind"] == "swap" and v["block_n"] == 16
+    v = fp8bq.fp8bq_select_variant(4096, 24576, 7168, "fp32", "bf16")
+    assert v["from_table"] is False and v["kind"] == "normal"
+    # other fmt/out of a tabulated (N,K) also misses
+    assert fp8bq.fp8bq_select_variant(1, 4096, 7168, "fp32", "bf16")["from_table"] is False
+
+
+def test_variant_workspace_bytes():
+    v1 = fp8bq.make_variant("swap", 16, 1)
+    assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, v1) == 0
+    v4 = fp8bq.make_variant("swap", 16, 4)
+    tiles = 7168 // 128
+    assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, v4) == \
+        65536 + tiles * 4 * 128 * 16 * 4
+    # linear: counter prefix + codes + scales (+ partials)
+    lin = fp8bq.fp8bq_linear_workspace_bytes(8, 7168, 18432, "ue8m0", "bf16")
+    g = fp8bq.fp8bq_gemm_workspace_bytes(8, 7168, 18432, "ue8m0", "bf16")
+    codes = (8 * 18432 + 255) // 256 * 256
+    scales = (4 * ((144 + 3) // 4) * 8 + 255) // 256 * 256
+    assert lin == 65536 + codes + scales + (g - 65536 if g else 0)
+    bad = fp8bq.make_variant("swap", 48, 1)
+    assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, bad) == 0

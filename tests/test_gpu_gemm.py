@@ -1,0 +1,166 @@
+"""GPU parity of the block-scaled GEMM (every variant) and the fused linear
+layer against the fp64 oracle, within the stated element-wise / Frobenius
+bounds.  Inputs are quantised by the oracle on the host, so the GEMM is
+checked independently of the GPU quant kernel."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp8_group_gb300 import synth
+from parity import (TORCH_OUT, check_gemm, oracle_full, oracle_rows, quantised_problem,
+                    sample_rows, scales_to_dev, to_dev, to_dev_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8bq():
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq as m
+    return m
+
+
+def upload(qa, sa, qw, sw):
+    return to_dev(qa), scales_to_dev(sa), to_dev(qw), to_dev(sw)
+
+
+VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (1, 2, 3)] +
+            [("normal", bn, s) for bn in (128, 256) for s in (1, 2, 5)])
+
+
+@pytest.mark.parametrize("kind,bn,split", VARIANTS)
+@pytest.mark.parametrize("M,N,K,ue", [(1, 128, 128, False), (5, 320, 640, True),
+                                      (77, 256, 1024, False), (130, 384, 768, True)])
+def test_variants_small(fp8bq, kind, bn, split, M, N, K, ue):
+    if split > K // 128:
+        pytest.skip("more splits than K slabs")
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, ue, synth.act_decode)
+    ref = oracle_full(qa, sa, qw, sw, ue)
+    d = upload(qa, sa, qw, sw)
+    v = fp8bq.make_variant(kind, bn, split)
+    for out in ("bf16", "fp32"):
+        o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0" if ue else "fp32",
+                                     out_dtype=TORCH_OUT[out])
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy(), ref, out, f"{kind}/{bn}/{split} {M}x{N}x{K} {out}")
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7])
+def test_persistent_grid_loops_over_items(fp8bq, grid):
+    M, N, K = 40, 640, 1280
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_prefill)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    d = upload(qa, sa, qw, sw)
+    for v in (fp8bq.make_variant("swap", 64, 3, grid), fp8bq.make_variant("normal", 128, 2, grid)):
+        o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check_gemm(o.cpu().numpy(), ref, "fp32", f"grid {grid} {v.as_dict()}")
+
+
+def test_split_k_is_bit_stable_and_reusable(fp8bq):
+    M, N, K = 24, 1024, 2048
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_decode)
+    d = upload(qa, sa, qw, sw)
+    v = fp8bq.make_variant("swap", 32, 7)
+    outs = [fp8bq.fp8bq_gemm_variant(*d, v, out_dtype=torch.float32) for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    check_gemm(outs[0].cpu().numpy(), oracle_full(qa, sa, qw, sw, False), "fp32", "split 7")
+
+
+def test_fp16_output(fp8bq):
+    M, N, K = 33, 512, 1024
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_full_grid)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    o = fp8bq.fp8bq_gemm(*upload(qa, sa, qw, sw), fmt="ue8m0", out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    check_gemm(o.float().cpu().numpy(), ref, "fp16")
+
+
+def test_small_config_full(fp8bq):
+    """M=16, N=K=1536: bf16 N(0,1) activations with fp32 scales, fp32
+    N(0,0.02) weights, bf16 output -- every element."""
+    M, N, K = 16, 1536, 1536
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_small)
+    ref = oracle_full(qa, sa, qw, sw, False)
+    o = fp8bq.fp8bq_gemm(*upload(qa, sa, qw, sw), fmt="fp32", out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    check_gemm(o.float().cpu().numpy(), ref, "bf16", "small config")
+    # the same through the GPU quant kernels and the fused linear entry point
+    w = synth.weight_f32(N, K)
+    wq, ws = fp8bq.fp8bq_quant_weight(to_dev(w), "fp32")
+    o2 = fp8bq.fp8bq_linear(to_dev_bits(xb), wq, ws, fmt="fp32", out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    check_gemm(o2.float().cpu().numpy(), ref, "bf16", "small config linear")
+
+
+@pytest.mark.parametrize("N,K", synth.DECODE_NK)
+@pytest.mark.parametrize("M", [1, 8, 24, 128])
+def test_decode_full_size_sampled(fp8bq, N, K, M):
+    """Decode sweep shapes at full size (UE8M0, bf16 out), in the variant the
+    table selects; sampled rows, all columns."""
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode, weight="bf16")
+    o = fp8bq.fp8bq_gemm(*upload(qa, sa, qw, sw), fmt="ue8m0", out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, 6)
+    check_gemm(o.float().cpu().numpy()[rows], oracle_rows(qa, sa, qw, sw, True, rows), "bf16",
+               f"decode {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("N,K", synth.PREFILL_NK)
+@pytest.mark.parametrize("M", [256, 1536, 4096])
+def test_prefill_full_size_sampled(fp8bq, N, K, M):
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_prefill, weight="bf16")
+    d = upload(qa, sa, qw, sw)
+    rows = sample_rows(M, 5)
+    ref = oracle_rows(qa, sa, qw, sw, False, rows)
+    for out in ("bf16", "fp32"):
+        o = fp8bq.fp8bq_gemm(*d, fmt="fp32", out_dtype=TORCH_OUT[out])
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy()[rows], ref, out, f"prefill {M}x{N}x{K} {out}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1536, 7168), (48, 7168, 1536), (300, 4096, 7168),
+                                   (2048, 24576, 7168)])
+@pytest.mark.parametrize("out", ["fp16", "bf16"])
+def test_linear_full_grid_sampled(fp8bq, M, N, K, out):
+    """Fused quant + GEMM (UE8M0) on full-grid shapes; the reference quantises
+    with the oracle on the host."""
+    xb = synth.act_full_grid(M, K)
+    wb = synth.weight_bf16(N, K)
+    wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
+    o = fp8bq.fp8bq_linear(to_dev_bits(xb), wq, ws, fmt="ue8m0", out_dtype=TORCH_OUT[out])
+    torch.cuda.synchronize()
+    rows = sample_rows(M, 4)
+    qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+    qa, sa = oracle.quant_act(np.ascontiguousarray(xb[rows]), oracle.BF16, 128, True)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    check_gemm(o.float().cpu().numpy()[rows], ref, out, f"linear {M}x{N}x{K}")
+
+
+def test_empty_and_errors(fp8bq):
+    a = torch.zeros((0, 256), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
+    w = torch.zeros((128, 256), dtype=torch.uint8, device="cuda")
+    ws = torch.ones((1, 2), dtype=torch.float32, device="cuda")
+    # M = 0 is a no-op (pointers of empty tensors may be null: use a dummy)
+    o = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    st = fp8bq.lib().fp8bq_gemm(0, 128, 256, w.data_ptr(), ws.data_ptr(), w.data_ptr(),
+                                ws.data_ptr(), 128, 128, 128, 0, 0, w.data_ptr(), None, 0, None)
+    assert st == 0
+    with pytest.raises(fp8bq.Fp8bqError):
+        fp8bq.fp8bq_gemm_variant(w[:, :256], ws, w, ws, fp8bq.make_variant("swap", 48, 1))
+    # a too-small workspace is rejected before launching
+    M, N, K = 8, 1024, 1024
+    qa = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((8, 8), dtype=torch.float32, device="cuda")
+    wq = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((8, 8), dtype=torch.float32, device="cuda")
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp8bq.Fp8bqError) as e:
+        fp8bq.fp8bq_gemm_variant(qa, sa, wq, sw, fp8bq.make_variant("swap", 16, 4),
+                                 workspace=small)
+    assert e.value.status == 5

@@ -1,0 +1,136 @@
+"""GPU parity of activation and weight quantisation against the oracle:
+codes and scales bit-exact, padding included."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp8_group_gb300 import synth
+from parity import scales_bits, to_dev, to_dev_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8bq():
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq as m
+    return m
+
+
+def run_act(fp8bq, xb, fp16, ue):
+    x = to_dev_bits(xb, torch.float16 if fp16 else torch.bfloat16)
+    q, s = fp8bq.fp8bq_quant_act(x, "ue8m0" if ue else "fp32")
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), scales_bits(s)
+
+
+@pytest.mark.parametrize("ue", [False, True])
+@pytest.mark.parametrize("fp16", [False, True])
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 640), (5, 512), (37, 1536), (130, 7168),
+                                 (64, 18432), (9, 1152)])
+def test_act_quant_bit_exact(fp8bq, M, K, fp16, ue):
+    x = synth.normal((M, K), seed=M * 7 + K)
+    synth.group_spikes(x, 128, seed=5, row_period=3, row_phase=1)
+    xb = synth.f32_to_f16_bits(x) if fp16 else synth.f32_to_bf16_bits(x)
+    q, s = run_act(fp8bq, xb, fp16, ue)
+    rq, rs = oracle.quant_act(xb, oracle.FP16 if fp16 else oracle.BF16, 128, ue)
+    np.testing.assert_array_equal(q, rq)
+    np.testing.assert_array_equal(s, rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("ue", [False, True])
+def test_act_quant_every_bf16_value_through_the_converter(fp8bq, ue):
+    """Groups whose amax is 448 have s = 1 in both modes, so their other 127
+    elements reach the fp8 conversion unchanged: every finite bf16 value in
+    [-448, 448] is checked against the oracle's encoder."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_bits_to_f32(bits)
+    keep = bits[np.isfinite(vals) & (np.abs(vals) <= 448)]
+    per = 127
+    G = (keep.size + per - 1) // per
+    groups = np.zeros((G, 128), dtype=np.uint16)
+    flat = np.concatenate([keep, np.zeros(G * per - keep.size, dtype=np.uint16)])
+    groups[:, 1:] = flat.reshape(G, per)
+    groups[:, 0] = synth.f32_to_bf16_bits(np.array([448.0], dtype=np.float32))[0]
+    K = 1024
+    rows = (G + 7) // 8
+    xb = np.zeros((rows * 8, 128), dtype=np.uint16)
+    xb[:G] = groups
+    xb[G:, 0] = groups[0, 0]
+    xb = xb.reshape(rows, K)
+    q, s = run_act(fp8bq, xb, False, ue)
+    rq, rs = oracle.quant_act(xb, oracle.BF16, 128, ue)
+    np.testing.assert_array_equal(q, rq)
+    np.testing.assert_array_equal(s, rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("ue", [False, True])
+@pytest.mark.parametrize("M", [1, 64, 1024, 4096, 16384])
+@pytest.mark.parametrize("K", [1536, 7168, 18432])
+def test_act_quant_full_size_sampled(fp8bq, M, K, ue):
+    """The standalone-quant workload at full size: sampled rows vs the oracle
+    (quantisation is row-local), padding rows of the scale buffer zero."""
+    xb = synth.act_quant(M, K)
+    q, s = run_act(fp8bq, xb, False, ue)
+    Mp = (M + 3) // 4 * 4
+    G = K // 128
+    cols = (G + 3) // 4 if ue else G
+    assert s.shape == (cols, Mp)
+    assert np.all(s[:, M:] == 0)
+    rows = sorted({0, M - 1} | set(range(3, M, 8 * max(1, M // 64))) |
+                  set(np.random.default_rng(M + K).choice(M, size=min(M, 6), replace=False)))
+    for m in rows:
+        rq, rs = oracle.quant_act(np.ascontiguousarray(xb[m:m + 1]), oracle.BF16, 128, ue)
+        np.testing.assert_array_equal(q[m], rq[0], err_msg=f"row {m}")
+        np.testing.assert_array_equal(s[:, m], rs.view(np.uint32)[:, 0], err_msg=f"row {m}")
+
+
+@pytest.mark.parametrize("ue", [False, True])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "fp16"])
+@pytest.mark.parametrize("N,K", [(128, 128), (200, 384), (1536, 1536), (320, 640)])
+def test_weight_quant_bit_exact(fp8bq, N, K, dt, ue):
+    wf = synth.weight_f32(N, K, seed=N + K)
+    if dt == "f32":
+        host, code, dev = wf, oracle.FP32, to_dev(wf)
+    elif dt == "bf16":
+        host = synth.f32_to_bf16_bits(wf)
+        code, dev = oracle.BF16, to_dev_bits(host, torch.bfloat16)
+    else:
+        host = synth.f32_to_f16_bits(wf)
+        code, dev = oracle.FP16, to_dev_bits(host, torch.float16)
+    q, s = fp8bq.fp8bq_quant_weight(dev, "ue8m0" if ue else "fp32")
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_weight(host, code, 128, 128, ue)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def test_quant_weight_decode_shapes(fp8bq):
+    """The decode-sweep weight shapes at full size, sampled blocks."""
+    for N, K in synth.DECODE_NK:
+        wb = synth.weight_bf16(N, K)
+        q, s = fp8bq.fp8bq_quant_weight(to_dev_bits(wb, torch.bfloat16), "ue8m0")
+        torch.cuda.synchronize()
+        q = q.cpu().numpy()
+        s = s.cpu().numpy()
+        rng = np.random.default_rng(N)
+        for nb, kb in [(0, 0), (N // 128 - 1, K // 128 - 1)] + [
+                (int(a), int(b)) for a, b in zip(rng.integers(0, N // 128, 4),
+                                                 rng.integers(0, K // 128, 4))]:
+            blk = np.ascontiguousarray(wb[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128])
+            rq, rs = oracle.quant_weight(blk, oracle.BF16, 128, 128, True)
+            np.testing.assert_array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128], rq)
+            assert s[nb, kb] == rs[0, 0]
+
+
+def test_bounded_wait_times_out_and_reports(fp8bq):
+    assert fp8bq.fp8bq_device_status() == 0
+    fp8bq.fp8bq_selftest_wait_timeout(20_000_000)  # 20 ms, nothing ever arrives
+    assert fp8bq.fp8bq_device_status() == 7        # FP8BQ_ERR_DEVICE_TIMEOUT
+    assert fp8bq.fp8bq_device_status() == 0        # read clears it
+    # the context is still usable
+    x = to_dev_bits(synth.act_small(4, 256))
+    fp8bq.fp8bq_quant_act(x, "fp32")
+    torch.cuda.synchronize()
