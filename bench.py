@@ -1,0 +1,469 @@
+"""Benchmark of the W8A8 block-FP8 linear hot path on GB300.
+
+Workload (one "step"): the decode sweep -- (N, K) in {(7168, 18432),
+(18432, 7168), (4096, 7168)} x M in {1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128},
+33 problems; per problem the activation quant (bf16 -> e4m3 + packed UE8M0
+scales) and the block-scaled GEMM (UE8M0, bf16 out) in the variant the
+per-shape table selects.  Activations: bf16 N(0,1) with 1% of the K channels
+x30; weights bf16 N(0,0.02) quantised 128x128 (UE8M0) once, outside the timed
+region (as the pages' benchmark does).  Every GEMM of a step reads its own
+copy of the weights (3.2 GB per step), so no GEMM finds its operands in L2.
+
+Reported: value = algorithmic bytes of the whole step / step time (GB/s),
+per-problem GEMM us / TFLOPS / GB/s / roofline fraction, the roofline of the
+dominant kernel (the GEMM) against the measured HBM copy bandwidth, an
+end-to-end number through fp8bq_linear with pinned host buffers, and the CPU
+oracle timed on a bounded sample.  `--impl reference` times the oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_scaled_fp8_group_gb300 import synth  # noqa: E402
+
+METRIC = "block-FP8 GEMM µs, TFLOPS and GB/s per (M,N,K) on 1 GB300; % of roofline"
+WORKLOAD = ("decode sweep: (N,K) in {(7168,18432),(18432,7168),(4096,7168)} x "
+            "M in {1,2,4,8,16,24,32,48,64,96,128}; act bf16 N(0,1), 1% channels x30 -> "
+            "per-token-group quant (UE8M0 packed); weights bf16 N(0,0.02) 128x128 UE8M0; "
+            "bf16 out")
+# The pages' DeepGEMM numbers on H100 80GB HBM3 for shapes of this sweep
+# ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §3.2, DeepGEMM table) -- context only.
+H100_DEEPGEMM_US = {(8, 7168, 18432): 70.8, (8, 18432, 7168): 69.3, (8, 4096, 7168): 102.9,
+                    (64, 7168, 18432): 69.4, (64, 18432, 7168): 70.4, (64, 4096, 7168): 69.1,
+                    (128, 7168, 18432): 71.9, (128, 18432, 7168): 69.3,
+                    (128, 4096, 7168): 141.1}
+FP8_TO_BF16_NOMINAL = 2.0  # 4.5 / 2.25 PFLOP/s dense, nominal ratio
+
+
+def problems():
+    return [(M, N, K) for M in synth.DECODE_M for (N, K) in synth.DECODE_NK]
+
+
+def gemm_bytes(M, N, K):
+    """Algorithmic bytes of one GEMM launch: e4m3 A and W, packed UE8M0 act
+    scales, fp32 weight scales, bf16 output."""
+    G = K // 128
+    Mp = (M + 3) // 4 * 4
+    return M * K + N * K + 4 * Mp * ((G + 3) // 4) + 4 * ((N + 127) // 128) * G + 2 * M * N
+
+
+def quant_bytes(M, K):
+    G = K // 128
+    Mp = (M + 3) // 4 * 4
+    return 2 * M * K + M * K + 4 * Mp * ((G + 3) // 4)
+
+
+def step_bytes(M, N, K):
+    """Algorithmic bytes of one problem of the step (linear layer): bf16 A in,
+    W, weight scales, bf16 out (the intermediate codes are not counted)."""
+    G = K // 128
+    return 2 * M * K + N * K + 4 * ((N + 127) // 128) * G + 2 * M * N
+
+
+def pages_gbs_bytes(M, N, K):
+    """The pages' GB/s numerator: m*k + k*n + 2*m*n ("vLLM DeepGEMM FP8 Block GEMM
+    基准测试" §4.3)."""
+    return M * K + K * N + 2 * M * N
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(ROOT, "block_scaled_fp8_group_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_decode_sweep_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    t = re.search(r"traffic_bytes_per_launch_avg:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != gemm_source_hash():
+        return None
+    return float(t.group(1))
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm_max = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] > 0.5 * sm_max] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in loaded])), "sm_max_mhz": sm_max,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ------------------------------------------------------------- oracle legs
+
+_ORACLE_W = {}
+
+
+def oracle_time_sample(rows_per_shape=1, reps=1):
+    """Times the CPU oracle (quant of the sampled rows + their GEMM rows) on
+    one thread; returns (extrapolated whole-step seconds, sample seconds,
+    description).  Weights are quantised by the oracle outside the timing."""
+    import oracle
+    total_rows = sum(synth.DECODE_M)
+    est = 0.0
+    sample_s = 0.0
+    for (N, K) in synth.DECODE_NK:
+        if (N, K) not in _ORACLE_W:
+            _ORACLE_W[(N, K)] = oracle.quant_weight(synth.weight_bf16(N, K), oracle.BF16, 128,
+                                                    128, True)
+        qw, sw = _ORACLE_W[(N, K)]
+        xb = synth.act_decode(rows_per_shape, K)
+        best = None
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
+            oracle.gemm(qa, sa, qw, sw, True)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        sample_s += best
+        est += best / rows_per_shape * total_rows
+    desc = (f"{rows_per_shape} activation row(s) per (N,K) through oracle quant + fp64 GEMM "
+            f"(all N columns), single thread; whole-step time extrapolated linearly in M "
+            f"({total_rows} rows per (N,K))")
+    return est, sample_s, desc
+
+
+def total_step_bytes():
+    return sum(step_bytes(M, N, K) for (M, N, K) in problems())
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    steps, warm = args.steps_ref, max(0, args.warmup)
+    for _ in range(warm):
+        oracle_time_sample(1)
+    ests = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        est, _, desc = oracle_time_sample(1)
+        ests.append(est)
+    wall = time.perf_counter() - t0
+    est = float(np.mean(ests))
+    value = total_step_bytes() / est / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": est * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    probs = problems()
+    stream = torch.cuda.current_stream()
+
+    # ---- setup (untimed): weights quantised once, one copy per M point
+    w_q, w_s = {}, {}
+    for (N, K) in synth.DECODE_NK:
+        wb = synth.weight_bf16(N, K)
+        wd = torch.from_numpy(wb.view(np.int16)).view(torch.bfloat16).to(dev)
+        q, s = fp8bq.fp8bq_quant_weight(wd, "ue8m0")
+        del wd
+        for M in synth.DECODE_M:
+            w_q[(M, N, K)] = q.clone()
+        w_s[(N, K)] = s
+        del q
+    torch.cuda.synchronize()
+    xs, aqs, ass, outs = {}, {}, {}, {}
+    for (M, N, K) in probs:
+        xb = synth.act_decode(M, K)
+        xs[(M, N, K)] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+        aqs[(M, N, K)], ass[(M, N, K)] = (
+            torch.empty((M, K), dtype=torch.uint8, device=dev),
+            torch.empty(fp8bq.act_scale_shape(M, K, 128, "ue8m0")[0], dtype=torch.int32,
+                        device=dev))
+        outs[(M, N, K)] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = max(fp8bq.fp8bq_linear_workspace_bytes(M, N, K, "ue8m0", torch.bfloat16)
+                   for (M, N, K) in probs)
+    ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
+    variants = {p: fp8bq.fp8bq_select_variant(*p, "ue8m0", torch.bfloat16) for p in probs}
+
+    def launch_step(ev_pairs):
+        for i, p in enumerate(probs):
+            M, N, K = p
+            fp8bq.fp8bq_quant_act(xs[p], "ue8m0", q=aqs[p], s=ass[p])
+            if ev_pairs is not None:
+                ev_pairs[i][0].record()
+            fp8bq.fp8bq_gemm(aqs[p], ass[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
+                             out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
+            if ev_pairs is not None:
+                ev_pairs[i][1].record()
+
+    # ---- timing instruments: graph with external timing events, else eager
+    mode = args.mode
+    ext_ok = True
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        ext_ok = False
+    if mode == "graph" and not ext_ok:
+        mode = "eager"
+    mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if mode == "graph" else \
+        (lambda: torch.cuda.Event(enable_timing=True))
+    ev_pairs = [(mk(), mk()) for _ in probs]
+    ev_start, ev_end = mk(), mk()
+
+    launch_step(None)  # first launches: loads the table, sets kernel attributes
+    torch.cuda.synchronize()
+    graph = None
+    if mode == "graph":
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                ev_start.record()
+                launch_step(ev_pairs)
+                ev_end.record()
+        torch.cuda.synchronize()
+
+    def run_one():
+        if graph is not None:
+            graph.replay()
+        else:
+            ev_start.record()
+            launch_step(ev_pairs)
+            ev_end.record()
+
+    for _ in range(args.warmup):
+        run_one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    step_ms, gemm_ms = [], np.zeros(len(probs))
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_one()
+        ev_end.synchronize()
+        step_ms.append(ev_start.elapsed_time(ev_end))
+        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_pairs])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if rank == 0 else None
+    step_s = float(np.mean(step_ms)) / 1e3
+    if world > 1:
+        t = torch.tensor([step_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_s = float(t.item())
+    gemm_us = gemm_ms / args.steps * 1e3
+    launches = args.steps * 2 * len(probs)
+
+    # ---- end to end through the public fp8bq_linear call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = {p: xs[p].cpu().pin_memory() for p in probs}
+        hout = {p: torch.empty(outs[p].shape, dtype=torch.bfloat16).pin_memory() for p in probs}
+        h2d = sum(2 * M * K for (M, N, K) in probs)
+        d2h = sum(2 * M * N for (M, N, K) in probs)
+        xd = {p: torch.empty_like(xs[p]) for p in probs}
+
+        def e2e_step():
+            for p in probs:
+                M, N, K = p
+                xd[p].copy_(hx[p], non_blocking=True)
+                fp8bq.fp8bq_linear(xd[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
+                                   out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
+                hout[p].copy_(outs[p], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+        a.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record()
+        b.synchronize()
+        e2e_s = a.elapsed_time(b) / 1e3 / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * total_step_bytes() / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
+               "api": "fp8bq_linear (quant + GEMM, PDL) per problem, pinned host x/out"}
+
+    if rank != 0:
+        return 0
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
+    per = []
+    for i, (M, N, K) in enumerate(probs):
+        t = gemm_us[i] * 1e-6
+        b = gemm_bytes(M, N, K)
+        fl = 2.0 * M * N * K
+        t_roof = max(b / (peaks["hbm_gbs"] * 1e9), fl / (fp8_peak * 1e12))
+        per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
+                    "tflops": round(fl / t / 1e12, 2),
+                    "gbs_pages": round(pages_gbs_bytes(M, N, K) / t / 1e9, 1),
+                    "gbs_alg": round(b / t / 1e9, 1), "roofline_frac": round(t_roof / t, 3),
+                    "variant": "{kind}/{block_n}/s{split}".format(**variants[(M, N, K)]),
+                    "h100_deepgemm_us": H100_DEEPGEMM_US.get((M, N, K))})
+    tot_gemm_bytes = sum(gemm_bytes(*p) for p in probs)
+    achieved = tot_gemm_bytes / (gemm_us.sum() * 1e-6) / 1e9
+    traffic = profile_traffic()
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "kernel": "gemm_kernel (decode sweep, 33 launches per step)",
+            "algorithmic_bytes_per_launch_avg": tot_gemm_bytes / len(probs),
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        est, sample_s, desc = oracle_time_sample(rows_per_shape=args.oracle_rows)
+        cpu = {"value": total_step_bytes() / est / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": desc + f" (sample took {sample_s:.1f} s)"}
+    value = world * total_step_bytes() / step_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "problems_per_step": len(probs),
+                   "l2": "inputs larger than L2: each GEMM reads its own weight copy "
+                         "(3.2 GB of weights per step)",
+                   "timing": f"{mode}: CUDA events on the launching stream per step and "
+                             "around every GEMM launch",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk, "per_shape": per, "wall_timed_s": round(t_wall, 3),
+        "gemm_source_sha256_16": gemm_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("fp8bq", "reference"), default="fp8bq")
+    ap.add_argument("--mode", choices=("graph", "eager"), default="graph")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--oracle-rows", type=int, default=4)
+    ap.add_argument("--steps-ref", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.steps_ref is None:
+        args.steps_ref = max(1, min(args.steps, 10))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    rc = run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

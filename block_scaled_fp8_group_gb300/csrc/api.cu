@@ -80,7 +80,8 @@ uint64_t wait_timeout_ns() {
 
 fp8bq_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return FP8BQ_OK;
-    cudaGetLastError();  // clear the sticky-free error state for the next call
+    cudaGetLastError();  // clear the non-sticky error state for the next call
+    log_error(cudaGetErrorString(e));
     return FP8BQ_ERR_LAUNCH;
 }
 
@@ -174,11 +175,12 @@ void load_table_locked(const std::string& device_name) {
 
 // Default variant when the table has no entry (speed only, never correctness;
 // "vLLM 量化 Kernel 配置机制" §4.1).  Swap-AB below 129 tokens, otherwise the
-// normal orientation with 256-wide weight tiles; the K split is the one that
-// minimises (slabs on the busiest CTA) + a small per-split penalty.
+// normal orientation with 256-wide weight tiles.  When the tiles cannot keep
+// every SM busy for whole waves, the (tile, K-slab) units are shared out
+// evenly (stream-K, split = 0); the tile count must fit the workspace's
+// counter prefix for that.
 fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
     fp8bq_variant v = {};
-    const int64_t G = K / 128;
     int64_t tiles;
     if (M <= 128) {
         v.kind = FP8BQ_KIND_SWAP_AB;
@@ -189,20 +191,9 @@ fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
         v.block_n = N >= 256 ? 256 : 128;
         tiles = ((N + v.block_n - 1) / v.block_n) * ((M + 127) / 128);
     }
-    const int64_t max_split = G < 16 ? G : 16;
-    double best = 1e300;
-    int best_s = 1;
-    for (int s = 1; s <= max_split; ++s) {
-        const int64_t items = tiles * s;
-        const int64_t waves = (items + num_sms - 1) / num_sms;
-        const double slabs = static_cast<double>(waves) * static_cast<double>((G + s - 1) / s);
-        const double penalty = (s > 1 ? 1.0 : 0.0) * (M <= 128 ? 0.5 : 4.0) * s;
-        if (slabs + penalty < best) {
-            best = slabs + penalty;
-            best_s = s;
-        }
-    }
-    v.split = best_s;
+    const bool fits_counters = tiles * 8 * 4 <= static_cast<int64_t>(kCounterRegion);
+    const bool whole_waves = tiles % num_sms == 0 || tiles >= 4 * static_cast<int64_t>(num_sms);
+    v.split = (!whole_waves && fits_counters) ? 0 : 1;
     v.grid = 0;
     v.from_table = 0;
     return v;
@@ -552,6 +543,14 @@ fp8bq_status fp8bq_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t strea
 }  // extern "C"
 
 namespace fp8bq {
+
+void log_error(const char* what) {
+    static const bool on = [] {
+        const char* e = std::getenv("FP8BQ_LOG");
+        return e && std::atoi(e) == 1;
+    }();
+    if (on) std::fprintf(stderr, "fp8bq: %s\n", what);
+}
 
 EncodeTiledFn get_encode_tiled() {
     static EncodeTiledFn fn = [] {

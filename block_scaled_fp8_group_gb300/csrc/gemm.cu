@@ -8,21 +8,34 @@
 // accumulator); "用 Helion 为 vLLM 构建高性能可移植线性后端", 内核实现, the
 // Split-K and Swap-AB variants.
 //
-// Design (one CTA per SM, persistent over work items):
+// Design (one CTA per SM, persistent over its work):
 //   warp 0     TMA producer: per K slab, one 128x128 tile of the MMA-M operand
 //              and one BNx128 tile of the MMA-N operand into a STAGES-deep
-//              shared-memory ring (128-byte swizzle, K-major).
+//              shared-memory ring (128-byte swizzle, K-major), and the slab's
+//              scales (activation scales of the tile's tokens, the weight
+//              block's scale) into a separate SR-deep scale ring.
 //   warp 1     MMA issuer: four tcgen05.mma (K = 32 each) per slab into a
 //              fresh TMEM accumulator buffer; commits free the smem stage and
 //              publish the TMEM buffer.  Warp 1 also owns the TMEM allocation.
 //   warps 2..  promotion/epilogue: per slab, tcgen05.ld the slab's fp32 sums,
 //              release the TMEM buffer, and fold them into a register
-//              accumulator with fma(P, sa*sw, acc).  NBUF TMEM buffers let the
-//              MMA of slab kb+1 overlap the promotion of slab kb.
-// Work item = (output tile, K split).  split == 1 is the plain (Standard)
-// GEMM; split > 1 writes fp32 partial tiles to the workspace and the last CTA
-// to finish a tile (atomic ticket; no CTA waits for another) sums the splits
-// in fixed order 0..S-1, so results are run-to-run bit-stable.
+//              accumulator with fma(P, sa*sw, acc), the scales read from the
+//              scale ring.  NBUF TMEM buffers let the MMA of slab kb+1 overlap
+//              the promotion of slab kb.
+//
+// Work: the output is cut into tiles; a tile's K slabs are split into
+// segments processed by different CTAs when the tiles alone cannot fill the
+// GPU.  Two schedules:
+//   split-K (split >= 1): work item = (tile, split s), items dealt round-robin
+//       over the CTAs, split s covering slabs [s*G/S, (s+1)*G/S);
+//   stream-K (split == 0): the tiles x G (tile, slab) units are divided into
+//       equal contiguous ranges, one per CTA, so every CTA streams the same
+//       number of slabs; a range holds at most two partial tiles.
+// A tile finished by one segment is stored directly.  Otherwise every segment
+// writes an fp32 partial tile to the workspace and takes a ticket (one per
+// epilogue warp and tile); the last to arrive sums the partials in K order
+// and stores, so results are run-to-run bit-stable and no CTA ever waits for
+// another.
 // Swap-AB (decode): the MMA-M operand is the weight (128 rows of n), the
 // MMA-N operand the tokens (BN = 16..128), so small M does not waste a
 // 128-row MMA; the epilogue writes the transposed tile back into [M,N].
@@ -40,9 +53,13 @@ namespace fp8bq {
 
 namespace {
 
-constexpr int BM = 128;  // MMA M
-constexpr int BK = 128;  // K slab (one scale block)
+constexpr int BM = 128;              // MMA M
+constexpr int BK = 128;              // K slab (one scale block)
 constexpr int kCountersPerTile = 8;  // one split-K ticket per epilogue warp
+constexpr int SR = 16;               // scale ring depth (slabs)
+constexpr int SLOT_BYTES = 768;      // per slab: 128 act scales, 2 weight-scale chunks
+constexpr int SLOT_SW = 512;         // weight-scale chunk c at SLOT_SW + c * SLOT_SW_STEP
+constexpr int SLOT_SW_STEP = 128;    // (TMA destinations 128-byte aligned)
 
 template <int BN>
 struct Cfg {
@@ -60,8 +77,10 @@ struct Cfg {
     static constexpr int EPI_WARPS = BN >= 128 ? 8 : 4;
     static constexpr int CPT = BN / (EPI_WARPS / 4);  // accumulator columns per thread
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * NBUF + 1) + 16;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int RING_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * NBUF + 1) + 16;
+    static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(CPT % 16 == 0, "TMEM loads are 16 columns wide");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -69,15 +88,15 @@ struct Cfg {
 
 struct KArgs {
     int M, N, G;
-    int Mp;          // activation-scale column stride (rows padded to 4)
+    int NB;          // weight row blocks
     int swap;        // MMA-M operand is the weight
     int tiles_tok;   // token tiles (MMA-M tiles when !swap, MMA-N tiles when swap)
-    int split;
-    int num_items;
+    int tiles;
+    int split;       // >= 1: split-K round robin; 0: stream-K
+    int num_items;   // split-K: tiles * split
+    long long units; // stream-K: tiles * G
     int ue8m0;
     int out_dtype;
-    const void* sa;
-    const float* sw;
     void* out;
     float* partials;
     unsigned* counters;
@@ -85,41 +104,95 @@ struct KArgs {
     unsigned long long timeout_ns;
 };
 
-struct Item {
-    int tile;     // linear tile index
-    int tok0;     // first token of the tile
-    int w0;       // first weight row (n) of the tile
-    int kb0, kb1; // K slab range
-    int split;    // index of this split
+// One contiguous run of K slabs of one tile.
+struct Seg {
+    int tile;
+    int kb0, kb1;
+    int part;    // index of this segment among the tile's segments (K order)
+    int nparts;  // segments of this tile (1: the tile is stored directly)
 };
 
-template <int BN>
-__device__ __forceinline__ Item decode_item(const KArgs& a, int item) {
-    Item it;
-    it.tile = item / a.split;
-    it.split = item - it.tile * a.split;
-    const int wt = it.tile / a.tiles_tok;        // weight tile (slow)
-    const int tt = it.tile - wt * a.tiles_tok;   // token tile (fast: neighbours share weights)
-    if (a.swap) {
-        it.w0 = wt * BM;
-        it.tok0 = tt * BN;
-    } else {
-        it.w0 = wt * BN;
-        it.tok0 = tt * BM;
-    }
-    it.kb0 = static_cast<int>((static_cast<long long>(it.split) * a.G) / a.split);
-    it.kb1 = static_cast<int>((static_cast<long long>(it.split + 1) * a.G) / a.split);
-    return it;
+// Stream-K ownership: CTA c owns units [c*T/P, (c+1)*T/P).
+__device__ __forceinline__ long long sk_begin(long long c, long long T, long long P) {
+    return c * T / P;
+}
+__device__ __forceinline__ int sk_owner(long long u, long long T, long long P) {
+    return static_cast<int>(((u + 1) * P - 1) / T);
 }
 
-__device__ __forceinline__ float act_scale(const KArgs& a, int m, int kb) {
-    if (m >= a.M) return 0.0f;
-    if (a.ue8m0) {
-        const uint32_t w =
-            __ldg(static_cast<const uint32_t*>(a.sa) + static_cast<int64_t>(kb >> 2) * a.Mp + m);
-        return __uint_as_float(((w >> (8 * (kb & 3))) & 0xFFu) << 23);
+// Iterates this CTA's segments in order (identically in every role).
+struct WorkIter {
+    long long u, u_end;  // stream-K
+    int item;            // split-K
+
+    __device__ void init(const KArgs& a) {
+        if (a.split == 0) {
+            u = sk_begin(blockIdx.x, a.units, gridDim.x);
+            u_end = sk_begin(blockIdx.x + 1, a.units, gridDim.x);
+        } else {
+            item = blockIdx.x;
+        }
     }
-    return __ldg(static_cast<const float*>(a.sa) + static_cast<int64_t>(kb) * a.Mp + m);
+
+    __device__ bool next(const KArgs& a, Seg& s) {
+        if (a.split == 0) {
+            if (u >= u_end) return false;
+            s.tile = static_cast<int>(u / a.G);
+            s.kb0 = static_cast<int>(u - static_cast<long long>(s.tile) * a.G);
+            const long long left = u_end - u;
+            s.kb1 = left < a.G - s.kb0 ? s.kb0 + static_cast<int>(left) : a.G;
+            const long long t0 = static_cast<long long>(s.tile) * a.G;
+            const int c_first = sk_owner(t0, a.units, gridDim.x);
+            const int c_last = sk_owner(t0 + a.G - 1, a.units, gridDim.x);
+            s.nparts = c_last - c_first + 1;
+            s.part = static_cast<int>(blockIdx.x) - c_first;
+            u += s.kb1 - s.kb0;
+            return true;
+        }
+        if (item >= a.num_items) return false;
+        s.tile = item / a.split;
+        s.part = item - s.tile * a.split;
+        s.nparts = a.split;
+        s.kb0 = static_cast<int>((static_cast<long long>(s.part) * a.G) / a.split);
+        s.kb1 = static_cast<int>((static_cast<long long>(s.part + 1) * a.G) / a.split);
+        item += gridDim.x;
+        return true;
+    }
+};
+
+// Workspace slot of segment `p` of `tile`.
+__device__ __forceinline__ int64_t part_slot(const KArgs& a, int tile, int p) {
+    if (a.split == 0) {
+        const long long t0 = static_cast<long long>(tile) * a.G;
+        const int c = sk_owner(t0, a.units, gridDim.x) + p;
+        const long long b = sk_begin(c, a.units, gridDim.x);
+        return 2 * static_cast<int64_t>(c) + ((b / a.G) == tile ? 0 : 1);
+    }
+    return static_cast<int64_t>(tile) * a.split + p;
+}
+
+struct TileOrigin {
+    int tok0;  // first token
+    int w0;    // first weight row (n)
+};
+
+template <bool SWAP, int BN>
+__device__ __forceinline__ TileOrigin tile_origin(const KArgs& a, int tile) {
+    const int wt = tile / a.tiles_tok;       // weight tile (slow)
+    const int tt = tile - wt * a.tiles_tok;  // token tile (fast: neighbours share weights)
+    TileOrigin o;
+    if (SWAP) {
+        o.w0 = wt * BM;
+        o.tok0 = tt * BN;
+    } else {
+        o.w0 = wt * BN;
+        o.tok0 = tt * BM;
+    }
+    return o;
+}
+
+__device__ __forceinline__ float ue8m0_value(uint32_t word, int kb) {
+    return __uint_as_float(((word >> (8 * (kb & 3))) & 0xFFu) << 23);
 }
 
 __device__ __forceinline__ void store_out1(void* out, int dtype, int64_t idx, float v) {
@@ -135,13 +208,13 @@ __device__ __forceinline__ void store_out1(void* out, int dtype, int64_t idx, fl
 __device__ __forceinline__ void store_out8(void* out, int dtype, int64_t idx, float v0, float v1,
                                            float v2, float v3, float v4, float v5, float v6,
                                            float v7) {
-    const float v[8] = {v0, v1, v2, v3, v4, v5, v6, v7};
     if (dtype == FP8BQ_FP32) {
         float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
-        p[0] = make_float4(v[0], v[1], v[2], v[3]);
-        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+        p[0] = make_float4(v0, v1, v2, v3);
+        p[1] = make_float4(v4, v5, v6, v7);
         return;
     }
+    const float v[8] = {v0, v1, v2, v3, v4, v5, v6, v7};
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -165,20 +238,34 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity,
     }
 }
 
-template <int BN>
+// Warp-uniform bounded wait: lane 0 waits, the warp follows its verdict, so
+// the warp-collective instructions after it are always reached together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* status, uint64_t tmo, int code) {
+    int got = 1;
+    if ((threadIdx.x & 31) == 0) got = mbar_wait_bounded(bar, parity, abort, status, tmo, code);
+    return __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
+}
+
+template <bool SWAP, int BN>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K]
-                const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K]
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
+                const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
+                const __grid_constant__ CUtensorMap tm_sa,     // act scales [cols][Mp] 4-byte
+                const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                 const KArgs a) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                                // STAGES x [128 rows x 128 B]
-    uint8_t* sB = smem + C::STAGES * C::A_BYTES;       // STAGES x [BN rows x 128 B]
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t* sA = smem;                            // STAGES x [128 rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;   // STAGES x [BN rows x 128 B]
+    uint8_t* ring = smem + C::RING_OFF;            // SR x SLOT_BYTES
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + C::STAGES;
-    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* sfull = empty + C::STAGES;
+    uint64_t* sempty = sfull + SR;
+    uint64_t* tfull = sempty + SR;
     uint64_t* tempty = tfull + C::NBUF;
     uint64_t* mma_done = tempty + C::NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -192,6 +279,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sempty[s], C::EPI_WARPS);
+        }
         for (int b = 0; b < C::NBUF; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], C::EPI_WARPS);
@@ -201,6 +292,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tm_mma_m);
         tma_prefetch_desc(&tm_mma_n);
+        tma_prefetch_desc(&tm_sa);
+        tma_prefetch_desc(&tm_sw);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -215,6 +308,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t tmo = a.timeout_ns;
     const int code = static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT);
+    // bytes one scale slot receives: the activation scales of the tile's
+    // tokens plus one (swap-AB, 128-row weight tile) or two (256-wide weight
+    // tile) 16-byte chunks of weight scales
+    const int sw_chunks = (!SWAP && BN > BM) ? 2 : 1;
+    const uint32_t slot_tx = 4u * (SWAP ? BN : BM) + 16u * sw_chunks;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -222,17 +320,21 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             // weights stream once; activations are re-read by other tiles
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
-            const uint64_t pol_m = a.swap ? pol_w : pol_a;
-            const uint64_t pol_n = a.swap ? pol_a : pol_w;
-            int stage = 0;
-            uint32_t phase = 0;
-            long long fills = 0;
-            for (int item = blockIdx.x; item < a.num_items; item += gridDim.x) {
-                const Item it = decode_item<BN>(a, item);
-                const int row_m = a.swap ? it.w0 : it.tok0;
-                const int row_n = a.swap ? it.tok0 : it.w0;
-                bool ok = true;
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            const uint64_t pol_m = SWAP ? pol_w : pol_a;
+            const uint64_t pol_n = SWAP ? pol_a : pol_w;
+            int stage = 0, slot = 0;
+            uint32_t phase = 0, sphase = 0;
+            long long fills = 0, sfills = 0;
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+                const int row_m = SWAP ? o.w0 : o.tok0;
+                const int row_n = SWAP ? o.tok0 : o.w0;
+                const int nb = o.w0 / BK;
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, tmo,
                                            code)) {
                         ok = false;
@@ -248,14 +350,32 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (!mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag, a.status, tmo,
+                                           code)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sl = ring + slot * SLOT_BYTES;
+                    mbar_arrive_expect_tx(&sfull[slot], slot_tx);
+                    tma_load_2d(sl, &tm_sa, &sfull[slot], o.tok0, a.ue8m0 ? (kb >> 2) : kb);
+                    const int e0 = nb * a.G + kb;
+                    tma_load_2d(sl + SLOT_SW, &tm_sw, &sfull[slot], e0 & ~3, 0);
+                    if (sw_chunks == 2)
+                        tma_load_2d(sl + SLOT_SW + SLOT_SW_STEP, &tm_sw, &sfull[slot],
+                                    (e0 + a.G) & ~3, 0);
+                    ++sfills;
+                    if (++slot == SR) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
                 }
-                if (!ok) break;
             }
             // Let every issued copy land before the CTA can exit.
-            const long long first = fills > C::STAGES ? fills - C::STAGES : 0;
-            for (long long f = first; f < fills; ++f)
+            for (long long f = fills > C::STAGES ? fills - C::STAGES : 0; f < fills; ++f)
                 mbar_wait_drain(&full[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1),
                                 tmo);
+            for (long long f = sfills > SR ? sfills - SR : 0; f < sfills; ++f)
+                mbar_wait_drain(&sfull[f % SR], static_cast<uint32_t>((f / SR) & 1), tmo);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -263,10 +383,12 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, bphase = 0;
-            for (int item = blockIdx.x; item < a.num_items; item += gridDim.x) {
-                const Item it = decode_item<BN>(a, item);
-                bool ok = true;
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait_bounded(&tempty[buf], bphase ^ 1u, abort_flag, a.status, tmo,
                                            code) ||
                         !mbar_wait_bounded(&full[stage], phase, abort_flag, a.status, tmo, code)) {
@@ -292,7 +414,6 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                         bphase ^= 1u;
                     }
                 }
-                if (!ok) break;
             }
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0, tmo);
@@ -305,70 +426,64 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         const int row = quad * 32 + lane;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                 static_cast<uint32_t>(chalf * C::CPT);
-        constexpr int SA_REGS = C::CPT >= 32 ? C::CPT / 32 : 1;
-        int buf = 0;
-        uint32_t bphase = 0;
+        int buf = 0, slot = 0;
+        uint32_t bphase = 0, sphase = 0;
+        WorkIter wi;
+        wi.init(a);
+        Seg sg;
         bool ok = true;
-        for (int item = blockIdx.x; item < a.num_items && ok; item += gridDim.x) {
-            const Item it = decode_item<BN>(a, item);
+        while (ok && wi.next(a, sg)) {
+            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const int nb = o.w0 / BK;
             float acc[C::CPT];
 #pragma unroll
             for (int j = 0; j < C::CPT; ++j) acc[j] = 0.0f;
 
-            // Per-slab scale factors.  Normal: one factor per thread (its row
-            // is a token m, its columns lie in one 128-wide weight block).
-            // Swap-AB: sw is uniform over the tile (128 weight rows = one
-            // block); sa varies per column (token), held one per lane and
-            // broadcast by shuffles.
-            const int m_row = it.tok0 + row;                       // normal
-            const int nb_norm = (it.w0 + chalf * C::CPT) / BK;     // normal
-            const int nb_swap = it.w0 / BK;                        // swap
-            const int tok_col0 = it.tok0 + chalf * C::CPT;         // swap
-            const int NB = (a.N + BK - 1) / BK;
-
-            auto load_factor = [&](int kb, float (&sreg)[SA_REGS], float& sw) {
-                if (!a.swap) {
-                    const float s_w = nb_norm < NB ? __ldg(a.sw + static_cast<int64_t>(nb_norm) * a.G + kb) : 0.0f;
-                    sreg[0] = act_scale(a, m_row, kb);
-                    sw = s_w;
-                } else {
-                    sw = __ldg(a.sw + static_cast<int64_t>(nb_swap) * a.G + kb);
-#pragma unroll
-                    for (int r = 0; r < SA_REGS; ++r) {
-                        const int c = r * 32 + lane;
-                        sreg[r] = c < C::CPT ? act_scale(a, tok_col0 + c, kb) : 0.0f;
-                    }
-                }
-            };
-
-            float sa_next[SA_REGS], sw_next;
-            load_factor(it.kb0, sa_next, sw_next);
-            for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                float sa_cur[SA_REGS];
-#pragma unroll
-                for (int r = 0; r < SA_REGS; ++r) sa_cur[r] = sa_next[r];
-                const float sw_cur = sw_next;
-                if (kb + 1 < it.kb1) load_factor(kb + 1, sa_next, sw_next);
-
-                // lane 0 waits (bounded), the warp follows its verdict, so the
-                // warp-collective TMEM loads below are always reached together
-                int got = 1;
-                if (lane == 0)
-                    got = mbar_wait_bounded(&tfull[buf], bphase, abort_flag, a.status, tmo, code)
-                              ? 1
-                              : 0;
-                got = __shfl_sync(0xFFFFFFFFu, got, 0);
-                if (!got) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (!warp_wait(&sfull[slot], sphase, abort_flag, a.status, tmo, code) ||
+                    !warp_wait(&tfull[buf], bphase, abort_flag, a.status, tmo, code)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint8_t* sl = ring + slot * SLOT_BYTES;
+                // weight scale of this warp's columns (swap: the tile's block;
+                // normal: block of this column half)
+                const int e = (nb + (SWAP ? 0 : (chalf * C::CPT) / BK)) * a.G + kb;
+                const int chunk = (SWAP || chalf * C::CPT < BK) ? 0 : 1;
+                const float swv =
+                    reinterpret_cast<const float*>(sl + SLOT_SW + SLOT_SW_STEP * chunk)[e & 3];
+                float f_norm = 0.0f;
+                if (!SWAP) {
+                    const float sam = a.ue8m0
+                                          ? ue8m0_value(reinterpret_cast<const uint32_t*>(sl)[row], kb)
+                                          : reinterpret_cast<const float*>(sl)[row];
+                    f_norm = (o.tok0 + row < a.M) ? sam * swv : 0.0f;
+                }
                 const uint32_t t_buf = t_lane + static_cast<uint32_t>(buf * BN);
-                const float f_norm = sa_cur[0] * sw_cur;
 #pragma unroll
                 for (int c0 = 0; c0 < C::CPT; c0 += 16) {
                     uint32_t r[16];
                     tmem_ld16(t_buf + c0, r);
+                    float f[16];
+                    if (SWAP) {
+                        // per-column (token) factors: broadcast reads of the slot
+                        const int t0 = chalf * C::CPT + c0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w = reinterpret_cast<const uint4*>(sl)[(t0 >> 2) + q];
+                            const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float s = a.ue8m0 ? ue8m0_value(ws4[i], kb)
+                                                        : __uint_as_float(ws4[i]);
+                                f[4 * q + i] = (o.tok0 + t0 + 4 * q + i < a.M) ? s * swv : 0.0f;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = f_norm;
+                    }
                     tmem_ld_wait();
                     if (c0 + 16 == C::CPT) {
                         // all of this buffer is in registers: hand it back
@@ -377,59 +492,80 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                         if (lane == 0) mbar_arrive(&tempty[buf]);
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = c0 + j;
-                        float f;
-                        if (!a.swap) {
-                            f = f_norm;
-                        } else {
-                            f = __shfl_sync(0xFFFFFFFFu, sa_cur[col >> 5], col & 31) * sw_cur;
-                        }
-                        acc[col] = fmaf(__uint_as_float(r[j]), f, acc[col]);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        acc[c0 + j] = fmaf(__uint_as_float(r[j]), f[j], acc[c0 + j]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[slot]);
                 if (++buf == C::NBUF) {
                     buf = 0;
                     bphase ^= 1u;
                 }
+                if (++slot == SR) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
             }
             if (!ok) break;
 
-            // ---------------------------------------------- split-K reduction
+            // -------------------------------------------- split reduction
             // Each epilogue warp owns a fixed 32-row x CPT-column sub-block of
             // the tile and takes its own ticket for it, so no barrier between
             // warps is needed (and none can be left waiting after an abort).
-            if (a.split > 1) {
-                float* part = a.partials + static_cast<int64_t>(it.tile) * a.split * (BM * BN);
-                float* mine = part + static_cast<int64_t>(it.split) * (BM * BN);
+            if (sg.nparts > 1) {
+                constexpr int64_t TILE = BM * BN;
+                float* mine = a.partials + part_slot(a, sg.tile, sg.part) * TILE;
 #pragma unroll
                 for (int j = 0; j < C::CPT; ++j)
                     __stcg(mine + (chalf * C::CPT + j) * BM + row, acc[j]);
                 __threadfence();
                 __syncwarp();
-                unsigned* ctr = a.counters + static_cast<int64_t>(it.tile) * kCountersPerTile + ew;
+                unsigned* ctr = a.counters + static_cast<int64_t>(sg.tile) * kCountersPerTile + ew;
                 unsigned prev = 0;
                 if (lane == 0) prev = atomicAdd(ctr, 1u);
                 prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-                if (prev != static_cast<unsigned>(a.split - 1)) continue;
+                if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
                 __threadfence();
+                // sum the segments in K order, 16 columns x PU segments of
+                // independent loads at a time
+                constexpr int PU = C::CPT >= 128 ? 1 : C::CPT >= 64 ? 2 : 4;
 #pragma unroll
-                for (int j = 0; j < C::CPT; ++j) {
-                    const int64_t off = (chalf * C::CPT + j) * BM + row;
-                    float v = it.split == 0 ? acc[j] : __ldcg(part + off);
-                    for (int s = 1; s < a.split; ++s)
-                        v += (s == it.split) ? acc[j]
-                                             : __ldcg(part + static_cast<int64_t>(s) * (BM * BN) + off);
-                    acc[j] = v;
+                for (int c0 = 0; c0 < C::CPT; c0 += 16) {
+                    float v[16];
+                    for (int p0 = 0; p0 < sg.nparts; p0 += PU) {
+                        float t[PU][16];
+#pragma unroll
+                        for (int q = 0; q < PU; ++q) {
+                            const int p = p0 + q;
+                            if (p < sg.nparts && p != sg.part) {
+                                const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
+                                                   (chalf * C::CPT + c0) * BM + row;
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) t[q][j] = __ldcg(src + j * BM);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < PU; ++q) {
+                            const int p = p0 + q;
+                            if (p >= sg.nparts) break;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float x = (p == sg.part) ? acc[c0 + j] : t[q][j];
+                                v[j] = (p == 0) ? x : v[j] + x;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[c0 + j] = v[j];
                 }
                 if (lane == 0) *ctr = 0u;  // ready for the next call
             }
 
             // ------------------------------------------------------- store
-            if (!a.swap) {
-                const int m = it.tok0 + row;
+            if (!SWAP) {
+                const int m = o.tok0 + row;
                 if (m < a.M) {
-                    const int n0 = it.w0 + chalf * C::CPT;
+                    const int n0 = o.w0 + chalf * C::CPT;
 #pragma unroll
                     for (int j = 0; j < C::CPT; j += 8)
                         if (n0 + j < a.N)
@@ -438,13 +574,14 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                                        acc[j + 5], acc[j + 6], acc[j + 7]);
                 }
             } else {
-                const int n = it.w0 + row;
+                const int n = o.w0 + row;
+                const int t0 = o.tok0 + chalf * C::CPT;
                 if (n < a.N) {
 #pragma unroll
-                    for (int j = 0; j < C::CPT; ++j) {
-                        const int t = tok_col0 + j;
-                        if (t < a.M) store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, acc[j]);
-                    }
+                    for (int j = 0; j < C::CPT; ++j)
+                        if (t0 + j < a.M)
+                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t0 + j) * a.N + n,
+                                       acc[j]);
                 }
             }
         }
@@ -461,19 +598,28 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
 
 // ------------------------------------------------------------------ host
 
-bool encode_map(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapSwizzle swz) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, K] e4m3 operand, 128-byte swizzled boxes of box_rows x 128.
+bool encode_operand(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows,
+                    uint32_t box_rows) {
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {K};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int BN>
+template <bool SWAP, int BN>
 cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
     using C = Cfg<BN>;
     static int attr_done[64] = {0};
@@ -481,43 +627,65 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        err = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::SMEM);
+        err = cudaFuncSetAttribute(gemm_kernel<SWAP, BN>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (err != cudaSuccess) return err;
         attr_done[dev] = 1;
     }
-    const bool swap = p.kind == FP8BQ_KIND_SWAP_AB;
-    CUtensorMap tm_m, tm_n;
+    const bool swap = SWAP;
     const uint64_t K = static_cast<uint64_t>(g.K);
+    const int G = static_cast<int>(g.K / BK);
+    const int NB = static_cast<int>((g.N + BK - 1) / BK);
+    const uint64_t Mp = static_cast<uint64_t>(pad_rows4(g.M));
+    CUtensorMap tm_m, tm_n, tm_sa, tm_sw;
     bool ok;
     if (swap) {
-        ok = encode_map(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), BM) &&
-             encode_map(&tm_n, g.a_q, K, static_cast<uint64_t>(g.M), BN);
+        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), BM) &&
+             encode_operand(&tm_n, g.a_q, K, static_cast<uint64_t>(g.M), BN);
     } else {
-        ok = encode_map(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
-             encode_map(&tm_n, g.w_q, K, static_cast<uint64_t>(g.N), BN);
+        ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
+             encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(g.N), BN);
     }
-    if (!ok) return cudaErrorInvalidValue;
+    {
+        // activation scales: [cols][Mp] of 4-byte words; box = the tile's tokens of one column
+        const cuuint64_t dims[2] = {Mp, static_cast<cuuint64_t>(g.ue8m0 ? (G + 3) / 4 : G)};
+        const cuuint64_t strides[1] = {Mp * 4};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(swap ? BN : BM), 1};
+        ok = ok && encode(&tm_sa, g.ue8m0 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, g.a_s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+        // weight scales: the flat [NB*G] fp32 array as one row, 16-byte boxes
+        const cuuint64_t flat = static_cast<cuuint64_t>(NB) * G;
+        const cuuint64_t wdims[2] = {flat, 1};
+        const cuuint64_t wstrides[1] = {(flat * 4 + 15) / 16 * 16};
+        const cuuint32_t wbox[2] = {4, 1};
+        ok = ok && encode(&tm_sw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, g.w_s, wdims, wstrides, wbox,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok) {
+        log_error("tensor-map encoding failed for the GEMM operands or scales");
+        return cudaErrorInvalidValue;
+    }
 
     KArgs a;
     a.M = static_cast<int>(g.M);
     a.N = static_cast<int>(g.N);
-    a.G = static_cast<int>(g.K / BK);
-    a.Mp = static_cast<int>(pad_rows4(g.M));
+    a.G = G;
+    a.NB = NB;
     a.swap = swap ? 1 : 0;
     a.tiles_tok = p.tiles_tok;
+    a.tiles = p.tiles_tok * p.tiles_w;
     a.split = p.split;
     a.num_items = p.num_items;
+    a.units = static_cast<long long>(a.tiles) * G;
     a.ue8m0 = g.ue8m0;
     a.out_dtype = g.out_dtype;
-    a.sa = g.a_s;
-    a.sw = g.w_s;
     a.out = g.out;
     // workspace: [tile counters: fixed kCounterRegion prefix] [fp32 partial tiles]
-    a.counters = p.split > 1 ? static_cast<unsigned*>(g.workspace) : nullptr;
-    a.partials = p.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(g.workspace) +
-                                                        kCounterRegion + g.ws_data_offset)
-                             : nullptr;
+    a.counters = p.ws_bytes ? static_cast<unsigned*>(g.workspace) : nullptr;
+    a.partials = p.ws_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(g.workspace) +
+                                                       kCounterRegion + g.ws_data_offset)
+                            : nullptr;
     a.status = g.status;
     a.timeout_ns = g.timeout_ns;
 
@@ -531,15 +699,10 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = g.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, tm_m, tm_n, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
 }  // namespace
-
-static size_t workspace_for(int tiles, int split, int bn) {
-    if (split <= 1) return 0;
-    return kCounterRegion + static_cast<size_t>(tiles) * split * BM * bn * sizeof(float);
-}
 
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
                     GemmPlan* p) {
@@ -551,7 +714,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     } else {
         if (v.block_n != 128 && v.block_n != 256) return false;
     }
-    if (v.split < 1 || v.split > 64 || v.split > G) return false;
+    if (v.split < 0 || v.split > 64 || v.split > G) return false;
     if (v.grid < 0) return false;
     p->kind = v.kind;
     p->bn = v.block_n;
@@ -564,29 +727,40 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
         p->tiles_w = static_cast<int>((N + v.block_n - 1) / v.block_n);
     }
     const long long tiles = static_cast<long long>(p->tiles_tok) * p->tiles_w;
-    const long long items = tiles * v.split;
-    if (items <= 0 || items > (1LL << 30)) return false;
-    // split-K tickets live in the fixed counter prefix of the workspace
-    if (v.split > 1 && tiles * kCountersPerTile * 4 > kCounterRegion) return false;
-    p->num_items = static_cast<int>(items);
+    if (tiles <= 0 || tiles > (1LL << 30)) return false;
     const int g = v.grid > 0 ? v.grid : num_sms;
-    p->grid = static_cast<int>(items < g ? items : g);
-    p->ws_bytes = workspace_for(static_cast<int>(tiles), v.split, v.block_n);
+    const size_t tile_bytes = static_cast<size_t>(BM) * v.block_n * sizeof(float);
+    if (v.split == 0) {
+        // stream-K: one CTA per equal share of the tiles x G (tile, slab) units
+        const long long units = tiles * G;
+        p->num_items = 0;
+        p->grid = static_cast<int>(units < g ? units : g);
+        p->ws_bytes = kCounterRegion + static_cast<size_t>(2) * p->grid * tile_bytes;
+    } else {
+        const long long items = tiles * v.split;
+        if (items > (1LL << 30)) return false;
+        p->num_items = static_cast<int>(items);
+        p->grid = static_cast<int>(items < g ? items : g);
+        p->ws_bytes = v.split > 1 ? kCounterRegion + static_cast<size_t>(items) * tile_bytes : 0;
+    }
+    // split tickets live in the fixed counter prefix of the workspace
+    if (p->ws_bytes && tiles * kCountersPerTile * 4 > static_cast<long long>(kCounterRegion))
+        return false;
     return true;
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
     if (p.kind == FP8BQ_KIND_SWAP_AB) {
         switch (p.bn) {
-            case 16: return launch_bn<16>(p, g, stream);
-            case 32: return launch_bn<32>(p, g, stream);
-            case 64: return launch_bn<64>(p, g, stream);
-            case 128: return launch_bn<128>(p, g, stream);
+            case 16: return launch_bn<true, 16>(p, g, stream);
+            case 32: return launch_bn<true, 32>(p, g, stream);
+            case 64: return launch_bn<true, 64>(p, g, stream);
+            case 128: return launch_bn<true, 128>(p, g, stream);
         }
     } else {
         switch (p.bn) {
-            case 128: return launch_bn<128>(p, g, stream);
-            case 256: return launch_bn<256>(p, g, stream);
+            case 128: return launch_bn<false, 128>(p, g, stream);
+            case 256: return launch_bn<false, 256>(p, g, stream);
         }
     }
     return cudaErrorInvalidValue;

@@ -94,4 +94,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
+// One line to stderr when FP8BQ_LOG=1 (diagnostics only).
+void log_error(const char* what);
+
 }  // namespace fp8bq

@@ -1,0 +1,62 @@
+"""Runs one GEMM (or linear) problem a few times -- the small, self-contained
+command the profiler captures.
+
+    python -m block_scaled_fp8_group_gb300.runcase --m 8 --n 18432 --k 7168 \
+        --fmt ue8m0 --iters 3 [--variant swap/16/0] [--op gemm|linear|quant]
+
+Inputs are the decode-sweep distributions from ``synth`` (bf16 N(0,1) with 1%
+outlier channels, bf16 N(0,0.02) weights), quantised on the GPU.
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+import torch
+
+from . import fp8bq, synth
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--m", type=int, required=True)
+    ap.add_argument("--n", type=int, required=True)
+    ap.add_argument("--k", type=int, required=True)
+    ap.add_argument("--fmt", default="ue8m0", choices=("fp32", "ue8m0"))
+    ap.add_argument("--out", default="bf16", choices=("bf16", "fp16", "fp32"))
+    ap.add_argument("--op", default="gemm", choices=("gemm", "linear", "quant"))
+    ap.add_argument("--variant", default=None, help="kind/block_n/split[/grid]")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+    dev = torch.device("cuda")
+    out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[args.out]
+    x = torch.from_numpy(synth.act_decode(args.m, args.k).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    if args.op == "quant":
+        for _ in range(args.iters):
+            fp8bq.fp8bq_quant_act(x, args.fmt)
+        torch.cuda.synchronize()
+        return
+    w = torch.from_numpy(synth.weight_bf16(args.n, args.k).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    wq, ws = fp8bq.fp8bq_quant_weight(w, args.fmt)
+    aq, as_ = fp8bq.fp8bq_quant_act(x, args.fmt)
+    v = None
+    if args.variant:
+        parts = args.variant.split("/")
+        v = fp8bq.make_variant(parts[0], int(parts[1]), int(parts[2]),
+                               int(parts[3]) if len(parts) > 3 else 0)
+    for _ in range(args.iters):
+        if args.op == "linear":
+            fp8bq.fp8bq_linear(x, wq, ws, fmt=args.fmt, out_dtype=out_dt)
+        elif v is not None:
+            fp8bq.fp8bq_gemm_variant(aq, as_, wq, ws, v, fmt=args.fmt, out_dtype=out_dt)
+        else:
+            fp8bq.fp8bq_gemm(aq, as_, wq, ws, fmt=args.fmt, out_dtype=out_dt)
+    torch.cuda.synchronize()
+    if fp8bq.fp8bq_device_status() != 0:
+        raise SystemExit("device wait timed out")
+
+
+if __name__ == "__main__":
+    main()

@@ -26,8 +26,9 @@ def upload(qa, sa, qw, sw):
     return to_dev(qa), scales_to_dev(sa), to_dev(qw), to_dev(sw)
 
 
-VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (1, 2, 3)] +
-            [("normal", bn, s) for bn in (128, 256) for s in (1, 2, 5)])
+# split 0 = stream-K (equal shares of the (tile, K slab) units per CTA)
+VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (0, 1, 2, 3)] +
+            [("normal", bn, s) for bn in (128, 256) for s in (0, 1, 2, 5)])
 
 
 @pytest.mark.parametrize("kind,bn,split", VARIANTS)
@@ -53,22 +54,25 @@ def test_persistent_grid_loops_over_items(fp8bq, grid):
     xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_prefill)
     ref = oracle_full(qa, sa, qw, sw, True)
     d = upload(qa, sa, qw, sw)
-    for v in (fp8bq.make_variant("swap", 64, 3, grid), fp8bq.make_variant("normal", 128, 2, grid)):
+    for v in (fp8bq.make_variant("swap", 64, 3, grid), fp8bq.make_variant("normal", 128, 2, grid),
+              fp8bq.make_variant("swap", 32, 0, grid), fp8bq.make_variant("normal", 256, 0, grid)):
         o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=torch.float32)
         torch.cuda.synchronize()
         check_gemm(o.cpu().numpy(), ref, "fp32", f"grid {grid} {v.as_dict()}")
 
 
-def test_split_k_is_bit_stable_and_reusable(fp8bq):
+@pytest.mark.parametrize("split,grid", [(7, 0), (0, 0), (0, 13)])
+def test_split_k_is_bit_stable_and_reusable(fp8bq, split, grid):
     M, N, K = 24, 1024, 2048
     xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_decode)
     d = upload(qa, sa, qw, sw)
-    v = fp8bq.make_variant("swap", 32, 7)
+    v = fp8bq.make_variant("swap", 32, split, grid)
     outs = [fp8bq.fp8bq_gemm_variant(*d, v, out_dtype=torch.float32) for _ in range(4)]
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
-    check_gemm(outs[0].cpu().numpy(), oracle_full(qa, sa, qw, sw, False), "fp32", "split 7")
+    check_gemm(outs[0].cpu().numpy(), oracle_full(qa, sa, qw, sw, False), "fp32",
+               f"split {split} grid {grid}")
 
 
 def test_fp16_output(fp8bq):
