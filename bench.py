@@ -271,18 +271,25 @@ def run_gpu(args, rank, world):
     ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
     variants = {p: fp8bq.fp8bq_select_variant(*p, "ue8m0", torch.bfloat16) for p in probs}
 
-    def launch_step(ev_pairs):
+    def step_linear():
+        # the timed step: one fp8bq_linear call (quant + GEMM, PDL) per problem
+        for p in probs:
+            M, N, K = p
+            fp8bq.fp8bq_linear(xs[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
+                               out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
+
+    def step_split(ev_pairs):
+        # the instrumented step: quant and GEMM as separate calls, with timing
+        # events around every GEMM launch
         for i, p in enumerate(probs):
             M, N, K = p
             fp8bq.fp8bq_quant_act(xs[p], "ue8m0", q=aqs[p], s=ass[p])
-            if ev_pairs is not None:
-                ev_pairs[i][0].record()
+            ev_pairs[i][0].record()
             fp8bq.fp8bq_gemm(aqs[p], ass[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
                              out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
-            if ev_pairs is not None:
-                ev_pairs[i][1].record()
+            ev_pairs[i][1].record()
 
-    # ---- timing instruments: graph with external timing events, else eager
+    # ---- timing instruments: CUDA graphs with external timing events, else eager
     mode = args.mode
     ext_ok = True
     try:
@@ -295,31 +302,48 @@ def run_gpu(args, rank, world):
         (lambda: torch.cuda.Event(enable_timing=True))
     ev_pairs = [(mk(), mk()) for _ in probs]
     ev_start, ev_end = mk(), mk()
+    ev2_start, ev2_end = mk(), mk()
 
-    launch_step(None)  # first launches: loads the table, sets kernel attributes
+    # first launches: load the table, set kernel attributes
+    step_linear()
+    step_split(ev_pairs)
     torch.cuda.synchronize()
-    graph = None
+    graphs = None
     if mode == "graph":
-        graph = torch.cuda.CUDAGraph()
+        g_lin, g_split = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            with torch.cuda.graph(graph, stream=side):
+            with torch.cuda.graph(g_lin, stream=side):
                 ev_start.record()
-                launch_step(ev_pairs)
+                step_linear()
                 ev_end.record()
+            with torch.cuda.graph(g_split, stream=side):
+                ev2_start.record()
+                step_split(ev_pairs)
+                ev2_end.record()
         torch.cuda.synchronize()
+        graphs = (g_lin, g_split)
 
-    def run_one():
-        if graph is not None:
-            graph.replay()
+    def run_timed():
+        if graphs is not None:
+            graphs[0].replay()
         else:
             ev_start.record()
-            launch_step(ev_pairs)
+            step_linear()
             ev_end.record()
 
+    def run_instr():
+        if graphs is not None:
+            graphs[1].replay()
+        else:
+            ev2_start.record()
+            step_split(ev_pairs)
+            ev2_end.record()
+
     for _ in range(args.warmup):
-        run_one()
+        run_timed()
+        run_instr()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -327,13 +351,12 @@ def run_gpu(args, rank, world):
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
-    step_ms, gemm_ms = [], np.zeros(len(probs))
+    step_ms = []
     t_wall0 = time.perf_counter()
     for _ in range(args.steps):
-        run_one()
+        run_timed()
         ev_end.synchronize()
         step_ms.append(ev_start.elapsed_time(ev_end))
-        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_pairs])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -344,7 +367,15 @@ def run_gpu(args, rank, world):
         t = torch.tensor([step_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         step_s = float(t.item())
-    gemm_us = gemm_ms / args.steps * 1e3
+    # instrumented pass (same problems, same cold weights): per-GEMM durations
+    n_instr = max(1, min(args.steps, args.instr_steps))
+    gemm_ms, split_ms = np.zeros(len(probs)), []
+    for _ in range(n_instr):
+        run_instr()
+        ev2_end.synchronize()
+        split_ms.append(ev2_start.elapsed_time(ev2_end))
+        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_pairs])
+    gemm_us = gemm_ms / n_instr * 1e3
     launches = args.steps * 2 * len(probs)
 
     # ---- end to end through the public fp8bq_linear call with host buffers
@@ -423,8 +454,12 @@ def run_gpu(args, rank, world):
         "config": {"workload": WORKLOAD, "problems_per_step": len(probs),
                    "l2": "inputs larger than L2: each GEMM reads its own weight copy "
                          "(3.2 GB of weights per step)",
-                   "timing": f"{mode}: CUDA events on the launching stream per step and "
-                             "around every GEMM launch",
+                   "timing": f"{mode}: step = fp8bq_linear per problem (PDL between "
+                             "kernels), CUDA events on the launching stream around each step; "
+                             "per-GEMM durations from an instrumented pass of the same step "
+                             "(quant and GEMM as separate calls, events around every GEMM)",
+                   "instrumented_step_ms": round(float(np.mean(split_ms)), 4),
+                   "instrumented_steps": n_instr,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk, "per_shape": per, "wall_timed_s": round(t_wall, 3),
@@ -442,6 +477,7 @@ def main():
     ap.add_argument("--impl", choices=("fp8bq", "reference"), default="fp8bq")
     ap.add_argument("--mode", choices=("graph", "eager"), default="graph")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--instr-steps", type=int, default=200)
     ap.add_argument("--oracle-rows", type=int, default=4)
     ap.add_argument("--steps-ref", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")

@@ -261,8 +261,8 @@ fp8bq_status check_ws(const GemmPlan& plan, const void* ws, size_t ws_bytes) {
 
 fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, const void* a_q,
                       const void* a_s, const void* w_q, const float* w_s, int fmt, int out_dtype,
-                      void* out, void* ws, size_t ws_data_offset, DeviceInfo* d, int pdl,
-                      cudaStream_t stream) {
+                      void* out, void* ws, size_t ws_data_offset, DeviceInfo* d,
+                      int prefetch_w, cudaStream_t stream) {
     GemmLaunch g;
     g.M = M;
     g.N = N;
@@ -278,7 +278,7 @@ fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, con
     g.ws_data_offset = ws_data_offset;
     g.status = d->status;
     g.timeout_ns = wait_timeout_ns();
-    g.pdl = pdl;
+    g.prefetch_w = prefetch_w;
     return from_cuda(launch_gemm(plan, g, stream));
 }
 
@@ -390,7 +390,6 @@ fp8bq_status fp8bq_quant_act(const void* x, fp8bq_dtype x_dtype, int64_t M, int6
     a.G = static_cast<int>(K / kGroup);
     a.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
     a.fp16 = x_dtype == FP8BQ_FP16;
-    a.pdl_trigger = 0;
     return from_cuda(launch_quant_act(a, stream));
 }
 
@@ -508,7 +507,6 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
     qa.G = static_cast<int>(K / kGroup);
     qa.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
     qa.fp16 = x_dtype == FP8BQ_FP16;
-    qa.pdl_trigger = 1;
     st = from_cuda(launch_quant_act(qa, stream));
     if (st != FP8BQ_OK) return st;
     return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, base,

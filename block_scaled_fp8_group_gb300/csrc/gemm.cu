@@ -61,7 +61,7 @@ constexpr int SLOT_BYTES = 768;      // per slab: 128 act scales, 2 weight-scale
 constexpr int SLOT_SW = 512;         // weight-scale chunk c at SLOT_SW + c * SLOT_SW_STEP
 constexpr int SLOT_SW_STEP = 128;    // (TMA destinations 128-byte aligned)
 
-template <int BN>
+template <bool SWAP, int BN>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
@@ -74,13 +74,18 @@ struct Cfg {
                                      : TMEM_NEED <= 128 ? 128
                                      : TMEM_NEED <= 256 ? 256
                                                         : 512;
-    static constexpr int EPI_WARPS = BN >= 128 ? 8 : 4;
+    // swap-AB: 4 epilogue warps hold all BN token columns (up to 128 fp32
+    // accumulators per thread); the normal orientation splits 256-wide tiles
+    // over 8 warps
+    static constexpr int EPI_WARPS = (!SWAP && BN >= 128) ? 8 : 4;
     static constexpr int CPT = BN / (EPI_WARPS / 4);  // accumulator columns per thread
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int RING_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * NBUF + 1) + 16;
-    static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
+    static constexpr int FACT_OFF = (BAR_OFF + BAR_BYTES + 15) / 16 * 16;  // per-warp factors
+    static constexpr int SMEM = 1024 + FACT_OFF + EPI_WARPS * CPT * 4;
+    static constexpr int CHUNK = (EPI_WARPS == 8 || CPT < 32) ? 16 : 32;  // TMEM cols per load
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(CPT % 16 == 0, "TMEM loads are 16 columns wide");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -97,6 +102,7 @@ struct KArgs {
     long long units; // stream-K: tiles * G
     int ue8m0;
     int out_dtype;
+    int prefetch_w;  // weights may be read before the previous grid finishes
     void* out;
     float* partials;
     unsigned* counters;
@@ -248,13 +254,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <bool SWAP, int BN>
-__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_sa,     // act scales [cols][Mp] 4-byte
                 const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                 const KArgs a) {
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -270,6 +276,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     uint64_t* mma_done = tempty + C::NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* fact = reinterpret_cast<float*>(smem + C::FACT_OFF);  // EPI_WARPS x CPT
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -299,15 +306,43 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    // Programmatic dependent launch: everything above overlapped the tail of
-    // the previous kernel; inputs are read only after it has finished.
-    pdl_wait_prior_grid();
+    // Every warp reconverges before a CTA barrier: bar.sync counts warps, so a
+    // warp must reach it with all its lanes at once.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t tmo = a.timeout_ns;
     const int code = static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT);
+
+    // Programmatic dependent launch: the set-up above overlapped the tail of
+    // the previous kernel.  When the caller guarantees that the weights were
+    // complete before the previous kernel started (the fused linear path),
+    // the producer starts streaming the first weight tiles now; everything
+    // else is read or written only after the previous grid has finished.
+    int prefetched = 0;
+    if (a.prefetch_w && warp == 0 && lane == 0) {
+        WorkIter wi;
+        wi.init(a);
+        Seg sg;
+        if (wi.next(a, sg)) {
+            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const int nslab = sg.kb1 - sg.kb0;
+            prefetched = nslab < C::STAGES ? nslab : C::STAGES;
+            for (int i = 0; i < prefetched; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+                if (SWAP)
+                    tma_load_2d_hint(sA + i * C::A_BYTES, &tm_mma_m, &full[i], (sg.kb0 + i) * BK,
+                                     o.w0, policy_evict_first());
+                else
+                    tma_load_2d_hint(sB + i * C::B_BYTES, &tm_mma_n, &full[i], (sg.kb0 + i) * BK,
+                                     o.w0, policy_evict_first());
+            }
+        }
+    }
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
     // bytes one scale slot receives: the activation scales of the tile's
     // tokens plus one (swap-AB, 128-row weight tile) or two (256-wide weight
     // tile) 16-byte chunks of weight scales
@@ -335,16 +370,26 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, tmo,
-                                           code)) {
-                        ok = false;
-                        break;
+                    if (fills < prefetched) {
+                        // the weight tile of this stage is already on its way
+                        if (SWAP)
+                            tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
+                                             kb * BK, row_n, pol_n);
+                        else
+                            tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
+                                             kb * BK, row_m, pol_m);
+                    } else {
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                               tmo, code)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
+                                         kb * BK, row_m, pol_m);
+                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
+                                         kb * BK, row_n, pol_n);
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage], kb * BK,
-                                     row_m, pol_m);
-                    tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage], kb * BK,
-                                     row_n, pol_n);
                     ++fills;
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -454,46 +499,50 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 const float swv =
                     reinterpret_cast<const float*>(sl + SLOT_SW + SLOT_SW_STEP * chunk)[e & 3];
                 float f_norm = 0.0f;
+                float* fw = fact + ew * C::CPT;
                 if (!SWAP) {
                     const float sam = a.ue8m0
                                           ? ue8m0_value(reinterpret_cast<const uint32_t*>(sl)[row], kb)
                                           : reinterpret_cast<const float*>(sl)[row];
                     f_norm = (o.tok0 + row < a.M) ? sam * swv : 0.0f;
+                } else {
+                    // per-column (token) factors sa[t] * sw, computed once per
+                    // slab by the warp's lanes and read back as broadcasts
+                    for (int c = lane; c < C::CPT; c += 32) {
+                        const int t = chalf * C::CPT + c;
+                        const uint32_t w = reinterpret_cast<const uint32_t*>(sl)[t];
+                        const float sv = a.ue8m0 ? ue8m0_value(w, kb) : __uint_as_float(w);
+                        fw[c] = (o.tok0 + t < a.M) ? sv * swv : 0.0f;
+                    }
+                    __syncwarp();
                 }
                 const uint32_t t_buf = t_lane + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-                for (int c0 = 0; c0 < C::CPT; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(t_buf + c0, r);
-                    float f[16];
-                    if (SWAP) {
-                        // per-column (token) factors: broadcast reads of the slot
-                        const int t0 = chalf * C::CPT + c0;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 w = reinterpret_cast<const uint4*>(sl)[(t0 >> 2) + q];
-                            const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float s = a.ue8m0 ? ue8m0_value(ws4[i], kb)
-                                                        : __uint_as_float(ws4[i]);
-                                f[4 * q + i] = (o.tok0 + t0 + 4 * q + i < a.M) ? s * swv : 0.0f;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) f[j] = f_norm;
-                    }
+                for (int c0 = 0; c0 < C::CPT; c0 += C::CHUNK) {
+                    uint32_t r[C::CHUNK];
+                    if constexpr (C::CHUNK == 32)
+                        tmem_ld32(t_buf + c0, r);
+                    else
+                        tmem_ld16(t_buf + c0, r);
                     tmem_ld_wait();
-                    if (c0 + 16 == C::CPT) {
+                    if (c0 + C::CHUNK == C::CPT) {
                         // all of this buffer is in registers: hand it back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[buf]);
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        acc[c0 + j] = fmaf(__uint_as_float(r[j]), f[j], acc[c0 + j]);
+                    for (int j = 0; j < C::CHUNK; j += 4) {
+                        float4 f4;
+                        if (SWAP)
+                            f4 = *reinterpret_cast<const float4*>(fw + c0 + j);
+                        else
+                            f4 = make_float4(f_norm, f_norm, f_norm, f_norm);
+                        acc[c0 + j] = fmaf(__uint_as_float(r[j]), f4.x, acc[c0 + j]);
+                        acc[c0 + j + 1] = fmaf(__uint_as_float(r[j + 1]), f4.y, acc[c0 + j + 1]);
+                        acc[c0 + j + 2] = fmaf(__uint_as_float(r[j + 2]), f4.z, acc[c0 + j + 2]);
+                        acc[c0 + j + 3] = fmaf(__uint_as_float(r[j + 3]), f4.w, acc[c0 + j + 3]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -526,37 +575,28 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
                 if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
                 __threadfence();
-                // sum the segments in K order, 16 columns x PU segments of
-                // independent loads at a time
-                constexpr int PU = C::CPT >= 128 ? 1 : C::CPT >= 64 ? 2 : 4;
+                // sum the segments in K order (own segment from registers);
+                // each segment's RC columns are loaded with independent loads
+                constexpr int RC = (C::EPI_WARPS == 8 || C::CPT < 32) ? 16 : 32;
 #pragma unroll
-                for (int c0 = 0; c0 < C::CPT; c0 += 16) {
-                    float v[16];
-                    for (int p0 = 0; p0 < sg.nparts; p0 += PU) {
-                        float t[PU][16];
+                for (int c0 = 0; c0 < C::CPT; c0 += RC) {
+                    float r[RC];
+                    for (int p = 0; p < sg.nparts; ++p) {
+                        float t[RC];
+                        if (p == sg.part) {
 #pragma unroll
-                        for (int q = 0; q < PU; ++q) {
-                            const int p = p0 + q;
-                            if (p < sg.nparts && p != sg.part) {
-                                const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
-                                                   (chalf * C::CPT + c0) * BM + row;
+                            for (int j = 0; j < RC; ++j) t[j] = acc[c0 + j];
+                        } else {
+                            const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
+                                               (chalf * C::CPT + c0) * BM + row;
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) t[q][j] = __ldcg(src + j * BM);
-                            }
+                            for (int j = 0; j < RC; ++j) t[j] = __ldcg(src + j * BM);
                         }
 #pragma unroll
-                        for (int q = 0; q < PU; ++q) {
-                            const int p = p0 + q;
-                            if (p >= sg.nparts) break;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float x = (p == sg.part) ? acc[c0 + j] : t[q][j];
-                                v[j] = (p == 0) ? x : v[j] + x;
-                            }
-                        }
+                        for (int j = 0; j < RC; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[c0 + j] = v[j];
+                    for (int j = 0; j < RC; ++j) acc[c0 + j] = r[j];
                 }
                 if (lane == 0) *ctr = 0u;  // ready for the next call
             }
@@ -587,6 +627,9 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         }
     }
 
+    // Reconverge each warp (its lane 0 may have run a role loop alone), then
+    // wait for the whole CTA before giving the TMEM back.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -621,7 +664,7 @@ bool encode_operand(CUtensorMap* map, const void* base, uint64_t K, uint64_t row
 
 template <bool SWAP, int BN>
 cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
-    using C = Cfg<BN>;
+    using C = Cfg<SWAP, BN>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -680,6 +723,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     a.units = static_cast<long long>(a.tiles) * G;
     a.ue8m0 = g.ue8m0;
     a.out_dtype = g.out_dtype;
+    a.prefetch_w = g.prefetch_w;
     a.out = g.out;
     // workspace: [tile counters: fixed kCounterRegion prefix] [fp32 partial tiles]
     a.counters = p.ws_bytes ? static_cast<unsigned*>(g.workspace) : nullptr;
@@ -696,7 +740,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = g.pdl ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);

@@ -34,7 +34,6 @@ struct QuantActArgs {
     int G;       // groups per row
     int ue8m0;
     int fp16;    // input is fp16 (else bf16)
-    int pdl_trigger;  // signal a programmatic dependent launch early
 };
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream);
 
@@ -80,7 +79,10 @@ struct GemmLaunch {
     size_t ws_data_offset;  // partials start at kCounterRegion + this offset
     int* status;
     uint64_t timeout_ns;
-    int pdl;  // launched as a programmatic dependent of the previous kernel
+    // Weights may be read before the previous kernel in the stream has
+    // finished: only when that kernel cannot have written them (the fused
+    // linear path, where it is this library's activation quant).
+    int prefetch_w;
 };
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmLaunch& g, cudaStream_t stream);
 

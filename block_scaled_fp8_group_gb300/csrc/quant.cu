@@ -66,7 +66,10 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
     const int g = quad * 4 + (lane >> 3);    // this lane's group
     const bool active = row < a.M && g < a.G;
 
-    if (a.pdl_trigger) pdl_launch_dependents();
+    // Programmatic dependent launch: wait for the previous kernel (it may
+    // produce x or still read q/s), then let the next one start its set-up.
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
     if (row >= a.Mp) return;
 
     const int64_t off = row * a.K + static_cast<int64_t>(quad) * 512 + lane * 16;
@@ -237,13 +240,19 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
     const int quads = (a.G + 3) / 4;
-    dim3 grid(static_cast<unsigned>((a.Mp + kQuantRows - 1) / kQuantRows),
-              static_cast<unsigned>(quads));
-    if (a.fp16)
-        quant_act_kernel<true><<<grid, kQuantRows * 32, 0, stream>>>(a);
-    else
-        quant_act_kernel<false><<<grid, kQuantRows * 32, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((a.Mp + kQuantRows - 1) / kQuantRows),
+                       static_cast<unsigned>(quads));
+    cfg.blockDim = dim3(kQuantRows * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.fp16) return cudaLaunchKernelEx(&cfg, quant_act_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel<false>, a);
 }
 
 cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream) {

@@ -1,0 +1,157 @@
+"""Builds the per-shape variant table by measurement ("vLLM 量化 Kernel 配置机制"
+§3: per (N, K, device, dtype) and per point of the M grid, time every candidate
+kernel configuration and keep the fastest).
+
+    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small \
+        [--out block_scaled_fp8_group_gb300/tables/<device>.tbl]
+
+Candidates per M: swap-AB with token tiles 16..128 and the normal
+orientation with 128/256-wide weight tiles, each with stream-K (split 0),
+no split, and a few fixed K splits.  Each candidate is timed on cold weights
+(a rotation of weight copies larger than L2) as the mean of a batch of
+back-to-back launches queued behind a GPU sleep, so launch gaps do not count
+host time.  Lines of the table file: N K fmt out M kind block_n split grid.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import time
+
+import numpy as np
+import torch
+
+from . import fp8bq, synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+L2_BYTES = 160 << 20  # rotate through more than the L2 holds
+
+SETS = {
+    # (N, K, fmt, out dtype, M grid)
+    "small": [(1536, 1536, "fp32", "bf16", (16,))],
+    "decode": [(n, k, "ue8m0", "bf16", synth.DECODE_M) for n, k in synth.DECODE_NK],
+    "prefill": [(n, k, "fp32", o, synth.PREFILL_M) for n, k in synth.PREFILL_NK
+                for o in ("bf16", "fp32")],
+    "full": [(n, k, "ue8m0", o, synth.M_GRID) for n, k in synth.FULL_NK for o in ("fp16", "bf16")],
+}
+
+
+def device_table_path() -> str:
+    name = torch.cuda.get_device_name().replace(" ", "_")
+    return os.path.join(HERE, "tables", f"{name}.tbl")
+
+
+def candidates(M: int, N: int, K: int):
+    G = K // 128
+    out = []
+    if M <= 128:
+        tok = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+        bns = sorted({tok, max(16, tok // 2)})
+        for bn in bns:
+            for split in (0, 1, 2, 3, 4, 6, 8):
+                if split <= G:
+                    out.append(("swap", bn, split))
+    else:
+        for bn in (128, 256):
+            for split in (0, 1, 2):
+                out.append(("normal", bn, split))
+        for split in (0, 1):
+            out.append(("swap", 128, split))
+    return out
+
+
+def time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf, batch=24, reps=3):
+    for c in copies[:2]:
+        fp8bq.fp8bq_gemm_variant(aq, as_, c, ws, v, fmt=fmt, out_dtype=out_dt, out=out,
+                                 workspace=ws_buf)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(1_000_000)
+        a.record()
+        for i in range(batch):
+            fp8bq.fp8bq_gemm_variant(aq, as_, copies[i % len(copies)], ws, v, fmt=fmt,
+                                     out_dtype=out_dt, out=out, workspace=ws_buf)
+        b.record()
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e3 / batch
+        best = t if best is None else min(best, t)
+    return best
+
+
+def tune_shape(N, K, fmt, out_name, Ms, log):
+    dev = torch.device("cuda")
+    out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_name]
+    w = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
+    wq, ws = fp8bq.fp8bq_quant_weight(w, fmt)
+    del w
+    n_copies = max(2, int(np.ceil(L2_BYTES / (N * K))) + 1)
+    copies = [wq] + [wq.clone() for _ in range(n_copies - 1)]
+    rows = []
+    for M in Ms:
+        x = torch.from_numpy(synth.act_decode(M, K).view(np.int16)).view(torch.bfloat16).to(dev)
+        aq, as_ = fp8bq.fp8bq_quant_act(x, fmt)
+        out = torch.empty((M, N), dtype=out_dt, device=dev)
+        results = []
+        for kind, bn, split in candidates(M, N, K):
+            v = fp8bq.make_variant(kind, bn, split)
+            need = fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v)
+            if need == 0 and split != 1:
+                continue  # not supported for this shape (e.g. too many tiles for tickets)
+            ws_buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
+            t = time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf)
+            results.append((t, kind, bn, split))
+        results.sort()
+        t, kind, bn, split = results[0]
+        rows.append(f"{N} {K} {fmt} {out_name} {M} {kind} {bn} {split} 0")
+        log(f"  N={N} K={K} {fmt}/{out_name} M={M}: best {kind}/{bn}/s{split} {t:.2f} us "
+            f"(next {results[1][1]}/{results[1][2]}/s{results[1][3]} {results[1][0]:.2f} us)"
+            if len(results) > 1 else f"  M={M}: {kind}/{bn}/s{split} {t:.2f} us")
+    del copies
+    torch.cuda.empty_cache()
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--sets", default="small,decode,prefill,full")
+    ap.add_argument("--out", default=None)
+    args = ap.parse_args()
+    path = args.out or device_table_path()
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    keep = {}
+    if os.path.exists(path):
+        for line in open(path):
+            body = line.split("#")[0].split()
+            if len(body) == 9:
+                keep[tuple(body[:5])] = " ".join(body)
+    os.environ.pop("FP8BQ_TABLE", None)
+    # time without any table influence: explicit variants only
+    t0 = time.time()
+    done = set()
+    for name in args.sets.split(","):
+        for (N, K, fmt, out_name, Ms) in SETS[name]:
+            key = (N, K, fmt, out_name)
+            Ms = tuple(m for m in Ms if (key, m) not in done)
+            if not Ms:
+                continue
+            print(f"tuning N={N} K={K} {fmt}/{out_name} over M={list(Ms)}", flush=True)
+            for row in tune_shape(N, K, fmt, out_name, Ms, lambda s: print(s, flush=True)):
+                f = row.split()
+                keep[tuple(f[:5])] = row
+            done |= {(key, m) for m in Ms}
+    lines = sorted(keep.values(), key=lambda r: tuple(int(x) if x.isdigit() else x
+                                                      for x in r.split()))
+    with open(path, "w") as f:
+        f.write("# fp8bq variant table, measured by block_scaled_fp8_group_gb300/tune.py on "
+                f"{torch.cuda.get_device_name()}\n")
+        f.write("# N K fmt out M kind block_n split grid\n")
+        for r in lines:
+            f.write(r + "\n")
+    print(f"wrote {len(lines)} entries to {path} in {time.time() - t0:.0f} s")
+
+
+if __name__ == "__main__":
+    main()
