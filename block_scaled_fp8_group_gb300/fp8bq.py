@@ -33,6 +33,7 @@ EXPORTS = (
     "fp8bq_quant_weight", "fp8bq_gemm", "fp8bq_gemm_variant", "fp8bq_linear",
     "fp8bq_select_variant", "fp8bq_reload_table", "fp8bq_device_status",
     "fp8bq_selftest_wait_timeout", "fp8bq_status_string", "fp8bq_abi_version",
+    "fp8bq_gemm_noalloc",
 )
 
 
@@ -79,6 +80,8 @@ def _load():
         "fp8bq_reload_table": (i32, []),
         "fp8bq_device_status": (i32, [ctypes.POINTER(ctypes.c_int), vp]),
         "fp8bq_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp]),
+        "fp8bq_gemm_noalloc": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                     vp]),
         "fp8bq_status_string": (ctypes.c_char_p, [i32]),
         "fp8bq_abi_version": (i32, []),
     }

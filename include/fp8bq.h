@@ -178,6 +178,31 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
                           int block_k, fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* fp8bq_gemm for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this exists for integration, not for the method.)
+ * Some callers cannot call cudaMalloc where they run a layer -- runtimes that
+ * hand out all device memory from their own pool at start-up and forbid
+ * allocations later, code that must not risk the device synchronisation an
+ * allocation can cause, plug-ins that only receive tensors and a stream -- so
+ * they cannot provide the split-K workspace fp8bq_gemm may need.  This entry
+ * point takes the same arguments minus the workspace and allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library call.  Its scratch is one
+ * array of 32 MiB (33554432 bytes) built into the library; every GPU that
+ * loads the library holds it until the process exits.
+ *   - Problems whose chosen kernel needs more split-K scratch than 32 MiB are
+ *     rejected with FP8BQ_ERR_WORKSPACE (nothing is launched); use fp8bq_gemm
+ *     with a workspace for those.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, and each call clears the counters at its
+ *     start (cudaMemsetAsync on `stream`): calls that overlap on the GPU
+ *     (different streams without ordering) race and give wrong results. */
+fp8bq_status fp8bq_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                const void* a_s, const void* w_q, const float* w_s, int group,
+                                int block_n, int block_k, fp8bq_scale_fmt fmt,
+                                fp8bq_dtype out_dtype, void* out, cudaStream_t stream);
+
 /* ------------------------------------------------------------ host queries */
 
 /* The variant fp8bq_gemm would run for this shape (host only, no GPU work):
