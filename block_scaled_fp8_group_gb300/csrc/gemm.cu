@@ -67,25 +67,35 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = BN <= 16 ? 10 : BN <= 32 ? 9 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
-    static constexpr int NBUF = BN <= 64 ? 4 : 2;
+    // TMEM accumulator buffers: as many as fit in the 512 columns (at most 8)
+    static constexpr int NBUF = 512 / BN >= 8 ? 8 : 512 / BN;
     static constexpr int TMEM_NEED = NBUF * BN;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                      : TMEM_NEED <= 64  ? 64
                                      : TMEM_NEED <= 128 ? 128
                                      : TMEM_NEED <= 256 ? 256
                                                         : 512;
-    // swap-AB: 4 epilogue warps hold all BN token columns (up to 128 fp32
-    // accumulators per thread); the normal orientation splits 256-wide tiles
-    // over 8 warps
-    static constexpr int EPI_WARPS = (!SWAP && BN >= 128) ? 8 : 4;
+    // 4 epilogue warps (one per TMEM lane quadrant) below 64 columns; wider
+    // tiles split their columns over 8 warps
+    static constexpr int EPI_WARPS = BN >= 64 ? 8 : 4;
     static constexpr int CPT = BN / (EPI_WARPS / 4);  // accumulator columns per thread
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    // 128 accumulators per thread do not fit the 168 registers a 320-thread
+    // CTA gets; such tiles run warpgroup 0 (producer, MMA, 2 idle warps) on
+    // few registers and hand the rest to the two epilogue warpgroups
+    // (setmaxnreg).  The shares must add up to at most the launch total.
+    static constexpr bool REGSPLIT = CPT >= 128;
+    static constexpr int EPI_FIRST = REGSPLIT ? 4 : 2;  // first epilogue warp
+    static constexpr int THREADS = 32 * EPI_FIRST + 32 * EPI_WARPS;
+    static constexpr int REG_ROLE = 64;   // per thread, warpgroup 0
+    static constexpr int REG_EPI = 208;   // per thread, epilogue warpgroups
+    static constexpr int REG_MIN_LAUNCH =  // registers per thread the launch must provide
+        (REG_ROLE * 128 + REG_EPI * 32 * EPI_WARPS + THREADS - 1) / THREADS;
     static constexpr int RING_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * NBUF + 1) + 16;
     static constexpr int FACT_OFF = (BAR_OFF + BAR_BYTES + 15) / 16 * 16;  // per-warp factors
     static constexpr int SMEM = 1024 + FACT_OFF + EPI_WARPS * CPT * 4;
-    static constexpr int CHUNK = (EPI_WARPS == 8 || CPT < 32) ? 16 : 32;  // TMEM cols per load
+    static constexpr int CHUNK = (REGSPLIT || CPT == 32) ? 32 : 16;  // TMEM columns per load
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(CPT % 16 == 0, "TMEM loads are 16 columns wide");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -315,6 +325,12 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t tmo = a.timeout_ns;
     const int code = static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT);
+    if constexpr (C::REGSPLIT) {
+        // warpgroup 0 gives registers back; the epilogue warpgroups take
+        // them at the start of their branch (so the compiler budgets that
+        // code with REG_EPI registers)
+        if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_ROLE));
+    }
 
     // Programmatic dependent launch: the set-up above overlapped the tail of
     // the previous kernel.  When the caller guarantees that the weights were
@@ -463,9 +479,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0, tmo);
         }
-    } else {
+    } else if (warp >= C::EPI_FIRST) {
         // ------------------------------------------------ promotion/epilogue
-        const int ew = warp - 2;
+        if constexpr (C::REGSPLIT)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_EPI));
+        const int ew = warp - C::EPI_FIRST;
         const int quad = warp & 3;   // TMEM lanes this warp may access
         const int chalf = ew >> 2;   // column half (8 epilogue warps)
         const int row = quad * 32 + lane;
@@ -517,20 +535,30 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
                     __syncwarp();
                 }
                 const uint32_t t_buf = t_lane + static_cast<uint32_t>(buf * BN);
+                // double-buffered TMEM loads: chunk c+1 is in flight while the
+                // FMAs of chunk c run (tcgen05.wait::ld waits for all loads)
+                constexpr int NCH = C::CPT / C::CHUNK;
+                uint32_t rr[2][C::CHUNK];
+                if constexpr (C::CHUNK == 32)
+                    tmem_ld32(t_buf, rr[0]);
+                else
+                    tmem_ld16(t_buf, rr[0]);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c0 = 0; c0 < C::CPT; c0 += C::CHUNK) {
-                    uint32_t r[C::CHUNK];
-                    if constexpr (C::CHUNK == 32)
-                        tmem_ld32(t_buf + c0, r);
-                    else
-                        tmem_ld16(t_buf + c0, r);
-                    tmem_ld_wait();
-                    if (c0 + C::CHUNK == C::CPT) {
+                for (int c = 0; c < NCH; ++c) {
+                    const int c0 = c * C::CHUNK;
+                    if (c + 1 < NCH) {
+                        if constexpr (C::CHUNK == 32)
+                            tmem_ld32(t_buf + c0 + C::CHUNK, rr[(c + 1) & 1]);
+                        else
+                            tmem_ld16(t_buf + c0 + C::CHUNK, rr[(c + 1) & 1]);
+                    } else {
                         // all of this buffer is in registers: hand it back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[buf]);
                     }
+                    const uint32_t* r = rr[c & 1];
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; j += 4) {
                         float4 f4;
@@ -543,6 +571,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
                         acc[c0 + j + 2] = fmaf(__uint_as_float(r[j + 2]), f4.z, acc[c0 + j + 2]);
                         acc[c0 + j + 3] = fmaf(__uint_as_float(r[j + 3]), f4.w, acc[c0 + j + 3]);
                     }
+                    if (c + 1 < NCH) tmem_ld_wait();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -577,7 +606,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
                 __threadfence();
                 // sum the segments in K order (own segment from registers);
                 // each segment's RC columns are loaded with independent loads
-                constexpr int RC = (C::EPI_WARPS == 8 || C::CPT < 32) ? 16 : 32;
+                constexpr int RC = C::CPT >= 128 ? 8 : (C::EPI_WARPS == 8 || C::CPT < 32) ? 16 : 32;
 #pragma unroll
                 for (int c0 = 0; c0 < C::CPT; c0 += RC) {
                     float r[RC];
@@ -673,6 +702,18 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         err = cudaFuncSetAttribute(gemm_kernel<SWAP, BN>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (err != cudaSuccess) return err;
+        if (C::REGSPLIT) {
+            // the register split asks for REG_ROLE/REG_EPI per warpgroup; a
+            // launch that provides fewer registers in total would never
+            // satisfy setmaxnreg.inc, so refuse it
+            cudaFuncAttributes fa;
+            err = cudaFuncGetAttributes(&fa, gemm_kernel<SWAP, BN>);
+            if (err != cudaSuccess) return err;
+            if (fa.numRegs < C::REG_MIN_LAUNCH) {
+                log_error("GEMM kernel compiled with too few registers for its register split");
+                return cudaErrorInvalidConfiguration;
+            }
+        }
         attr_done[dev] = 1;
     }
     const bool swap = SWAP;
