@@ -604,25 +604,39 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
                 prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
                 if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
                 __threadfence();
-                // sum the segments in K order (own segment from registers);
-                // each segment's RC columns are loaded with independent loads
+                // Sum the segments in K order (own segment from registers).
+                // The loads of PB segments are all issued before the first
+                // add, so PB parts cost one L2 round trip per RC-column
+                // chunk instead of one each; PB is as large as the
+                // registers allow without spilling (1 from 64 columns a thread).
                 constexpr int RC = C::CPT >= 128 ? 8 : (C::EPI_WARPS == 8 || C::CPT < 32) ? 16 : 32;
+                constexpr int PB = C::CPT == 16 ? 4 : C::CPT == 32 ? 2 : 1;
 #pragma unroll
                 for (int c0 = 0; c0 < C::CPT; c0 += RC) {
                     float r[RC];
-                    for (int p = 0; p < sg.nparts; ++p) {
-                        float t[RC];
-                        if (p == sg.part) {
+                    for (int p0 = 0; p0 < sg.nparts; p0 += PB) {
+                        float t[PB][RC];
 #pragma unroll
-                            for (int j = 0; j < RC; ++j) t[j] = acc[c0 + j];
-                        } else {
-                            const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
-                                               (chalf * C::CPT + c0) * BM + row;
+                        for (int q = 0; q < PB; ++q) {
+                            const int p = p0 + q;
+                            if (p < sg.nparts && p != sg.part) {
+                                const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
+                                                   (chalf * C::CPT + c0) * BM + row;
 #pragma unroll
-                            for (int j = 0; j < RC; ++j) t[j] = __ldcg(src + j * BM);
+                                for (int j = 0; j < RC; ++j) t[q][j] = __ldcg(src + j * BM);
+                            }
                         }
 #pragma unroll
-                        for (int j = 0; j < RC; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
+                        for (int q = 0; q < PB; ++q) {
+                            const int p = p0 + q;
+                            if (p < sg.nparts) {
+#pragma unroll
+                                for (int j = 0; j < RC; ++j) {
+                                    const float v = (p == sg.part) ? acc[c0 + j] : t[q][j];
+                                    r[j] = (p == 0) ? v : r[j] + v;
+                                }
+                            }
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < RC; ++j) acc[c0 + j] = r[j];
