@@ -90,8 +90,9 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 // ------------------------------------------------------- variant table
 //
-// Text file, one entry per line:  N K fmt out M kind block_n split grid
-// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap).  Per
+// Text file, one entry per line:  N K fmt out M kind block_n split grid [mma_scale]
+// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap; mma_scale 0 when
+// absent).  Per
 // (N, K, fmt, out) the entries form an M grid; a lookup takes the grid point
 // nearest to M, the smaller one on a tie ("vLLM 量化 Kernel 配置机制" §4.2:
 // configs[min(keys, key=|x - M|)], e.g. M=37 -> 32, M=2050 -> 2048).
@@ -156,10 +157,10 @@ void load_table_locked(const std::string& device_name) {
         if (hash) *hash = 0;
         long long N, K, M;
         char fmt[16], out[16], kind[16];
-        int bn, split, grid;
-        if (std::sscanf(line, "%lld %lld %15s %15s %lld %15s %d %d %d", &N, &K, fmt, out, &M, kind,
-                        &bn, &split, &grid) != 9)
-            continue;  // blank or malformed line: skipped
+        int bn, split, grid, mma_scale = 0;
+        const int got = std::sscanf(line, "%lld %lld %15s %15s %lld %15s %d %d %d %d", &N, &K, fmt,
+                                    out, &M, kind, &bn, &split, &grid, &mma_scale);
+        if (got != 9 && got != 10) continue;  // blank or malformed line: skipped
         const int ifmt = parse_fmt(fmt), iout = parse_out(out), ikind = parse_kind(kind);
         if (ifmt < 0 || iout < 0 || ikind < 0 || M < 0) continue;
         fp8bq_variant v = {};
@@ -167,6 +168,7 @@ void load_table_locked(const std::string& device_name) {
         v.block_n = bn;
         v.split = split;
         v.grid = grid;
+        v.mma_scale = mma_scale;
         v.from_table = 1;
         g_table.rows[TableKey(N, K, ifmt, iout)][M] = v;
     }
@@ -263,6 +265,9 @@ fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, con
                       const void* a_s, const void* w_q, const float* w_s, int fmt, int out_dtype,
                       void* out, void* ws, size_t ws_data_offset, DeviceInfo* d,
                       int prefetch_w, cudaStream_t stream) {
+    // the block-scaled MMA takes E8M0 factors in whole groups of four slabs
+    if (plan.mx && (fmt != FP8BQ_SCALE_UE8M0 || K % (4 * kGroup) != 0))
+        return FP8BQ_ERR_UNSUPPORTED;
     GemmLaunch g;
     g.M = M;
     g.N = N;

@@ -682,6 +682,427 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
     }
 }
 
+// ------------------------------------------------------ block-scaled path
+//
+// Swap-AB with UE8M0 scales applied by the tensor core: the E8M0 factors of
+// the weights (one per 128x128 block) and of the tokens (one per 1x128 group)
+// go to TMEM, and tcgen05.mma.kind::mxf8f6f4.block_scale multiplies each
+// 32-wide K block's products by 2^(ea+ew) as it accumulates, so a segment's
+// sum of promoted slab products builds up in one TMEM accumulator and is read
+// once.  A slab's four K blocks share its group's factors.  The packed UE8M0
+// activation words (four groups per u32) are the TMEM factor words as they
+// are: slab kb uses byte kb % 4 (the instruction's factor ids) of word kb / 4.
+//
+//   warp 0     TMA: per slab the weight and token tiles (as gemm_kernel);
+//              per 4-slab group the tile's token factor words and the weight
+//              block's four fp32 scales into the scale ring.
+//   warp 1     MMA issuer; owns TMEM.  Per slab four block-scaled MMAs into
+//              the segment's accumulator (two, alternating by segment).
+//   warps 2-5  factor writers: per group, tcgen05.st of the factor words into
+//              a TMEM ring entry, each warp into its 32-lane quarter (every
+//              quarter holds a full copy: weight word at columns 0-3, token
+//              word of token 32c+l at lane l, column 8+c).
+//   warps 6-9  epilogue: per segment, read the accumulator, store or reduce
+//              the split parts (same workspace protocol as gemm_kernel).
+//
+// Requires K % 512 == 0 (whole groups of four slabs, so the four weight
+// scales of a group are one aligned 16-byte chunk).
+template <int BN>
+struct MxCfg {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = Cfg<true, BN>::STAGES;
+    static constexpr int NC = (BN + 31) / 32;       // factor columns of the token operand
+    // one factor-ring entry: weight factors at columns +0..3, token factors at
+    // +8..8+NC-1; both start on an 8-column boundary (tcgen05.st.x4 and the
+    // MMA's factor addresses need aligned columns)
+    static constexpr int SF_B = 8;
+    static constexpr int SF_COLS = 16;
+    static constexpr int RF = 8;                    // factor-ring entries (groups in flight)
+    static constexpr int SF_BASE = 2 * BN;          // after the two accumulators
+    static constexpr int TMEM_NEED = SF_BASE + RF * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
+                                     : TMEM_NEED <= 64  ? 64
+                                     : TMEM_NEED <= 128 ? 128
+                                     : TMEM_NEED <= 256 ? 256
+                                                        : 512;
+    static constexpr int EPI_FIRST = 6;             // factor writers 2..5, epilogue 6..9
+    static constexpr int THREADS = 32 * 10;
+    static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // accumulator columns per TMEM load
+    static constexpr int RING_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * RF + 4 + 1) + 16;
+    static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
+    static_assert(TMEM_NEED <= 512, "TMEM columns");
+    static_assert(SF_BASE % 16 == 0 && NC <= SF_COLS - SF_B, "factor-ring column alignment");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(4 * BN <= SLOT_SW, "token factor words fit the scale slot");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_w,    // weights [N, K] e4m3
+                   const __grid_constant__ CUtensorMap tm_tok,  // tokens [M, K] e4m3
+                   const __grid_constant__ CUtensorMap tm_sa,   // packed act words [G/4][Mp]
+                   const __grid_constant__ CUtensorMap tm_sw,   // weight scales, flat fp32
+                   const KArgs a) {
+    using C = MxCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                           // STAGES x [128 weight rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN tokens x 128 B]
+    uint8_t* ring = smem + C::RING_OFF;           // SR x SLOT_BYTES
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* sfull = empty + C::STAGES;
+    uint64_t* sempty = sfull + SR;
+    uint64_t* ffull = sempty + SR;   // factor-ring entry written
+    uint64_t* fempty = ffull + C::RF;  // factor-ring entry consumed by its MMAs
+    uint64_t* tfull = fempty + C::RF;  // accumulator complete (2)
+    uint64_t* tempty = tfull + 2;      // accumulator read out (2)
+    uint64_t* mma_done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sempty[s], 4);
+        }
+        for (int r = 0; r < C::RF; ++r) {
+            mbar_init(&ffull[r], 4);
+            mbar_init(&fempty[r], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_tok);
+        tma_prefetch_desc(&tm_sa);
+        tma_prefetch_desc(&tm_sw);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t tmo = a.timeout_ns;
+    const int code = static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT);
+
+    // Programmatic dependent launch, as in gemm_kernel: only weight tiles may
+    // be read before the previous grid has finished.
+    int prefetched = 0;
+    if (a.prefetch_w && warp == 0 && lane == 0) {
+        WorkIter wi;
+        wi.init(a);
+        Seg sg;
+        if (wi.next(a, sg)) {
+            const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+            const int nslab = sg.kb1 - sg.kb0;
+            prefetched = nslab < C::STAGES ? nslab : C::STAGES;
+            for (int i = 0; i < prefetched; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+                tma_load_2d_hint(sA + i * C::A_BYTES, &tm_w, &full[i], (sg.kb0 + i) * BK, o.w0,
+                                 policy_evict_first());
+            }
+        }
+    }
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            int stage = 0, slot = 0;
+            uint32_t phase = 0, sphase = 0;
+            long long fills = 0, sfills = 0;
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+                const int nb = o.w0 / BK;
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (kb == sg.kb0 || (kb & 3) == 0) {
+                        // the group's factors: BN token words, four weight scales
+                        if (!mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag, a.status,
+                                               tmo, code)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* sl = ring + slot * SLOT_BYTES;
+                        mbar_arrive_expect_tx(&sfull[slot], 4u * BN + 16u);
+                        tma_load_2d(sl, &tm_sa, &sfull[slot], o.tok0, kb >> 2);
+                        tma_load_2d(sl + SLOT_SW, &tm_sw, &sfull[slot], nb * a.G + (kb & ~3), 0);
+                        ++sfills;
+                        if (++slot == SR) {
+                            slot = 0;
+                            sphase ^= 1u;
+                        }
+                    }
+                    if (fills < prefetched) {
+                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_tok, &full[stage], kb * BK,
+                                         o.tok0, pol_a);
+                    } else {
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                               tmo, code)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_w, &full[stage], kb * BK,
+                                         o.w0, pol_w);
+                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_tok, &full[stage], kb * BK,
+                                         o.tok0, pol_a);
+                    }
+                    ++fills;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (long long f = fills > C::STAGES ? fills - C::STAGES : 0; f < fills; ++f)
+                mbar_wait_drain(&full[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1),
+                                tmo);
+            for (long long f = sfills > SR ? sfills - SR : 0; f < sfills; ++f)
+                mbar_wait_drain(&sfull[f % SR], static_cast<uint32_t>((f / SR) & 1), tmo);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0, r = 0, acc = 0;
+            uint32_t phase = 0, rphase = 0, aphase = 0;
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                if (!mbar_wait_bounded(&tempty[acc], aphase ^ 1u, abort_flag, a.status, tmo,
+                                       code)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_addr = tmem_base + static_cast<uint32_t>(acc * BN);
+                int cur = 0;
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (kb == sg.kb0 || (kb & 3) == 0) {
+                        if (!mbar_wait_bounded(&ffull[r], rphase, abort_flag, a.status, tmo,
+                                               code)) {
+                            ok = false;
+                            break;
+                        }
+                        cur = r;
+                        if (++r == C::RF) {
+                            r = 0;
+                            rphase ^= 1u;
+                        }
+                    }
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, a.status, tmo, code)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(sA + stage * C::A_BYTES);
+                    const uint32_t b_addr = smem_addr(sB + stage * C::B_BYTES);
+                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(C::SF_BASE + cur * C::SF_COLS);
+                    const uint32_t idesc = idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(kb & 3));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk)
+                        mma_mxf8(d_addr, smem_desc_k128_sw128(a_addr + kk * 32),
+                                 smem_desc_k128_sw128(b_addr + kk * 32), idesc, sfa, sfa + C::SF_B,
+                                 (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if ((kb & 3) == 3 || kb == sg.kb1 - 1) mma_commit(&fempty[cur]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aphase ^= 1u;
+                }
+            }
+            mma_commit(mma_done);
+            mbar_wait_drain(mma_done, 0, tmo);
+        }
+    } else if (warp < C::EPI_FIRST) {
+        // -------------------------------------------------- factor writers
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const uint32_t t_quarter = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        int slot = 0, r = 0;
+        uint32_t sphase = 0, rphase = 0;
+        WorkIter wi;
+        wi.init(a);
+        Seg sg;
+        bool ok = true;
+        while (ok && wi.next(a, sg)) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (kb != sg.kb0 && (kb & 3) != 0) continue;
+                if (!warp_wait(&sfull[slot], sphase, abort_flag, a.status, tmo, code) ||
+                    !warp_wait(&fempty[r], rphase ^ 1u, abort_flag, a.status, tmo, code)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* sl = ring + slot * SLOT_BYTES;
+                // weight word: byte j = E8M0 exponent of the block's scale of
+                // slab 4*(kb/4)+j (the fp32 scales are powers of two)
+                const float* swc = reinterpret_cast<const float*>(sl + SLOT_SW);
+                uint32_t ww = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ww |= ((__float_as_uint(swc[j]) >> 23) & 0xFFu) << (8 * j);
+                const uint32_t* tw = reinterpret_cast<const uint32_t*>(sl);
+                const uint32_t col = static_cast<uint32_t>(C::SF_BASE + r * C::SF_COLS);
+                tmem_st4(t_quarter + col, ww, ww, ww, ww);
+#pragma unroll
+                for (int c = 0; c < C::NC; ++c) {
+                    const int t = 32 * c + lane;
+                    tmem_st1(t_quarter + col + C::SF_B + c, t < BN ? tw[t] : 0u);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ffull[r]);
+                    mbar_arrive(&sempty[slot]);
+                }
+                if (++slot == SR) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+                if (++r == C::RF) {
+                    r = 0;
+                    rphase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;  // weight row within the tile
+        int acc = 0;
+        uint32_t aphase = 0;
+        WorkIter wi;
+        wi.init(a);
+        Seg sg;
+        bool ok = true;
+        constexpr int NCH = BN / C::CHUNK;
+        while (ok && wi.next(a, sg)) {
+            const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+            if (!warp_wait(&tfull[acc], aphase, abort_flag, a.status, tmo, code)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            const int n = o.w0 + row;
+            constexpr int64_t TILE = BM * BN;
+            float* mine = sg.nparts > 1 ? a.partials + part_slot(a, sg.tile, sg.part) * TILE
+                                        : nullptr;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                uint32_t v[C::CHUNK];
+                if constexpr (C::CHUNK == 32)
+                    tmem_ld32(t_acc + c * C::CHUNK, v);
+                else
+                    tmem_ld16(t_acc + c * C::CHUNK, v);
+                tmem_ld_wait();
+                if (c + 1 == NCH) {
+                    // the accumulator is in registers: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                }
+                if (sg.nparts > 1) {
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j)
+                        __stcg(mine + (c * C::CHUNK + j) * BM + row, __uint_as_float(v[j]));
+                } else if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j) {
+                        const int t = o.tok0 + c * C::CHUNK + j;
+                        if (t < a.M)
+                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n,
+                                       __uint_as_float(v[j]));
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+            if (sg.nparts == 1) continue;
+            // split parts: per-warp ticket; the last to arrive sums all parts
+            // in K order and stores (every warp owns its 32 rows)
+            __threadfence();
+            __syncwarp();
+            unsigned* ctr = a.counters + static_cast<int64_t>(sg.tile) * kCountersPerTile + quad;
+            unsigned prev = 0;
+            if (lane == 0) prev = atomicAdd(ctr, 1u);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
+            __threadfence();
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                float r[C::CHUNK];
+                for (int p = 0; p < sg.nparts; ++p) {
+                    const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
+                                       (c * C::CHUNK) * BM + row;
+                    float t[C::CHUNK];
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j) t[j] = __ldcg(src + j * BM);
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
+                }
+                if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j) {
+                        const int t = o.tok0 + c * C::CHUNK + j;
+                        if (t < a.M)
+                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, r[j]);
+                    }
+                }
+            }
+            if (lane == 0) *ctr = 0u;  // ready for the next call
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
@@ -729,6 +1150,16 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
             }
         }
         attr_done[dev] = 1;
+    }
+    if constexpr (SWAP) {
+        static int mx_attr_done[64] = {0};
+        if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
+            err = cudaFuncSetAttribute(gemm_mx_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       MxCfg<BN>::SMEM);
+            if (err != cudaSuccess) return err;
+            mx_attr_done[dev] = 1;
+        }
     }
     const bool swap = SWAP;
     const uint64_t K = static_cast<uint64_t>(g.K);
@@ -798,6 +1229,13 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if constexpr (SWAP) {
+        if (p.mx) {
+            cfg.blockDim = dim3(MxCfg<BN>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<BN>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<BN>, tm_m, tm_n, tm_sa, tm_sw, a);
+        }
+    }
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
@@ -815,6 +1253,9 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     }
     if (v.split < 0 || v.split > 64 || v.split > G) return false;
     if (v.grid < 0) return false;
+    if (v.mma_scale != 0 && v.mma_scale != 1) return false;
+    if (v.mma_scale && !swap) return false;  // block-scaled MMA: swap-AB tiles only
+    p->mx = v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;
     p->split = v.split;

@@ -54,6 +54,7 @@ struct GemmPlan {
     int kind;      // fp8bq_kind
     int bn;        // MMA N
     int split;     // K splits per tile
+    int mx;        // 1: UE8M0 scales applied by the block-scaled MMA (gemm_mx_kernel)
     int grid;      // CTAs
     int tiles_tok; // token tiles
     int tiles_w;   // weight tiles

@@ -250,4 +250,51 @@ __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31u) == 0;
 }
 
+// ------------------------------------------- block-scaled MMA (UE8M0, MX)
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, E4M3 x E4M3, one UE8M0 factor per
+// row of A / row of B and 32-wide K block (scale_vec::1X), read from TMEM.
+// Factor layout in TMEM (per warp's 32-lane quarter): the factor word of row
+// r sits at lane r % 32, column base + r / 32; the instruction descriptor's
+// factor ids pick the byte of that word.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: E4M3 x E4M3 (formats 0),
+// both K-major, N >> 3 at bit 17, UE8M0 factors (bit 23), M >> 4 at bit 24,
+// factor ids of B at bits 4-5 and of A at bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, uint32_t sf_id) {
+    return (sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
+}
+
+// 32 lanes x 32 bit stores to TMEM: each thread writes consecutive columns of
+// its own lane (a warp reaches only its 32-lane quarter).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                         uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 }  // namespace fp8bq

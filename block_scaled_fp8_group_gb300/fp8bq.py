@@ -47,12 +47,12 @@ class Fp8bqError(RuntimeError):
 class Variant(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("block_n", ctypes.c_int32), ("split", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("from_table", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("mma_scale", ctypes.c_int32)]
 
     def as_dict(self):
         return {"kind": "swap" if self.kind == KIND_SWAP_AB else "normal",
                 "block_n": self.block_n, "split": self.split, "grid": self.grid,
-                "from_table": bool(self.from_table)}
+                "mma_scale": self.mma_scale, "from_table": bool(self.from_table)}
 
 
 def _load():
@@ -212,9 +212,12 @@ def fp8bq_select_variant(M: int, N: int, K: int, fmt="fp32", out_dtype=torch.bfl
     return v.as_dict()
 
 
-def make_variant(kind, block_n: int, split: int = 1, grid: int = 0) -> Variant:
+def make_variant(kind, block_n: int, split: int = 1, grid: int = 0,
+                 mma_scale: int = 0) -> Variant:
+    """A GEMM variant; mma_scale=1 has the tensor core apply UE8M0 scales
+    (block-scaled MMA; swap-AB, UE8M0, K % 512 == 0)."""
     k = kind if isinstance(kind, int) else (KIND_SWAP_AB if kind == "swap" else KIND_NORMAL)
-    return Variant(k, block_n, split, grid, 0, 0)
+    return Variant(k, block_n, split, grid, 0, mma_scale)
 
 
 def fp8bq_gemm_workspace_bytes(M, N, K, fmt="fp32", out_dtype=torch.bfloat16) -> int:

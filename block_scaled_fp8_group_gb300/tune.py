@@ -7,10 +7,13 @@ kernel configuration and keep the fastest).
 
 Candidates per M: swap-AB with token tiles 16..128 and the normal
 orientation with 128/256-wide weight tiles, each with stream-K (split 0),
-no split, and a few fixed K splits.  Each candidate is timed on cold weights
+no split, and a few fixed K splits; with UE8M0 scales and K % 512 == 0 every
+swap-AB candidate also runs with the scales applied by the block-scaled MMA
+(mma_scale 1).  Each candidate is timed on cold weights
 (a rotation of weight copies larger than L2) as the mean of a batch of
 back-to-back launches queued behind a GPU sleep, so launch gaps do not count
-host time.  Lines of the table file: N K fmt out M kind block_n split grid.
+host time.  Lines of the table file: N K fmt out M kind block_n split grid
+mma_scale.
 """
 from __future__ import annotations
 
@@ -41,8 +44,10 @@ def device_table_path() -> str:
     return os.path.join(HERE, "tables", f"{name}.tbl")
 
 
-def candidates(M: int, N: int, K: int):
+def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
+    """(kind, block_n, split, mma_scale) tuples."""
     G = K // 128
+    mx = fmt == "ue8m0" and K % 512 == 0
     out = []
     if M <= 128:
         tok = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
@@ -50,13 +55,13 @@ def candidates(M: int, N: int, K: int):
         for bn in bns:
             for split in (0, 1, 2, 3, 4, 6, 8):
                 if split <= G:
-                    out.append(("swap", bn, split))
+                    out += [("swap", bn, split, m) for m in ((0, 1) if mx else (0,))]
     else:
         for bn in (128, 256):
             for split in (0, 1, 2):
-                out.append(("normal", bn, split))
+                out.append(("normal", bn, split, 0))
         for split in (0, 1):
-            out.append(("swap", 128, split))
+            out += [("swap", 128, split, m) for m in ((0, 1) if mx else (0,))]
     return out
 
 
@@ -95,20 +100,26 @@ def tune_shape(N, K, fmt, out_name, Ms, log):
         aq, as_ = fp8bq.fp8bq_quant_act(x, fmt)
         out = torch.empty((M, N), dtype=out_dt, device=dev)
         results = []
-        for kind, bn, split in candidates(M, N, K):
-            v = fp8bq.make_variant(kind, bn, split)
+        for kind, bn, split, mx in candidates(M, N, K, fmt):
+            v = fp8bq.make_variant(kind, bn, split, 0, mx)
             need = fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v)
             if need == 0 and split != 1:
                 continue  # not supported for this shape (e.g. too many tiles for tickets)
             ws_buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
             t = time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf)
-            results.append((t, kind, bn, split))
+            results.append((t, kind, bn, split, mx))
         results.sort()
-        t, kind, bn, split = results[0]
-        rows.append(f"{N} {K} {fmt} {out_name} {M} {kind} {bn} {split} 0")
-        log(f"  N={N} K={K} {fmt}/{out_name} M={M}: best {kind}/{bn}/s{split} {t:.2f} us "
-            f"(next {results[1][1]}/{results[1][2]}/s{results[1][3]} {results[1][0]:.2f} us)"
-            if len(results) > 1 else f"  M={M}: {kind}/{bn}/s{split} {t:.2f} us")
+
+        def name(r):
+            return f"{r[1]}/{r[2]}/s{r[3]}" + ("/mx" if r[4] else "")
+
+        t, kind, bn, split, mx = results[0]
+        rows.append(f"{N} {K} {fmt} {out_name} {M} {kind} {bn} {split} 0 {mx}")
+        best_promo = min((r for r in results if not r[4]), default=None)
+        log(f"  N={N} K={K} {fmt}/{out_name} M={M}: best {name(results[0])} {t:.2f} us "
+            f"(next {name(results[1])} {results[1][0]:.2f} us"
+            + (f"; best promotion {name(best_promo)} {best_promo[0]:.2f} us" if best_promo else "")
+            + ")" if len(results) > 1 else f"  M={M}: {name(results[0])} {t:.2f} us")
     del copies
     torch.cuda.empty_cache()
     return rows
@@ -125,7 +136,7 @@ def main():
     if os.path.exists(path):
         for line in open(path):
             body = line.split("#")[0].split()
-            if len(body) == 9:
+            if len(body) in (9, 10):
                 keep[tuple(body[:5])] = " ".join(body)
     os.environ.pop("FP8BQ_TABLE", None)
     # time without any table influence: explicit variants only
@@ -147,7 +158,7 @@ def main():
     with open(path, "w") as f:
         f.write("# fp8bq variant table, measured by block_scaled_fp8_group_gb300/tune.py on "
                 f"{torch.cuda.get_device_name()}\n")
-        f.write("# N K fmt out M kind block_n split grid\n")
+        f.write("# N K fmt out M kind block_n split grid mma_scale\n")
         for r in lines:
             f.write(r + "\n")
     print(f"wrote {len(lines)} entries to {path} in {time.time() - t0:.0f} s")

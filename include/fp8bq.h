@@ -78,7 +78,11 @@ typedef struct {
     int32_t split;      /* K splits per output tile, 1..64 (1 = no split-K) */
     int32_t grid;       /* CTAs to launch; 0 = one per SM, capped by the work items */
     int32_t from_table; /* output of fp8bq_select_variant: 1 = measured table, 0 = default */
-    int32_t reserved;
+    int32_t mma_scale;  /* 0: each K slab's fp32 product is promoted by sa*sw on the CUDA
+                         * cores; 1: the tensor core applies the scales (block-scaled MMA,
+                         * E8M0 factors in TMEM) and accumulates all slabs itself -- swap-AB
+                         * only, UE8M0 scales only, K a multiple of 512 (FP8BQ_ERR_UNSUPPORTED
+                         * otherwise) */
 } fp8bq_variant;
 
 /* ------------------------------------------------------------ size queries */

@@ -109,6 +109,7 @@ def fake_table(tmp_path, monkeypatch):
     t.write_text(
         "# N K fmt out M kind block_n split grid\n"
         "4096 7168 ue8m0 bf16 1 swap 16 4 0\n"
+        "4096 7168 ue8m0 bf16 8 swap 16 4 0 1\n"
         "4096 7168 ue8m0 bf16 32 swap 32 2 0\n"
         "4096 7168 ue8m0 bf16 64 swap 64 1 120\n"
         "4096 7168 ue8m0 bf16 2048 normal 256 1 0\n"
@@ -127,8 +128,10 @@ def test_nearest_m_lookup(fake_table):
     assert sel(2050)["block_n"] == 256       # 2050 -> 2048
     assert sel(48)["block_n"] == 32          # tie between 32 and 64 -> smaller
     v = sel(64)
-    assert v == {"kind": "swap", "block_n": 64, "split": 1, "grid": 120, "from_table": True}
-    assert sel(1)["split"] == 4
+    assert v == {"kind": "swap", "block_n": 64, "split": 1, "grid": 120, "mma_scale": 0,
+                 "from_table": True}
+    assert sel(1)["split"] == 4 and sel(1)["mma_scale"] == 0  # 9-column line
+    assert sel(8)["split"] == 4 and sel(8)["mma_scale"] == 1  # optional 10th column
     assert sel(10 ** 6)["block_n"] == 128    # beyond the grid -> largest key
     assert sel(3072)["block_n"] == 256       # tie 2048/4096 -> smaller
 
@@ -157,3 +160,10 @@ def test_variant_workspace_bytes():
     assert lin == 65536 + codes + scales + (g - 65536 if g else 0)
     bad = fp8bq.make_variant("swap", 48, 1)
     assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, bad) == 0
+    # the block-scaled MMA splits K the same way (same partials workspace) ...
+    mx4 = fp8bq.make_variant("swap", 16, 4, 0, 1)
+    assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, mx4) == \
+        fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, v4)
+    # ... and exists for swap-AB tiles only
+    assert fp8bq.fp8bq_variant_workspace_bytes(
+        256, 7168, 18432, fp8bq.make_variant("normal", 128, 2, 0, 1)) == 0

@@ -48,6 +48,66 @@ def test_variants_small(fp8bq, kind, bn, split, M, N, K, ue):
         check_gemm(o.float().cpu().numpy(), ref, out, f"{kind}/{bn}/{split} {M}x{N}x{K} {out}")
 
 
+# block-scaled MMA: the tensor core applies the UE8M0 scales (swap-AB, K % 512 == 0)
+MX_VARIANTS = [(bn, s) for bn in (16, 32, 64, 128) for s in (0, 1, 2, 3)]
+
+
+@pytest.mark.parametrize("bn,split", MX_VARIANTS)
+@pytest.mark.parametrize("M,N,K", [(1, 128, 512), (5, 320, 1024), (77, 256, 2048),
+                                   (130, 384, 1536)])
+def test_mx_variants_small(fp8bq, bn, split, M, N, K):
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    d = upload(qa, sa, qw, sw)
+    v = fp8bq.make_variant("swap", bn, split, 0, 1)
+    for out in ("bf16", "fp32"):
+        o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=TORCH_OUT[out])
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy(), ref, out, f"mx swap/{bn}/{split} {M}x{N}x{K} {out}")
+
+
+@pytest.mark.parametrize("split,grid", [(7, 0), (0, 0), (0, 13), (1, 5)])
+def test_mx_bit_stable_and_persistent(fp8bq, split, grid):
+    M, N, K = 24, 1024, 4096
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_full_grid)
+    d = upload(qa, sa, qw, sw)
+    v = fp8bq.make_variant("swap", 32, split, grid, 1)
+    outs = [fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=torch.float32)
+            for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    check_gemm(outs[0].cpu().numpy(), oracle_full(qa, sa, qw, sw, True), "fp32",
+               f"mx split {split} grid {grid}")
+
+
+@pytest.mark.parametrize("N,K", synth.DECODE_NK)
+@pytest.mark.parametrize("M,bn,split", [(1, 16, 1), (8, 16, 0), (24, 32, 4), (128, 128, 2)])
+def test_mx_decode_full_size_sampled(fp8bq, N, K, M, bn, split):
+    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode, weight="bf16")
+    v = fp8bq.make_variant("swap", bn, split, 0, 1)
+    d = upload(qa, sa, qw, sw)
+    rows = sample_rows(M, 6)
+    ref = oracle_rows(qa, sa, qw, sw, True, rows)
+    for out in ("bf16", "fp32"):
+        o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=TORCH_OUT[out])
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy()[rows], ref, out, f"mx decode {M}x{N}x{K} {out}")
+
+
+def test_mx_rejections(fp8bq):
+    for (K, ue, kind) in ((512, False, "swap"),    # fp32 scales
+                          (640, True, "swap"),     # K not a multiple of 512
+                          (512, True, "normal")):  # swap-AB tiles only
+        xb, qa, sa, qw, sw = quantised_problem(16, 256, K, ue, synth.act_decode)
+        d = upload(qa, sa, qw, sw)
+        with pytest.raises(fp8bq.Fp8bqError) as e:
+            fp8bq.fp8bq_gemm_variant(*d, fp8bq.make_variant(kind, 128 if kind == "normal" else 16,
+                                                            1, 0, 1),
+                                     fmt="ue8m0" if ue else "fp32", out_dtype=torch.float32)
+        assert e.value.status == 4
+
+
 @pytest.mark.parametrize("grid", [1, 3, 7])
 def test_persistent_grid_loops_over_items(fp8bq, grid):
     M, N, K = 40, 640, 1280
