@@ -89,9 +89,9 @@ def quantised_problem(M, N, K, ue, act_maker, weight="f32"):
 
 
 def sample_rows(M: int, k: int = 8, seed: int = 11):
-    """Rows 0, M-1, the first and last row of the second 128-row tile and a
-    seeded sample of the rest."""
-    base = {0, M - 1}
+    """Rows 0, M-1, the first and last row of the second 128-row tile, the
+    first row of the last 128-row tile and a seeded sample of the rest."""
+    base = {0, M - 1, (M - 1) // 128 * 128}
     if M > 128:
         base |= {127, 128, min(M - 1, 255)}
     rng = np.random.default_rng(seed)

@@ -2,6 +2,8 @@
 layer against the fp64 oracle, within the stated element-wise / Frobenius
 bounds.  Inputs are quantised by the oracle on the host, so the GEMM is
 checked independently of the GPU quant kernel."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -81,20 +83,6 @@ def test_mx_bit_stable_and_persistent(fp8bq, split, grid):
                f"mx split {split} grid {grid}")
 
 
-@pytest.mark.parametrize("N,K", synth.DECODE_NK)
-@pytest.mark.parametrize("M,bn,split", [(1, 16, 1), (8, 16, 0), (24, 32, 4), (128, 128, 2)])
-def test_mx_decode_full_size_sampled(fp8bq, N, K, M, bn, split):
-    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode, weight="bf16")
-    v = fp8bq.make_variant("swap", bn, split, 0, 1)
-    d = upload(qa, sa, qw, sw)
-    rows = sample_rows(M, 6)
-    ref = oracle_rows(qa, sa, qw, sw, True, rows)
-    for out in ("bf16", "fp32"):
-        o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=TORCH_OUT[out])
-        torch.cuda.synchronize()
-        check_gemm(o.float().cpu().numpy()[rows], ref, out, f"mx decode {M}x{N}x{K} {out}")
-
-
 def test_mx_rejections(fp8bq):
     for (K, ue, kind) in ((512, False, "swap"),    # fp32 scales
                           (640, True, "swap"),     # K not a multiple of 512
@@ -161,25 +149,43 @@ def test_small_config_full(fp8bq):
     check_gemm(o2.float().cpu().numpy(), ref, "bf16", "small config linear")
 
 
+@functools.lru_cache(maxsize=3)
+def _decode_weights(N, K):
+    """Oracle-quantised decode weights (UE8M0), on the host and the device."""
+    wb = synth.weight_bf16(N, K)
+    qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+    return qw, sw, to_dev(qw), to_dev(sw)
+
+
 @pytest.mark.parametrize("N,K", synth.DECODE_NK)
-@pytest.mark.parametrize("M", [1, 8, 24, 128])
-def test_decode_full_size_sampled(fp8bq, N, K, M):
-    """Decode sweep shapes at full size (UE8M0, bf16 out), in the variant the
-    table selects; sampled rows, all columns."""
-    xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode, weight="bf16")
-    o = fp8bq.fp8bq_gemm(*upload(qa, sa, qw, sw), fmt="ue8m0", out_dtype=torch.bfloat16)
+@pytest.mark.parametrize("M", synth.DECODE_M)
+def test_decode_every_element(fp8bq, N, K, M):
+    """The decode sweep at full size (UE8M0, bf16 out): every output element,
+    in the variant the table selects and in both scale paths (CUDA-core
+    promotion and block-scaled MMA) of that variant's shape."""
+    qw, sw, dqw, dsw = _decode_weights(N, K)
+    qa, sa = oracle.quant_act(synth.act_decode(M, K), oracle.BF16, 128, True)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    da, dsa = to_dev(qa), scales_to_dev(sa)
+    o = fp8bq.fp8bq_gemm(da, dsa, dqw, dsw, fmt="ue8m0", out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
-    rows = sample_rows(M, 6)
-    check_gemm(o.float().cpu().numpy()[rows], oracle_rows(qa, sa, qw, sw, True, rows), "bf16",
-               f"decode {M}x{N}x{K}")
+    check_gemm(o.float().cpu().numpy(), ref, "bf16", f"decode {M}x{N}x{K} (table)")
+    sel = fp8bq.fp8bq_select_variant(M, N, K, "ue8m0", "bf16")
+    for mx in (0, 1):
+        v = fp8bq.make_variant(sel["kind"], sel["block_n"], sel["split"], sel["grid"], mx)
+        o = fp8bq.fp8bq_gemm_variant(da, dsa, dqw, dsw, v, fmt="ue8m0", out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy(), ref, "bf16", f"decode {M}x{N}x{K} {v.as_dict()}")
 
 
 @pytest.mark.parametrize("N,K", synth.PREFILL_NK)
-@pytest.mark.parametrize("M", [256, 1536, 4096])
+@pytest.mark.parametrize("M", synth.PREFILL_M)
 def test_prefill_full_size_sampled(fp8bq, N, K, M):
+    """Prefill sweep at full size (fp32 scales, bf16 and fp32 out): all N
+    columns of 64 seeded rows plus the tile-boundary rows."""
     xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_prefill, weight="bf16")
     d = upload(qa, sa, qw, sw)
-    rows = sample_rows(M, 5)
+    rows = sample_rows(M, 64)
     ref = oracle_rows(qa, sa, qw, sw, False, rows)
     for out in ("bf16", "fp32"):
         o = fp8bq.fp8bq_gemm(*d, fmt="fp32", out_dtype=TORCH_OUT[out])
@@ -187,22 +193,29 @@ def test_prefill_full_size_sampled(fp8bq, N, K, M):
         check_gemm(o.float().cpu().numpy()[rows], ref, out, f"prefill {M}x{N}x{K} {out}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1536, 7168), (48, 7168, 1536), (300, 4096, 7168),
-                                   (2048, 24576, 7168)])
-@pytest.mark.parametrize("out", ["fp16", "bf16"])
-def test_linear_full_grid_sampled(fp8bq, M, N, K, out):
-    """Fused quant + GEMM (UE8M0) on full-grid shapes; the reference quantises
-    with the oracle on the host."""
-    xb = synth.act_full_grid(M, K)
+@functools.lru_cache(maxsize=2)
+def _full_grid_weights(N, K):
     wb = synth.weight_bf16(N, K)
-    wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
-    o = fp8bq.fp8bq_linear(to_dev_bits(xb), wq, ws, fmt="ue8m0", out_dtype=TORCH_OUT[out])
-    torch.cuda.synchronize()
-    rows = sample_rows(M, 4)
     qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+    return wb, qw, sw
+
+
+@pytest.mark.parametrize("N,K", synth.FULL_NK)
+@pytest.mark.parametrize("M", [1, 24, 128, 512, 4096])
+def test_linear_full_grid(fp8bq, N, K, M):
+    """Fused quant + GEMM (UE8M0, fp16 and bf16 out) on the full-grid shapes;
+    the reference quantises with the oracle on the host.  Every element for
+    M <= 128, else all columns of 64 seeded rows plus the tile-boundary rows."""
+    wb, qw, sw = _full_grid_weights(N, K)
+    xb = synth.act_full_grid(M, K)
+    wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
+    rows = list(range(M)) if M <= 128 else sample_rows(M, 64)
     qa, sa = oracle.quant_act(np.ascontiguousarray(xb[rows]), oracle.BF16, 128, True)
     ref = oracle_full(qa, sa, qw, sw, True)
-    check_gemm(o.float().cpu().numpy()[rows], ref, out, f"linear {M}x{N}x{K}")
+    for out in ("fp16", "bf16"):
+        o = fp8bq.fp8bq_linear(to_dev_bits(xb), wq, ws, fmt="ue8m0", out_dtype=TORCH_OUT[out])
+        torch.cuda.synchronize()
+        check_gemm(o.float().cpu().numpy()[rows], ref, out, f"linear {M}x{N}x{K} {out}")
 
 
 def test_empty_and_errors(fp8bq):
