@@ -88,6 +88,11 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+def variant_name(v: dict) -> str:
+    """kind/block_n/s<split>, with /mx when the tensor core applies the scales."""
+    return "{kind}/{block_n}/s{split}".format(**v) + ("/mx" if v.get("mma_scale") else "")
+
+
 def gemm_source_hash():
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh", "internal.h"):
@@ -430,14 +435,18 @@ def run_gpu(args, rank, world):
                     "tflops": round(fl / t / 1e12, 2),
                     "gbs_pages": round(pages_gbs_bytes(M, N, K) / t / 1e9, 1),
                     "gbs_alg": round(b / t / 1e9, 1), "roofline_frac": round(t_roof / t, 3),
-                    "variant": "{kind}/{block_n}/s{split}".format(**variants[(M, N, K)]),
+                    "variant": variant_name(variants[(M, N, K)]),
                     "h100_deepgemm_us": H100_DEEPGEMM_US.get((M, N, K))})
+    n_mx = sum(1 for p in probs if variants[p]["mma_scale"])
     tot_gemm_bytes = sum(gemm_bytes(*p) for p in probs)
     achieved = tot_gemm_bytes / (gemm_us.sum() * 1e-6) / 1e9
     traffic = profile_traffic()
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": traffic, "kernel": "gemm_kernel (decode sweep, 33 launches per step)",
+            "traffic": traffic,
+            "kernel": f"block-scaled FP8 GEMM, decode sweep: {len(probs)} launches per step "
+                      f"({n_mx} gemm_mx_kernel, {len(probs) - n_mx} gemm_kernel, as the "
+                      "table selects)",
             "algorithmic_bytes_per_launch_avg": tot_gemm_bytes / len(probs),
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
     cpu = None
