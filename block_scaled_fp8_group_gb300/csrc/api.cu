@@ -91,8 +91,8 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 // ------------------------------------------------------- variant table
 //
 // Text file, one entry per line:  N K fmt out M kind block_n split grid [mma_scale]
-// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap; mma_scale 0 when
-// absent).  Per
+// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap|swap64; mma_scale 0
+// when absent).  Per
 // (N, K, fmt, out) the entries form an M grid; a lookup takes the grid point
 // nearest to M, the smaller one on a tie ("vLLM 量化 Kernel 配置机制" §4.2:
 // configs[min(keys, key=|x - M|)], e.g. M=37 -> 32, M=2050 -> 2048).
@@ -140,6 +140,7 @@ int parse_out(const char* s) {
 int parse_kind(const char* s) {
     if (!std::strcmp(s, "normal")) return FP8BQ_KIND_NORMAL;
     if (!std::strcmp(s, "swap")) return FP8BQ_KIND_SWAP_AB;
+    if (!std::strcmp(s, "swap64")) return FP8BQ_KIND_SWAP_AB_64;
     return -1;
 }
 

@@ -61,12 +61,21 @@ constexpr int SLOT_BYTES = 768;      // per slab: 128 act scales, 2 weight-scale
 constexpr int SLOT_SW = 512;         // weight-scale chunk c at SLOT_SW + c * SLOT_SW_STEP
 constexpr int SLOT_SW_STEP = 128;    // (TMA destinations 128-byte aligned)
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, int WM = BM>
 struct Cfg {
-    static constexpr int A_BYTES = BM * BK;
+    // MMA-M rows of a tile: tokens (normal, always 128) or weight rows (swap:
+    // 128, or 64 with the M = 64 MMA, whose accumulator row r sits at TMEM
+    // lane 32*(r/16) + r%16, i.e. lanes 0-15 of each 32-lane quarter)
+    static constexpr int MR = SWAP ? WM : BM;
+    static_assert(MR == 128 || (SWAP && MR == 64), "tile rows");
+    static constexpr int ROWS_PER_QUAD = MR / 4;
+    static constexpr int A_BYTES = MR * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN <= 16 ? 10 : BN <= 32 ? 9 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
+    // 64-row weight tiles carry half the bytes per stage, so twice the stages
+    // keep the same bytes in flight
+    static constexpr int STAGES_128 = BN <= 16 ? 10 : BN <= 32 ? 9 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
+    static constexpr int STAGES = MR == 128 ? STAGES_128 : (BN <= 16 ? 18 : 15);
     // TMEM accumulator buffers: as many as fit in the 512 columns (at most 8)
     static constexpr int NBUF = 512 / BN >= 8 ? 8 : 512 / BN;
     static constexpr int TMEM_NEED = NBUF * BN;
@@ -90,9 +99,10 @@ struct Cfg {
     static constexpr int REG_EPI = 208;   // per thread, epilogue warpgroups
     static constexpr int REG_MIN_LAUNCH =  // registers per thread the launch must provide
         (REG_ROLE * 128 + REG_EPI * 32 * EPI_WARPS + THREADS - 1) / THREADS;
+    static constexpr int SRC = STAGES + 4 > SR ? STAGES + 4 : SR;  // scale ring depth
     static constexpr int RING_OFF = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * NBUF + 1) + 16;
+    static constexpr int BAR_OFF = RING_OFF + SRC * SLOT_BYTES;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SRC + 2 * NBUF + 1) + 16;
     static constexpr int FACT_OFF = (BAR_OFF + BAR_BYTES + 15) / 16 * 16;  // per-warp factors
     static constexpr int SMEM = 1024 + FACT_OFF + EPI_WARPS * CPT * 4;
     static constexpr int CHUNK = (REGSPLIT || CPT == 32) ? 32 : 16;  // TMEM columns per load
@@ -192,13 +202,13 @@ struct TileOrigin {
     int w0;    // first weight row (n)
 };
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, int WM = BM>
 __device__ __forceinline__ TileOrigin tile_origin(const KArgs& a, int tile) {
     const int wt = tile / a.tiles_tok;       // weight tile (slow)
     const int tt = tile - wt * a.tiles_tok;  // token tile (fast: neighbours share weights)
     TileOrigin o;
     if (SWAP) {
-        o.w0 = wt * BM;
+        o.w0 = wt * WM;
         o.tok0 = tt * BN;
     } else {
         o.w0 = wt * BN;
@@ -263,18 +273,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
 }
 
-template <bool SWAP, int BN>
-__global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
+template <bool SWAP, int BN, int WM>
+__global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_sa,     // act scales [cols][Mp] 4-byte
                 const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                 const KArgs a) {
-    using C = Cfg<SWAP, BN>;
+    using C = Cfg<SWAP, BN, WM>;
+    constexpr int SR = C::SRC;  // scale ring depth of this configuration
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                            // STAGES x [128 rows x 128 B]
+    uint8_t* sA = smem;                            // STAGES x [MR rows x 128 B]
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;   // STAGES x [BN rows x 128 B]
     uint8_t* ring = smem + C::RING_OFF;            // SR x SLOT_BYTES
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
         wi.init(a);
         Seg sg;
         if (wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
             const int nslab = sg.kb1 - sg.kb0;
             prefetched = nslab < C::STAGES ? nslab : C::STAGES;
             for (int i = 0; i < prefetched; ++i) {
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
             Seg sg;
             bool ok = true;
             while (ok && wi.next(a, sg)) {
-                const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+                const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
                 const int row_m = SWAP ? o.w0 : o.tok0;
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
@@ -441,7 +452,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            constexpr uint32_t idesc = idesc_e4m3_f32(C::MR, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, bphase = 0;
             WorkIter wi;
@@ -486,7 +497,10 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
         const int ew = warp - C::EPI_FIRST;
         const int quad = warp & 3;   // TMEM lanes this warp may access
         const int chalf = ew >> 2;   // column half (8 epilogue warps)
-        const int row = quad * 32 + lane;
+        // MMA-M row of this lane; with 64-row tiles lanes 16-31 hold none
+        // and skip every store and partial access
+        const int row = quad * C::ROWS_PER_QUAD + lane;
+        const bool row_ok = lane < C::ROWS_PER_QUAD;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                 static_cast<uint32_t>(chalf * C::CPT);
         int buf = 0, slot = 0;
@@ -496,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
         Seg sg;
         bool ok = true;
         while (ok && wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
             const int nb = o.w0 / BK;
             float acc[C::CPT];
 #pragma unroll
@@ -591,11 +605,13 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
             // the tile and takes its own ticket for it, so no barrier between
             // warps is needed (and none can be left waiting after an abort).
             if (sg.nparts > 1) {
-                constexpr int64_t TILE = BM * BN;
+                constexpr int64_t TILE = C::MR * BN;
                 float* mine = a.partials + part_slot(a, sg.tile, sg.part) * TILE;
+                if (row_ok) {
 #pragma unroll
-                for (int j = 0; j < C::CPT; ++j)
-                    __stcg(mine + (chalf * C::CPT + j) * BM + row, acc[j]);
+                    for (int j = 0; j < C::CPT; ++j)
+                        __stcg(mine + (chalf * C::CPT + j) * C::MR + row, acc[j]);
+                }
                 __threadfence();
                 __syncwarp();
                 unsigned* ctr = a.counters + static_cast<int64_t>(sg.tile) * kCountersPerTile + ew;
@@ -621,9 +637,10 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
                             const int p = p0 + q;
                             if (p < sg.nparts && p != sg.part) {
                                 const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
-                                                   (chalf * C::CPT + c0) * BM + row;
+                                                   (chalf * C::CPT + c0) * C::MR + row;
 #pragma unroll
-                                for (int j = 0; j < RC; ++j) t[q][j] = __ldcg(src + j * BM);
+                                for (int j = 0; j < RC; ++j)
+                                    t[q][j] = row_ok ? __ldcg(src + j * C::MR) : 0.0f;
                             }
                         }
 #pragma unroll
@@ -659,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN>::THREADS, 1)
             } else {
                 const int n = o.w0 + row;
                 const int t0 = o.tok0 + chalf * C::CPT;
-                if (n < a.N) {
+                if (row_ok && n < a.N) {
 #pragma unroll
                     for (int j = 0; j < C::CPT; ++j)
                         if (t0 + j < a.M)
@@ -1126,15 +1143,15 @@ bool encode_operand(CUtensorMap* map, const void* base, uint64_t K, uint64_t row
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool SWAP, int BN>
+template <bool SWAP, int BN, int WM = BM>
 cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
-    using C = Cfg<SWAP, BN>;
+    using C = Cfg<SWAP, BN, WM>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        err = cudaFuncSetAttribute(gemm_kernel<SWAP, BN>,
+        err = cudaFuncSetAttribute(gemm_kernel<SWAP, BN, WM>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (err != cudaSuccess) return err;
         if (C::REGSPLIT) {
@@ -1142,7 +1159,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
             // launch that provides fewer registers in total would never
             // satisfy setmaxnreg.inc, so refuse it
             cudaFuncAttributes fa;
-            err = cudaFuncGetAttributes(&fa, gemm_kernel<SWAP, BN>);
+            err = cudaFuncGetAttributes(&fa, gemm_kernel<SWAP, BN, WM>);
             if (err != cudaSuccess) return err;
             if (fa.numRegs < C::REG_MIN_LAUNCH) {
                 log_error("GEMM kernel compiled with too few registers for its register split");
@@ -1151,7 +1168,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         }
         attr_done[dev] = 1;
     }
-    if constexpr (SWAP) {
+    if constexpr (SWAP && WM == BM) {
         static int mx_attr_done[64] = {0};
         if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
             err = cudaFuncSetAttribute(gemm_mx_kernel<BN>,
@@ -1169,7 +1186,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     CUtensorMap tm_m, tm_n, tm_sa, tm_sw;
     bool ok;
     if (swap) {
-        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), BM) &&
+        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), WM) &&
              encode_operand(&tm_n, g.a_q, K, static_cast<uint64_t>(g.M), BN);
     } else {
         ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
@@ -1229,14 +1246,14 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if constexpr (SWAP) {
+    if constexpr (SWAP && WM == BM) {
         if (p.mx) {
             cfg.blockDim = dim3(MxCfg<BN>::THREADS);
             cfg.dynamicSmemBytes = MxCfg<BN>::SMEM;
             return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<BN>, tm_m, tm_n, tm_sa, tm_sw, a);
         }
     }
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
 }  // namespace
@@ -1244,9 +1261,14 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
                     GemmPlan* p) {
     const int G = static_cast<int>(K / BK);
-    const bool swap = v.kind == FP8BQ_KIND_SWAP_AB;
-    if (v.kind != FP8BQ_KIND_SWAP_AB && v.kind != FP8BQ_KIND_NORMAL) return false;
-    if (swap) {
+    const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
+    const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
+    if (v.kind != FP8BQ_KIND_SWAP_AB && v.kind != FP8BQ_KIND_NORMAL &&
+        v.kind != FP8BQ_KIND_SWAP_AB_64)
+        return false;
+    if (v.kind == FP8BQ_KIND_SWAP_AB_64) {
+        if (v.block_n != 16 && v.block_n != 32) return false;
+    } else if (swap) {
         if (v.block_n != 16 && v.block_n != 32 && v.block_n != 64 && v.block_n != 128) return false;
     } else {
         if (v.block_n != 128 && v.block_n != 256) return false;
@@ -1254,14 +1276,15 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (v.split < 0 || v.split > 64 || v.split > G) return false;
     if (v.grid < 0) return false;
     if (v.mma_scale != 0 && v.mma_scale != 1) return false;
-    if (v.mma_scale && !swap) return false;  // block-scaled MMA: swap-AB tiles only
+    // block-scaled MMA: 128-row swap-AB tiles only
+    if (v.mma_scale && v.kind != FP8BQ_KIND_SWAP_AB) return false;
     p->mx = v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;
     p->split = v.split;
     if (swap) {
         p->tiles_tok = static_cast<int>((M + v.block_n - 1) / v.block_n);
-        p->tiles_w = static_cast<int>((N + BM - 1) / BM);
+        p->tiles_w = static_cast<int>((N + wm - 1) / wm);
     } else {
         p->tiles_tok = static_cast<int>((M + BM - 1) / BM);
         p->tiles_w = static_cast<int>((N + v.block_n - 1) / v.block_n);
@@ -1269,7 +1292,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     const long long tiles = static_cast<long long>(p->tiles_tok) * p->tiles_w;
     if (tiles <= 0 || tiles > (1LL << 30)) return false;
     const int g = v.grid > 0 ? v.grid : num_sms;
-    const size_t tile_bytes = static_cast<size_t>(BM) * v.block_n * sizeof(float);
+    const size_t tile_bytes = static_cast<size_t>(swap ? wm : BM) * v.block_n * sizeof(float);
     if (v.split == 0) {
         // stream-K: one CTA per equal share of the tiles x G (tile, slab) units
         const long long units = tiles * G;
@@ -1290,7 +1313,12 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
-    if (p.kind == FP8BQ_KIND_SWAP_AB) {
+    if (p.kind == FP8BQ_KIND_SWAP_AB_64) {
+        switch (p.bn) {
+            case 16: return launch_bn<true, 16, 64>(p, g, stream);
+            case 32: return launch_bn<true, 32, 64>(p, g, stream);
+        }
+    } else if (p.kind == FP8BQ_KIND_SWAP_AB) {
         switch (p.bn) {
             case 16: return launch_bn<true, 16>(p, g, stream);
             case 32: return launch_bn<true, 32>(p, g, stream);

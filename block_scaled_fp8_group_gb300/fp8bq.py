@@ -25,7 +25,8 @@ STATUS_NAMES = {
 }
 SCALE_FP32, SCALE_UE8M0 = 0, 1
 BF16, FP16, FP32 = 0, 1, 2
-KIND_NORMAL, KIND_SWAP_AB = 0, 1
+KIND_NORMAL, KIND_SWAP_AB, KIND_SWAP_AB_64 = 0, 1, 2
+_KIND_NAMES = {KIND_NORMAL: "normal", KIND_SWAP_AB: "swap", KIND_SWAP_AB_64: "swap64"}
 
 EXPORTS = (
     "fp8bq_act_scale_bytes", "fp8bq_weight_scale_bytes", "fp8bq_gemm_workspace_bytes",
@@ -50,7 +51,7 @@ class Variant(ctypes.Structure):
                 ("mma_scale", ctypes.c_int32)]
 
     def as_dict(self):
-        return {"kind": "swap" if self.kind == KIND_SWAP_AB else "normal",
+        return {"kind": _KIND_NAMES.get(self.kind, str(self.kind)),
                 "block_n": self.block_n, "split": self.split, "grid": self.grid,
                 "mma_scale": self.mma_scale, "from_table": bool(self.from_table)}
 
@@ -216,7 +217,7 @@ def make_variant(kind, block_n: int, split: int = 1, grid: int = 0,
                  mma_scale: int = 0) -> Variant:
     """A GEMM variant; mma_scale=1 has the tensor core apply UE8M0 scales
     (block-scaled MMA; swap-AB, UE8M0, K % 512 == 0)."""
-    k = kind if isinstance(kind, int) else (KIND_SWAP_AB if kind == "swap" else KIND_NORMAL)
+    k = kind if isinstance(kind, int) else {v: k for k, v in _KIND_NAMES.items()}[kind]
     return Variant(k, block_n, split, grid, 0, mma_scale)
 
 

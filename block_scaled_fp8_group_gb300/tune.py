@@ -5,7 +5,8 @@ kernel configuration and keep the fastest).
     python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small \
         [--out block_scaled_fp8_group_gb300/tables/<device>.tbl]
 
-Candidates per M: swap-AB with token tiles 16..128 and the normal
+Candidates per M: swap-AB with token tiles 16..128 (and 64 weight rows per
+tile for token tiles up to 32) and the normal
 orientation with 128/256-wide weight tiles, each with stream-K (split 0),
 no split, and a few fixed K splits; with UE8M0 scales and K % 512 == 0 every
 swap-AB candidate also runs with the scales applied by the block-scaled MMA
@@ -56,6 +57,8 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
             for split in (0, 1, 2, 3, 4, 6, 8):
                 if split <= G:
                     out += [("swap", bn, split, m) for m in ((0, 1) if mx else (0,))]
+                    if bn <= 32:
+                        out.append(("swap64", bn, split, 0))
     else:
         for bn in (128, 256):
             for split in (0, 1, 2):

@@ -69,7 +69,9 @@ typedef enum { FP8BQ_BF16 = 0, FP8BQ_FP16 = 1, FP8BQ_FP32 = 2 } fp8bq_dtype;
  * configs, nearest-M lookup. */
 typedef enum {
     FP8BQ_KIND_NORMAL = 0, /* MMA M = 128 tokens, MMA N = block_n weight rows */
-    FP8BQ_KIND_SWAP_AB = 1 /* D^T = W A^T: MMA M = 128 weight rows, MMA N = block_n tokens */
+    FP8BQ_KIND_SWAP_AB = 1, /* D^T = W A^T: MMA M = 128 weight rows, MMA N = block_n tokens */
+    FP8BQ_KIND_SWAP_AB_64 = 2 /* swap-AB with 64 weight rows per tile (MMA M = 64), twice the
+                               * tiles of kind 1 for narrow N; block_n 16 or 32 */
 } fp8bq_kind;
 
 typedef struct {

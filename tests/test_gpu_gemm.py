@@ -29,7 +29,9 @@ def upload(qa, sa, qw, sw):
 
 
 # split 0 = stream-K (equal shares of the (tile, K slab) units per CTA)
+# swap64: 64 weight rows per tile (MMA M = 64)
 VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (0, 1, 2, 3)] +
+            [("swap64", bn, s) for bn in (16, 32) for s in (0, 1, 2, 3)] +
             [("normal", bn, s) for bn in (128, 256) for s in (0, 1, 2, 5)])
 
 
@@ -161,8 +163,9 @@ def _decode_weights(N, K):
 @pytest.mark.parametrize("M", synth.DECODE_M)
 def test_decode_every_element(fp8bq, N, K, M):
     """The decode sweep at full size (UE8M0, bf16 out): every output element,
-    in the variant the table selects and in both scale paths (CUDA-core
-    promotion and block-scaled MMA) of that variant's shape."""
+    in the variant the table selects, and with the table's token tile and split
+    in both scale paths (CUDA-core promotion, block-scaled MMA) and, for token
+    tiles up to 32, with 64-row weight tiles."""
     qw, sw, dqw, dsw = _decode_weights(N, K)
     qa, sa = oracle.quant_act(synth.act_decode(M, K), oracle.BF16, 128, True)
     ref = oracle_full(qa, sa, qw, sw, True)
@@ -171,8 +174,10 @@ def test_decode_every_element(fp8bq, N, K, M):
     torch.cuda.synchronize()
     check_gemm(o.float().cpu().numpy(), ref, "bf16", f"decode {M}x{N}x{K} (table)")
     sel = fp8bq.fp8bq_select_variant(M, N, K, "ue8m0", "bf16")
-    for mx in (0, 1):
-        v = fp8bq.make_variant(sel["kind"], sel["block_n"], sel["split"], sel["grid"], mx)
+    bn, split = sel["block_n"], sel["split"]
+    others = [("swap", 0), ("swap", 1)] + ([("swap64", 0)] if bn <= 32 else [])
+    for kind, mx in others:
+        v = fp8bq.make_variant(kind, bn, split, 0, mx)
         o = fp8bq.fp8bq_gemm_variant(da, dsa, dqw, dsw, v, fmt="ue8m0", out_dtype=torch.bfloat16)
         torch.cuda.synchronize()
         check_gemm(o.float().cpu().numpy(), ref, "bf16", f"decode {M}x{N}x{K} {v.as_dict()}")
