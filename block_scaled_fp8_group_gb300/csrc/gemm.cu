@@ -701,9 +701,9 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
 
 // ------------------------------------------------------ block-scaled path
 //
-// Swap-AB with UE8M0 scales applied by the tensor core: the E8M0 factors of
-// the weights (one per 128x128 block) and of the tokens (one per 1x128 group)
-// go to TMEM, and tcgen05.mma.kind::mxf8f6f4.block_scale multiplies each
+// UE8M0 scales applied by the tensor core (both orientations): the E8M0
+// factors of the weights (one per 128x128 block) and of the tokens (one per
+// 1x128 group) go to TMEM, and tcgen05.mma.kind::mxf8f6f4.block_scale multiplies each
 // 32-wide K block's products by 2^(ea+ew) as it accumulates, so a segment's
 // sum of promoted slab products builds up in one TMEM accumulator and is read
 // once.  A slab's four K blocks share its group's factors.  The packed UE8M0
@@ -711,33 +711,43 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
 // are: slab kb uses byte kb % 4 (the instruction's factor ids) of word kb / 4.
 //
 //   warp 0     TMA: per slab the weight and token tiles (as gemm_kernel);
-//              per 4-slab group the tile's token factor words and the weight
-//              block's four fp32 scales into the scale ring.
+//              per 4-slab group the tile's token factor words and the four
+//              fp32 scales of each weight block of the tile into the scale
+//              ring.
 //   warp 1     MMA issuer; owns TMEM.  Per slab four block-scaled MMAs into
-//              the segment's accumulator (two, alternating by segment).
+//              the segment's accumulator (two alternating by segment, one for
+//              256-wide tiles).
 //   warps 2-5  factor writers: per group, tcgen05.st of the factor words into
 //              a TMEM ring entry, each warp into its 32-lane quarter (every
-//              quarter holds a full copy: weight word at columns 0-3, token
-//              word of token 32c+l at lane l, column 8+c).
+//              quarter holds a full copy).  MMA-M operand factors at columns
+//              0-3 (row r: lane r%32, column r/32), MMA-N operand factors from
+//              column 8: swap-AB -- weight word x4, then token 32c+l at lane
+//              l, column 8+c; normal -- token words x4, then the word of
+//              weight block c/4 in column 8+c.
 //   warps 6-9  epilogue: per segment, read the accumulator, store or reduce
 //              the split parts (same workspace protocol as gemm_kernel).
 //
 // Requires K % 512 == 0 (whole groups of four slabs, so the four weight
 // scales of a group are one aligned 16-byte chunk).
-template <int BN>
+template <bool SWAP, int BN>
 struct MxCfg {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = Cfg<true, BN>::STAGES;
-    static constexpr int NC = (BN + 31) / 32;       // factor columns of the token operand
+    static constexpr int STAGES = Cfg<SWAP, BN>::STAGES;
+    static constexpr int NC = (BN + 31) / 32;       // factor columns of the MMA-N operand
+    static constexpr int TOK_WORDS = SWAP ? BN : BM;  // token factor words per group
+    static constexpr int WBLK = SWAP ? 1 : BN / BK;   // weight blocks per tile
     // one factor-ring entry: weight factors at columns +0..3, token factors at
     // +8..8+NC-1; both start on an 8-column boundary (tcgen05.st.x4 and the
     // MMA's factor addresses need aligned columns)
     static constexpr int SF_B = 8;
     static constexpr int SF_COLS = 16;
     static constexpr int RF = 8;                    // factor-ring entries (groups in flight)
-    static constexpr int SF_BASE = 2 * BN;          // after the two accumulators
+    // accumulators: two (the next segment's MMAs overlap this one's read-out)
+    // when they fit beside the factor ring
+    static constexpr int NACC = 2 * BN + RF * SF_COLS <= 512 ? 2 : 1;
+    static constexpr int SF_BASE = NACC * BN;       // after the accumulators
     static constexpr int TMEM_NEED = SF_BASE + RF * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                      : TMEM_NEED <= 64  ? 64
@@ -749,27 +759,28 @@ struct MxCfg {
     static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // accumulator columns per TMEM load
     static constexpr int RING_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * RF + 4 + 1) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * RF + 2 * NACC + 1) + 16;
     static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
     static_assert(TMEM_NEED <= 512, "TMEM columns");
     static_assert(SF_BASE % 16 == 0 && NC <= SF_COLS - SF_B, "factor-ring column alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static_assert(4 * BN <= SLOT_SW, "token factor words fit the scale slot");
+    static_assert(4 * TOK_WORDS <= SLOT_SW && SLOT_SW + WBLK * SLOT_SW_STEP <= SLOT_BYTES,
+                  "scale slot layout");
 };
 
-template <int BN>
-__global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
-    gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_w,    // weights [N, K] e4m3
-                   const __grid_constant__ CUtensorMap tm_tok,  // tokens [M, K] e4m3
-                   const __grid_constant__ CUtensorMap tm_sa,   // packed act words [G/4][Mp]
-                   const __grid_constant__ CUtensorMap tm_sw,   // weight scales, flat fp32
+template <bool SWAP, int BN>
+__global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
+                   const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
+                   const __grid_constant__ CUtensorMap tm_sa,     // packed act words [G/4][Mp]
+                   const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                    const KArgs a) {
-    using C = MxCfg<BN>;
+    using C = MxCfg<SWAP, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                           // STAGES x [128 weight rows x 128 B]
-    uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN tokens x 128 B]
+    uint8_t* sA = smem;                           // STAGES x [128 MMA-M rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN MMA-N rows x 128 B]
     uint8_t* ring = smem + C::RING_OFF;           // SR x SLOT_BYTES
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + C::STAGES;
@@ -777,9 +788,9 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
     uint64_t* sempty = sfull + SR;
     uint64_t* ffull = sempty + SR;   // factor-ring entry written
     uint64_t* fempty = ffull + C::RF;  // factor-ring entry consumed by its MMAs
-    uint64_t* tfull = fempty + C::RF;  // accumulator complete (2)
-    uint64_t* tempty = tfull + 2;      // accumulator read out (2)
-    uint64_t* mma_done = tempty + 2;
+    uint64_t* tfull = fempty + C::RF;     // accumulator complete
+    uint64_t* tempty = tfull + C::NACC;   // accumulator read out
+    uint64_t* mma_done = tempty + C::NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -799,15 +810,15 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
             mbar_init(&ffull[r], 4);
             mbar_init(&fempty[r], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::NACC; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&tm_w);
-        tma_prefetch_desc(&tm_tok);
+        tma_prefetch_desc(&tm_mma_m);
+        tma_prefetch_desc(&tm_mma_n);
         tma_prefetch_desc(&tm_sa);
         tma_prefetch_desc(&tm_sw);
     }
@@ -831,13 +842,17 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
         wi.init(a);
         Seg sg;
         if (wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
             const int nslab = sg.kb1 - sg.kb0;
             prefetched = nslab < C::STAGES ? nslab : C::STAGES;
             for (int i = 0; i < prefetched; ++i) {
                 mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-                tma_load_2d_hint(sA + i * C::A_BYTES, &tm_w, &full[i], (sg.kb0 + i) * BK, o.w0,
-                                 policy_evict_first());
+                if (SWAP)
+                    tma_load_2d_hint(sA + i * C::A_BYTES, &tm_mma_m, &full[i], (sg.kb0 + i) * BK,
+                                     o.w0, policy_evict_first());
+                else
+                    tma_load_2d_hint(sB + i * C::B_BYTES, &tm_mma_n, &full[i], (sg.kb0 + i) * BK,
+                                     o.w0, policy_evict_first());
             }
         }
     }
@@ -847,8 +862,9 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_a = policy_evict_last();
+            // weights stream once; activations are re-read by other tiles
+            const uint64_t pol_m = SWAP ? policy_evict_first() : policy_evict_last();
+            const uint64_t pol_n = SWAP ? policy_evict_last() : policy_evict_first();
             int stage = 0, slot = 0;
             uint32_t phase = 0, sphase = 0;
             long long fills = 0, sfills = 0;
@@ -857,7 +873,9 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
             Seg sg;
             bool ok = true;
             while (ok && wi.next(a, sg)) {
-                const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+                const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+                const int row_m = SWAP ? o.w0 : o.tok0;
+                const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (kb == sg.kb0 || (kb & 3) == 0) {
@@ -868,9 +886,12 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
                             break;
                         }
                         uint8_t* sl = ring + slot * SLOT_BYTES;
-                        mbar_arrive_expect_tx(&sfull[slot], 4u * BN + 16u);
+                        mbar_arrive_expect_tx(&sfull[slot], 4u * C::TOK_WORDS + 16u * C::WBLK);
                         tma_load_2d(sl, &tm_sa, &sfull[slot], o.tok0, kb >> 2);
-                        tma_load_2d(sl + SLOT_SW, &tm_sw, &sfull[slot], nb * a.G + (kb & ~3), 0);
+#pragma unroll
+                        for (int b = 0; b < C::WBLK; ++b)
+                            tma_load_2d(sl + SLOT_SW + b * SLOT_SW_STEP, &tm_sw, &sfull[slot],
+                                        (nb + b) * a.G + (kb & ~3), 0);
                         ++sfills;
                         if (++slot == SR) {
                             slot = 0;
@@ -878,8 +899,13 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
                         }
                     }
                     if (fills < prefetched) {
-                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_tok, &full[stage], kb * BK,
-                                         o.tok0, pol_a);
+                        // the weight tile of this stage is already on its way
+                        if (SWAP)
+                            tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
+                                             kb * BK, row_n, pol_n);
+                        else
+                            tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
+                                             kb * BK, row_m, pol_m);
                     } else {
                         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
                                                tmo, code)) {
@@ -887,10 +913,10 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_w, &full[stage], kb * BK,
-                                         o.w0, pol_w);
-                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_tok, &full[stage], kb * BK,
-                                         o.tok0, pol_a);
+                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage], kb * BK,
+                                         row_m, pol_m);
+                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage], kb * BK,
+                                         row_n, pol_n);
                     }
                     ++fills;
                     if (++stage == C::STAGES) {
@@ -959,7 +985,7 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
-                if (++acc == 2) {
+                if (++acc == C::NACC) {
                     acc = 0;
                     aphase ^= 1u;
                 }
@@ -987,19 +1013,31 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint8_t* sl = ring + slot * SLOT_BYTES;
-                // weight word: byte j = E8M0 exponent of the block's scale of
+                // weight words: byte j = E8M0 exponent of the block's scale of
                 // slab 4*(kb/4)+j (the fp32 scales are powers of two)
-                const float* swc = reinterpret_cast<const float*>(sl + SLOT_SW);
-                uint32_t ww = 0;
+                uint32_t ww[C::WBLK];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) ww |= ((__float_as_uint(swc[j]) >> 23) & 0xFFu) << (8 * j);
+                for (int b = 0; b < C::WBLK; ++b) {
+                    const float* swc = reinterpret_cast<const float*>(sl + SLOT_SW + b * SLOT_SW_STEP);
+                    ww[b] = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        ww[b] |= ((__float_as_uint(swc[j]) >> 23) & 0xFFu) << (8 * j);
+                }
                 const uint32_t* tw = reinterpret_cast<const uint32_t*>(sl);
                 const uint32_t col = static_cast<uint32_t>(C::SF_BASE + r * C::SF_COLS);
-                tmem_st4(t_quarter + col, ww, ww, ww, ww);
+                if constexpr (SWAP) {
+                    tmem_st4(t_quarter + col, ww[0], ww[0], ww[0], ww[0]);
 #pragma unroll
-                for (int c = 0; c < C::NC; ++c) {
-                    const int t = 32 * c + lane;
-                    tmem_st1(t_quarter + col + C::SF_B + c, t < BN ? tw[t] : 0u);
+                    for (int c = 0; c < C::NC; ++c) {
+                        const int t = 32 * c + lane;
+                        tmem_st1(t_quarter + col + C::SF_B + c, t < BN ? tw[t] : 0u);
+                    }
+                } else {
+                    tmem_st4(t_quarter + col, tw[lane], tw[32 + lane], tw[64 + lane], tw[96 + lane]);
+#pragma unroll
+                    for (int b = 0; b < C::WBLK; ++b)
+                        tmem_st4(t_quarter + col + C::SF_B + 4 * b, ww[b], ww[b], ww[b], ww[b]);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -1021,7 +1059,7 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
     } else {
         // ---------------------------------------------------------- epilogue
         const int quad = warp & 3;
-        const int row = quad * 32 + lane;  // weight row within the tile
+        const int row = quad * 32 + lane;  // MMA-M row: weight row (swap-AB) or token
         int acc = 0;
         uint32_t aphase = 0;
         WorkIter wi;
@@ -1029,8 +1067,34 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
         Seg sg;
         bool ok = true;
         constexpr int NCH = BN / C::CHUNK;
+        // stores one chunk of this row's columns [c0, c0 + CHUNK) of the tile
+        auto store_chunk = [&](const TileOrigin& o, int c0, const float* v) {
+            if constexpr (SWAP) {
+                const int n = o.w0 + row;
+                if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; ++j) {
+                        const int t = o.tok0 + c0 + j;
+                        if (t < a.M)
+                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, v[j]);
+                    }
+                }
+            } else {
+                const int m = o.tok0 + row;
+                if (m < a.M) {
+#pragma unroll
+                    for (int j = 0; j < C::CHUNK; j += 8) {
+                        const int n0 = o.w0 + c0 + j;
+                        if (n0 < a.N)
+                            store_out8(a.out, a.out_dtype, static_cast<int64_t>(m) * a.N + n0, v[j],
+                                       v[j + 1], v[j + 2], v[j + 3], v[j + 4], v[j + 5], v[j + 6],
+                                       v[j + 7]);
+                    }
+                }
+            }
+        };
         while (ok && wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<true, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
             if (!warp_wait(&tfull[acc], aphase, abort_flag, a.status, tmo, code)) {
                 ok = false;
                 break;
@@ -1038,7 +1102,6 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
             tc_fence_after();
             const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            const int n = o.w0 + row;
             constexpr int64_t TILE = BM * BN;
             float* mine = sg.nparts > 1 ? a.partials + part_slot(a, sg.tile, sg.part) * TILE
                                         : nullptr;
@@ -1060,17 +1123,14 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; ++j)
                         __stcg(mine + (c * C::CHUNK + j) * BM + row, __uint_as_float(v[j]));
-                } else if (n < a.N) {
+                } else {
+                    float f[C::CHUNK];
 #pragma unroll
-                    for (int j = 0; j < C::CHUNK; ++j) {
-                        const int t = o.tok0 + c * C::CHUNK + j;
-                        if (t < a.M)
-                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n,
-                                       __uint_as_float(v[j]));
-                    }
+                    for (int j = 0; j < C::CHUNK; ++j) f[j] = __uint_as_float(v[j]);
+                    store_chunk(o, c * C::CHUNK, f);
                 }
             }
-            if (++acc == 2) {
+            if (++acc == C::NACC) {
                 acc = 0;
                 aphase ^= 1u;
             }
@@ -1097,14 +1157,7 @@ __global__ void __launch_bounds__(MxCfg<BN>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
                 }
-                if (n < a.N) {
-#pragma unroll
-                    for (int j = 0; j < C::CHUNK; ++j) {
-                        const int t = o.tok0 + c * C::CHUNK + j;
-                        if (t < a.M)
-                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, r[j]);
-                    }
-                }
+                store_chunk(o, c * C::CHUNK, r);
             }
             if (lane == 0) *ctr = 0u;  // ready for the next call
         }
@@ -1168,12 +1221,12 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         }
         attr_done[dev] = 1;
     }
-    if constexpr (SWAP && WM == BM) {
+    if constexpr (WM == BM) {
         static int mx_attr_done[64] = {0};
         if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
-            err = cudaFuncSetAttribute(gemm_mx_kernel<BN>,
+            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MxCfg<BN>::SMEM);
+                                       MxCfg<SWAP, BN>::SMEM);
             if (err != cudaSuccess) return err;
             mx_attr_done[dev] = 1;
         }
@@ -1246,11 +1299,11 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if constexpr (SWAP && WM == BM) {
+    if constexpr (WM == BM) {
         if (p.mx) {
-            cfg.blockDim = dim3(MxCfg<BN>::THREADS);
-            cfg.dynamicSmemBytes = MxCfg<BN>::SMEM;
-            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<BN>, tm_m, tm_n, tm_sa, tm_sw, a);
+            cfg.blockDim = dim3(MxCfg<SWAP, BN>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<SWAP, BN>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);
         }
     }
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM>, tm_m, tm_n, tm_sa, tm_sw, a);
@@ -1276,8 +1329,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (v.split < 0 || v.split > 64 || v.split > G) return false;
     if (v.grid < 0) return false;
     if (v.mma_scale != 0 && v.mma_scale != 1) return false;
-    // block-scaled MMA: 128-row swap-AB tiles only
-    if (v.mma_scale && v.kind != FP8BQ_KIND_SWAP_AB) return false;
+    // block-scaled MMA: 128-row tiles (swap-AB or normal), M = 128 MMAs only
+    if (v.mma_scale && v.kind == FP8BQ_KIND_SWAP_AB_64) return false;
     p->mx = v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;

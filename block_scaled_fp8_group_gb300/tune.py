@@ -9,8 +9,8 @@ Candidates per M: swap-AB with token tiles 16..128 (and 64 weight rows per
 tile for token tiles up to 32) and the normal
 orientation with 128/256-wide weight tiles, each with stream-K (split 0),
 no split, and a few fixed K splits; with UE8M0 scales and K % 512 == 0 every
-swap-AB candidate also runs with the scales applied by the block-scaled MMA
-(mma_scale 1).  Each candidate is timed on cold weights
+candidate with 128-row tiles also runs with the scales applied by the
+block-scaled MMA (mma_scale 1).  Each candidate is timed on cold weights
 (a rotation of weight copies larger than L2) as the mean of a batch of
 back-to-back launches queued behind a GPU sleep, so launch gaps do not count
 host time.  Lines of the table file: N K fmt out M kind block_n split grid
@@ -62,7 +62,7 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
     else:
         for bn in (128, 256):
             for split in (0, 1, 2):
-                out.append(("normal", bn, split, 0))
+                out += [("normal", bn, split, m) for m in ((0, 1) if mx else (0,))]
         for split in (0, 1):
             out += [("swap", 128, split, m) for m in ((0, 1) if mx else (0,))]
     return out

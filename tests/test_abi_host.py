@@ -164,6 +164,8 @@ def test_variant_workspace_bytes():
     mx4 = fp8bq.make_variant("swap", 16, 4, 0, 1)
     assert fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, mx4) == \
         fp8bq.fp8bq_variant_workspace_bytes(8, 7168, 18432, v4)
-    # ... and exists for swap-AB tiles only
+    # ... and exists for 128-row tiles only (M = 128 MMAs)
     assert fp8bq.fp8bq_variant_workspace_bytes(
-        256, 7168, 18432, fp8bq.make_variant("normal", 128, 2, 0, 1)) == 0
+        256, 7168, 18432, fp8bq.make_variant("normal", 128, 2, 0, 1)) > 0
+    assert fp8bq.fp8bq_variant_workspace_bytes(
+        8, 7168, 18432, fp8bq.make_variant("swap64", 16, 2, 0, 1)) == 0

@@ -52,22 +52,23 @@ def test_variants_small(fp8bq, kind, bn, split, M, N, K, ue):
         check_gemm(o.float().cpu().numpy(), ref, out, f"{kind}/{bn}/{split} {M}x{N}x{K} {out}")
 
 
-# block-scaled MMA: the tensor core applies the UE8M0 scales (swap-AB, K % 512 == 0)
-MX_VARIANTS = [(bn, s) for bn in (16, 32, 64, 128) for s in (0, 1, 2, 3)]
+# block-scaled MMA: the tensor core applies the UE8M0 scales (K % 512 == 0)
+MX_VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (0, 1, 2, 3)] +
+               [("normal", bn, s) for bn in (128, 256) for s in (0, 1, 2, 3)])
 
 
-@pytest.mark.parametrize("bn,split", MX_VARIANTS)
+@pytest.mark.parametrize("kind,bn,split", MX_VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(1, 128, 512), (5, 320, 1024), (77, 256, 2048),
-                                   (130, 384, 1536)])
-def test_mx_variants_small(fp8bq, bn, split, M, N, K):
+                                   (130, 384, 1536), (300, 640, 1024)])
+def test_mx_variants_small(fp8bq, kind, bn, split, M, N, K):
     xb, qa, sa, qw, sw = quantised_problem(M, N, K, True, synth.act_decode)
     ref = oracle_full(qa, sa, qw, sw, True)
     d = upload(qa, sa, qw, sw)
-    v = fp8bq.make_variant("swap", bn, split, 0, 1)
+    v = fp8bq.make_variant(kind, bn, split, 0, 1)
     for out in ("bf16", "fp32"):
         o = fp8bq.fp8bq_gemm_variant(*d, v, fmt="ue8m0", out_dtype=TORCH_OUT[out])
         torch.cuda.synchronize()
-        check_gemm(o.float().cpu().numpy(), ref, out, f"mx swap/{bn}/{split} {M}x{N}x{K} {out}")
+        check_gemm(o.float().cpu().numpy(), ref, out, f"mx {kind}/{bn}/{split} {M}x{N}x{K} {out}")
 
 
 @pytest.mark.parametrize("split,grid", [(7, 0), (0, 0), (0, 13), (1, 5)])
@@ -88,12 +89,11 @@ def test_mx_bit_stable_and_persistent(fp8bq, split, grid):
 def test_mx_rejections(fp8bq):
     for (K, ue, kind) in ((512, False, "swap"),    # fp32 scales
                           (640, True, "swap"),     # K not a multiple of 512
-                          (512, True, "normal")):  # swap-AB tiles only
+                          (512, True, "swap64")):  # M = 128 MMAs only
         xb, qa, sa, qw, sw = quantised_problem(16, 256, K, ue, synth.act_decode)
         d = upload(qa, sa, qw, sw)
         with pytest.raises(fp8bq.Fp8bqError) as e:
-            fp8bq.fp8bq_gemm_variant(*d, fp8bq.make_variant(kind, 128 if kind == "normal" else 16,
-                                                            1, 0, 1),
+            fp8bq.fp8bq_gemm_variant(*d, fp8bq.make_variant(kind, 16, 1, 0, 1),
                                      fmt="ue8m0" if ue else "fp32", out_dtype=torch.float32)
         assert e.value.status == 4
 
