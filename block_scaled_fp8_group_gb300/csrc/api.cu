@@ -181,8 +181,10 @@ void load_table_locked(const std::string& device_name) {
 // normal orientation with 256-wide weight tiles.  When the tiles cannot keep
 // every SM busy for whole waves, the (tile, K-slab) units are shared out
 // evenly (stream-K, split = 0); the tile count must fit the workspace's
-// counter prefix for that.
-fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
+// counter prefix for that.  With UE8M0 scales and whole groups of four K
+// slabs, the tensor core applies the scales (block-scaled MMA) on 128-wide and
+// wider tiles, where it measured faster on GB300.
+fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int fmt, int num_sms) {
     fp8bq_variant v = {};
     int64_t tiles;
     if (M <= 128) {
@@ -198,6 +200,10 @@ fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
     const bool whole_waves = tiles % num_sms == 0 || tiles >= 4 * static_cast<int64_t>(num_sms);
     v.split = (!whole_waves && fits_counters) ? 0 : 1;
     v.grid = 0;
+    v.mma_scale = (fmt == FP8BQ_SCALE_UE8M0 && K % (4 * kGroup) == 0 &&
+                   (v.kind == FP8BQ_KIND_NORMAL || v.block_n >= 64))
+                      ? 1
+                      : 0;
     v.from_table = 0;
     return v;
 }
@@ -229,7 +235,7 @@ fp8bq_variant select_variant(int64_t M, int64_t N, int64_t K, int fmt, int out,
                          static_cast<long long>(N), static_cast<long long>(K), fmt, out,
                          g_table.path.empty() ? "<none>" : g_table.path.c_str());
     }
-    return default_variant(M, N, K, num_sms);
+    return default_variant(M, N, K, fmt, num_sms);
 }
 
 // ------------------------------------------------------- argument checks

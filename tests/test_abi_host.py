@@ -140,7 +140,13 @@ def test_table_miss_uses_default(fake_table):
     v = fp8bq.fp8bq_select_variant(8, 7168, 18432, "ue8m0", "bf16")
     assert v["from_table"] is False and v["kind"] == "swap" and v["block_n"] == 16
     v = fp8bq.fp8bq_select_variant(4096, 24576, 7168, "fp32", "bf16")
-    assert v["from_table"] is False and v["kind"] == "normal"
+    assert v["from_table"] is False and v["kind"] == "normal" and v["mma_scale"] == 0
+    # UE8M0 with whole 4-slab groups: the tensor core applies the scales on
+    # wide tiles, not on 16/32-token decode tiles or when K % 512 != 0
+    assert fp8bq.fp8bq_select_variant(4096, 24576, 7168, "ue8m0", "bf16")["mma_scale"] == 1
+    assert fp8bq.fp8bq_select_variant(128, 24576, 7168, "ue8m0", "bf16")["mma_scale"] == 1
+    assert fp8bq.fp8bq_select_variant(8, 24576, 7168, "ue8m0", "bf16")["mma_scale"] == 0
+    assert fp8bq.fp8bq_select_variant(4096, 24576, 7296, "ue8m0", "bf16")["mma_scale"] == 0
     # other fmt/out of a tabulated (N,K) also misses
     assert fp8bq.fp8bq_select_variant(1, 4096, 7168, "fp32", "bf16")["from_table"] is False
 
