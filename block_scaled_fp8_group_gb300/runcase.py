@@ -2,7 +2,7 @@
 command the profiler captures.
 
     python -m block_scaled_fp8_group_gb300.runcase --m 8 --n 18432 --k 7168 \
-        --fmt ue8m0 --iters 3 [--variant swap/16/0] [--op gemm|linear|quant]
+        --fmt ue8m0 --iters 3 [--variant swap/16/0[/grid/mma_scale]] [--op gemm|linear|quant]
 
 Inputs are the decode-sweep distributions from ``synth`` (bf16 N(0,1) with 1%
 outlier channels, bf16 N(0,0.02) weights), quantised on the GPU.
@@ -25,7 +25,8 @@ def main():
     ap.add_argument("--fmt", default="ue8m0", choices=("fp32", "ue8m0"))
     ap.add_argument("--out", default="bf16", choices=("bf16", "fp16", "fp32"))
     ap.add_argument("--op", default="gemm", choices=("gemm", "linear", "quant"))
-    ap.add_argument("--variant", default=None, help="kind/block_n/split[/grid]")
+    ap.add_argument("--variant", default=None,
+                    help="kind/block_n/split[/grid[/mma_scale]] (default: the table's)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     dev = torch.device("cuda")
@@ -45,7 +46,8 @@ def main():
     if args.variant:
         parts = args.variant.split("/")
         v = fp8bq.make_variant(parts[0], int(parts[1]), int(parts[2]),
-                               int(parts[3]) if len(parts) > 3 else 0)
+                               int(parts[3]) if len(parts) > 3 else 0,
+                               int(parts[4]) if len(parts) > 4 else 0)
     for _ in range(args.iters):
         if args.op == "linear":
             fp8bq.fp8bq_linear(x, wq, ws, fmt=args.fmt, out_dtype=out_dt)
