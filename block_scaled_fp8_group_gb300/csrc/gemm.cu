@@ -1093,6 +1093,32 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                 }
             }
         };
+        // stores 16 columns [c0, c0 + 16) of this row (the split reduction's unit)
+        auto store_rc = [&](const TileOrigin& o, int c0, const float* v) {
+            if constexpr (SWAP) {
+                const int n = o.w0 + row;
+                if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = o.tok0 + c0 + j;
+                        if (t < a.M)
+                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, v[j]);
+                    }
+                }
+            } else {
+                const int m = o.tok0 + row;
+                if (m < a.M) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 8) {
+                        const int n0 = o.w0 + c0 + j;
+                        if (n0 < a.N)
+                            store_out8(a.out, a.out_dtype, static_cast<int64_t>(m) * a.N + n0, v[j],
+                                       v[j + 1], v[j + 2], v[j + 3], v[j + 4], v[j + 5], v[j + 6],
+                                       v[j + 7]);
+                    }
+                }
+            }
+        };
         while (ok && wi.next(a, sg)) {
             const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
             if (!warp_wait(&tfull[acc], aphase, abort_flag, a.status, tmo, code)) {
@@ -1145,19 +1171,54 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
             prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
             if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
             __threadfence();
+            if constexpr (BN <= 32) {
+                // narrow tiles split many ways: 16 columns at a time, the loads
+                // of PB parts go out before the first add (one L2 round trip
+                // per PB parts); the sum runs in K order
+                constexpr int RC = 16;
+                constexpr int PB = 4;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += RC) {
+                    float r[RC];
+                    for (int p0 = 0; p0 < sg.nparts; p0 += PB) {
+                        float t[PB][RC];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                float r[C::CHUNK];
-                for (int p = 0; p < sg.nparts; ++p) {
-                    const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
-                                       (c * C::CHUNK) * BM + row;
-                    float t[C::CHUNK];
+                        for (int q = 0; q < PB; ++q) {
+                            if (p0 + q < sg.nparts) {
+                                const float* src = a.partials +
+                                                   part_slot(a, sg.tile, p0 + q) * TILE + c0 * BM +
+                                                   row;
 #pragma unroll
-                    for (int j = 0; j < C::CHUNK; ++j) t[j] = __ldcg(src + j * BM);
+                                for (int j = 0; j < RC; ++j) t[q][j] = __ldcg(src + j * BM);
+                            }
+                        }
 #pragma unroll
-                    for (int j = 0; j < C::CHUNK; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
+                        for (int q = 0; q < PB; ++q) {
+                            if (p0 + q < sg.nparts) {
+#pragma unroll
+                                for (int j = 0; j < RC; ++j)
+                                    r[j] = (p0 + q == 0) ? t[q][j] : r[j] + t[q][j];
+                            }
+                        }
+                    }
+                    store_rc(o, c0, r);
                 }
-                store_chunk(o, c * C::CHUNK, r);
+            } else {
+                // wide tiles split at most a few ways: part by part, in K order
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    float r[C::CHUNK];
+                    for (int p = 0; p < sg.nparts; ++p) {
+                        const float* src = a.partials + part_slot(a, sg.tile, p) * TILE +
+                                           (c * C::CHUNK) * BM + row;
+                        float t[C::CHUNK];
+#pragma unroll
+                        for (int j = 0; j < C::CHUNK; ++j) t[j] = __ldcg(src + j * BM);
+#pragma unroll
+                        for (int j = 0; j < C::CHUNK; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
+                    }
+                    store_chunk(o, c * C::CHUNK, r);
+                }
             }
             if (lane == 0) *ctr = 0u;  // ready for the next call
         }
