@@ -291,7 +291,45 @@ fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, con
     g.status = d->status;
     g.timeout_ns = wait_timeout_ns();
     g.prefetch_w = prefetch_w;
+    g.x = nullptr;
+    g.x_fp16 = 0;
     return from_cuda(launch_gemm(plan, g, stream));
+}
+
+// The linear path's fused variant: the block-scaled GEMM quantises its own
+// activation tiles from x (one launch instead of quant + GEMM).
+fp8bq_status run_linear_fused(const GemmPlan& plan, int64_t M, int64_t N, int64_t K,
+                              const void* x, int x_fp16, const void* w_q, const float* w_s,
+                              int out_dtype, void* out, void* ws, DeviceInfo* d,
+                              cudaStream_t stream) {
+    GemmLaunch g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.a_q = nullptr;
+    g.a_s = nullptr;
+    g.w_q = w_q;
+    g.w_s = w_s;
+    g.ue8m0 = 1;
+    g.out_dtype = out_dtype;
+    g.out = out;
+    g.workspace = ws;
+    g.ws_data_offset = 0;
+    g.status = d->status;
+    g.timeout_ns = wait_timeout_ns();
+    g.prefetch_w = 1;
+    g.x = x;
+    g.x_fp16 = x_fp16;
+    return from_cuda(launch_gemm(plan, g, stream));
+}
+
+// FP8BQ_LINEAR_FUSE=1 turns the fused linear variant on.  It is off by
+// default: on GB300 it measured slower than quant + GEMM at every decode
+// shape (each 4-slab factor group waits for all four slabs' quantisation, so
+// the weight stream loses pipeline depth).  Both give the same bits.
+bool linear_fuse_enabled() {
+    const char* e = std::getenv("FP8BQ_LINEAR_FUSE");
+    return e && e[0] == '1';
 }
 
 }  // namespace
@@ -508,6 +546,19 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
     uint8_t* base = static_cast<uint8_t*>(workspace);
     void* a_q = base + kCounterRegion;
     void* a_s = base + kCounterRegion + q_bytes;
+
+    // UE8M0 with a swap-AB tile of 16/32 tokens: one block-scaled launch that
+    // quantises its own activation tiles (same codes, scales and sums as the
+    // two-launch path: bit-identical output to quant + block-scaled GEMM).
+    if (fmt == FP8BQ_SCALE_UE8M0 && v.kind == FP8BQ_KIND_SWAP_AB && v.block_n <= 32 &&
+        linear_fuse_enabled()) {
+        fp8bq_variant fv = v;
+        fv.mma_scale = 1;
+        GemmPlan fplan;
+        if (!make_gemm_plan(M, N, K, fv, d->num_sms, &fplan)) return FP8BQ_ERR_UNSUPPORTED;
+        return run_linear_fused(fplan, M, N, K, x, x_dtype == FP8BQ_FP16, w_q, w_s, out_dtype,
+                                out, base, d, stream);
+    }
 
     QuantActArgs qa;
     qa.x = x;

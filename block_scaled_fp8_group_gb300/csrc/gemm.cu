@@ -48,6 +48,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8bq {
 
@@ -123,6 +124,7 @@ struct KArgs {
     int ue8m0;
     int out_dtype;
     int prefetch_w;  // weights may be read before the previous grid finishes
+    const float* w_s;  // weight scales [NB][G] (read directly by the fused-quant path)
     void* out;
     float* partials;
     unsigned* counters;
@@ -729,12 +731,27 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
 //
 // Requires K % 512 == 0 (whole groups of four slabs, so the four weight
 // scales of a group are one aligned 16-byte chunk).
-template <bool SWAP, int BN>
+//
+// FQ (fused quant; fp8bq_linear, UE8M0, swap-AB token tiles of 16/32): the
+// operand tile of the tokens is quantised inside the kernel.  Warp 0 streams
+// the raw bf16/fp16 activation tile of each slab beside the weight tile.
+// Warps 2-5 each take a quarter of the token rows: group amax and E8M0 scale
+// with the standalone quant's arithmetic (quant_math.cuh), the e4m3 codes into
+// the 128-byte-swizzled operand tile, the exponents into a per-stage array.
+// Warps 6-9 (idle until a segment ends) gather each 4-slab group's exponents
+// into the same factor words as the unfused path (byte kb % 4) and write the
+// group's TMEM ring entry, each into its own lane quarter.  K % 128 suffices:
+// a group cut by a segment boundary is written when the segment ends.
+template <bool SWAP, int BN, int FQ = 0>
 struct MxCfg {
+    static_assert(FQ == 0 || (SWAP && BN <= 32), "fused quant: swap-AB token tiles of 16/32");
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = Cfg<SWAP, BN>::STAGES;
+    static constexpr int X_BYTES = FQ ? BN * BK * 2 : 0;  // raw activation tile (fused quant)
+    static constexpr int E_BYTES = FQ ? BN * 4 : 0;       // the tile rows' scale exponents
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + X_BYTES + E_BYTES;
+    static constexpr int STAGES = FQ ? (BN <= 16 ? 9 : 7) : Cfg<SWAP, BN>::STAGES;
+    static constexpr int SRM = FQ ? 0 : SR;  // scale-ring slots (the fused path has none)
     static constexpr int NC = (BN + 31) / 32;       // factor columns of the MMA-N operand
     static constexpr int TOK_WORDS = SWAP ? BN : BM;  // token factor words per group
     static constexpr int WBLK = SWAP ? 1 : BN / BK;   // weight blocks per tile
@@ -758,8 +775,8 @@ struct MxCfg {
     static constexpr int THREADS = 32 * 10;
     static constexpr int CHUNK = BN >= 32 ? 32 : 16;  // accumulator columns per TMEM load
     static constexpr int RING_OFF = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = RING_OFF + SR * SLOT_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * SR + 2 * RF + 2 * NACC + 1) + 16;
+    static constexpr int BAR_OFF = RING_OFF + SRM * SLOT_BYTES;
+    static constexpr int BAR_BYTES = 8 * (4 * STAGES + 2 * SRM + 2 * RF + 2 * NACC + 1) + 16;
     static constexpr int SMEM = 1024 + BAR_OFF + BAR_BYTES;
     static_assert(TMEM_NEED <= 512, "TMEM columns");
     static_assert(SF_BASE % 16 == 0 && NC <= SF_COLS - SF_B, "factor-ring column alignment");
@@ -768,19 +785,23 @@ struct MxCfg {
                   "scale slot layout");
 };
 
-template <bool SWAP, int BN>
-__global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
+template <bool SWAP, int BN, int FQ>
+__global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                    const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
+                                                                  // (FQ: raw activations, 2-byte)
                    const __grid_constant__ CUtensorMap tm_sa,     // packed act words [G/4][Mp]
                    const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                    const KArgs a) {
-    using C = MxCfg<SWAP, BN>;
+    using C = MxCfg<SWAP, BN, FQ>;
+    constexpr int SR = C::SRM;  // scale-ring slots of this configuration
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;                           // STAGES x [128 MMA-M rows x 128 B]
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN MMA-N rows x 128 B]
+    uint8_t* sX = sB + C::STAGES * C::B_BYTES;    // FQ: STAGES x [BN tokens x 256 B raw]
+    uint32_t* sE = reinterpret_cast<uint32_t*>(sX + C::STAGES * C::X_BYTES);  // FQ: STAGES x BN
     uint8_t* ring = smem + C::RING_OFF;           // SR x SLOT_BYTES
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + C::STAGES;
@@ -791,7 +812,9 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
     uint64_t* tfull = fempty + C::RF;     // accumulator complete
     uint64_t* tempty = tfull + C::NACC;   // accumulator read out
     uint64_t* mma_done = tempty + C::NACC;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* xfull = mma_done + 1;       // FQ: raw activation tile landed
+    uint64_t* qdone = xfull + C::STAGES;  // FQ: the stage's codes and exponents written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qdone + C::STAGES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -799,8 +822,11 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // FQ: the weight tile's bytes plus the four quantising warps' codes
+            mbar_init(&full[s], FQ ? 5 : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&xfull[s], 1);
+            mbar_init(&qdone[s], 4);
         }
         for (int s = 0; s < SR; ++s) {
             mbar_init(&sfull[s], 1);
@@ -846,7 +872,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
             const int nslab = sg.kb1 - sg.kb0;
             prefetched = nslab < C::STAGES ? nslab : C::STAGES;
             for (int i = 0; i < prefetched; ++i) {
-                mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+                mbar_arrive_expect_tx(&full[i], FQ ? C::A_BYTES : C::STAGE_BYTES);
                 if (SWAP)
                     tma_load_2d_hint(sA + i * C::A_BYTES, &tm_mma_m, &full[i], (sg.kb0 + i) * BK,
                                      o.w0, policy_evict_first());
@@ -878,7 +904,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (kb == sg.kb0 || (kb & 3) == 0) {
+                    if (!FQ && (kb == sg.kb0 || (kb & 3) == 0)) {
                         // the group's factors: BN token words, four weight scales
                         if (!mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag, a.status,
                                                tmo, code)) {
@@ -898,7 +924,22 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                             sphase ^= 1u;
                         }
                     }
-                    if (fills < prefetched) {
+                    if (FQ) {
+                        // weight tile to the operand stage, raw activations to sX
+                        if (fills >= prefetched) {
+                            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag,
+                                                   a.status, tmo, code)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&full[stage], C::A_BYTES);
+                            tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
+                                             kb * BK, row_m, pol_m);
+                        }
+                        mbar_arrive_expect_tx(&xfull[stage], C::X_BYTES);
+                        tma_load_2d_hint(sX + stage * C::X_BYTES, &tm_mma_n, &xfull[stage],
+                                         kb * BK, row_n, pol_n);
+                    } else if (fills < prefetched) {
                         // the weight tile of this stage is already on its way
                         if (SWAP)
                             tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
@@ -925,11 +966,17 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                     }
                 }
             }
-            for (long long f = fills > C::STAGES ? fills - C::STAGES : 0; f < fills; ++f)
+            for (long long f = fills > C::STAGES ? fills - C::STAGES : 0; f < fills; ++f) {
+                if (FQ)
+                    mbar_wait_drain(&xfull[f % C::STAGES],
+                                    static_cast<uint32_t>((f / C::STAGES) & 1), tmo);
                 mbar_wait_drain(&full[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1),
                                 tmo);
-            for (long long f = sfills > SR ? sfills - SR : 0; f < sfills; ++f)
-                mbar_wait_drain(&sfull[f % SR], static_cast<uint32_t>((f / SR) & 1), tmo);
+            }
+            if constexpr (SR > 0) {
+                for (long long f = sfills > SR ? sfills - SR : 0; f < sfills; ++f)
+                    mbar_wait_drain(&sfull[f % SR], static_cast<uint32_t>((f / SR) & 1), tmo);
+            }
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -970,6 +1017,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                     const uint32_t a_addr = smem_addr(sA + stage * C::A_BYTES);
                     const uint32_t b_addr = smem_addr(sB + stage * C::B_BYTES);
                     const uint32_t sfa = tmem_base + static_cast<uint32_t>(C::SF_BASE + cur * C::SF_COLS);
+                    // factor byte kb % 4 of the group's words
                     const uint32_t idesc = idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(kb & 3));
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk)
@@ -994,65 +1042,134 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
             mbar_wait_drain(mma_done, 0, tmo);
         }
     } else if (warp < C::EPI_FIRST) {
-        // -------------------------------------------------- factor writers
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const uint32_t t_quarter = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        int slot = 0, r = 0;
-        uint32_t sphase = 0, rphase = 0;
-        WorkIter wi;
-        wi.init(a);
-        Seg sg;
-        bool ok = true;
-        while (ok && wi.next(a, sg)) {
-            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                if (kb != sg.kb0 && (kb & 3) != 0) continue;
-                if (!warp_wait(&sfull[slot], sphase, abort_flag, a.status, tmo, code) ||
-                    !warp_wait(&fempty[r], rphase ^ 1u, abort_flag, a.status, tmo, code)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint8_t* sl = ring + slot * SLOT_BYTES;
-                // weight words: byte j = E8M0 exponent of the block's scale of
-                // slab 4*(kb/4)+j (the fp32 scales are powers of two)
-                uint32_t ww[C::WBLK];
-#pragma unroll
-                for (int b = 0; b < C::WBLK; ++b) {
-                    const float* swc = reinterpret_cast<const float*>(sl + SLOT_SW + b * SLOT_SW_STEP);
-                    ww[b] = 0;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        ww[b] |= ((__float_as_uint(swc[j]) >> 23) & 0xFFu) << (8 * j);
-                }
-                const uint32_t* tw = reinterpret_cast<const uint32_t*>(sl);
-                const uint32_t col = static_cast<uint32_t>(C::SF_BASE + r * C::SF_COLS);
-                if constexpr (SWAP) {
-                    tmem_st4(t_quarter + col, ww[0], ww[0], ww[0], ww[0]);
-#pragma unroll
-                    for (int c = 0; c < C::NC; ++c) {
-                        const int t = 32 * c + lane;
-                        tmem_st1(t_quarter + col + C::SF_B + c, t < BN ? tw[t] : 0u);
+        if constexpr (FQ) {
+            // ----------------------------------------- quantising warps (FQ)
+            // Per slab: the BN x 128 raw tile in sX (row-major, 256 B a row).
+            // Warp q takes rows [q*BN/4, (q+1)*BN/4): pass p covers 4 of them,
+            // 8 lanes a row, 16 elements a lane.
+            constexpr int RPW = BN / 4;      // rows per warp
+            constexpr int PASSES = RPW / 4;  // 1 (16 tokens) or 2 (32 tokens)
+            const int g = lane >> 3;         // row within the pass
+            const int c16 = lane & 7;        // 16-element chunk within the row
+            int stage = 0;
+            uint32_t phase = 0;
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (!warp_wait(&xfull[stage], phase, abort_flag, a.status, tmo, code)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    tmem_st4(t_quarter + col, tw[lane], tw[32 + lane], tw[64 + lane], tw[96 + lane]);
+                    const uint8_t* xs = sX + stage * C::X_BYTES;
+                    uint8_t* bs = sB + stage * C::B_BYTES;
+                    uint32_t* es = sE + stage * BN;
 #pragma unroll
-                    for (int b = 0; b < C::WBLK; ++b)
-                        tmem_st4(t_quarter + col + C::SF_B + 4 * b, ww[b], ww[b], ww[b], ww[b]);
+                    for (int p = 0; p < PASSES; ++p) {
+                        const int row = quarter * RPW + 4 * p + g;
+                        const uint4* src = reinterpret_cast<const uint4*>(xs + row * (2 * BK) + c16 * 32);
+                        const uint4 v0 = src[0], v1 = src[1];
+                        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                        float f[16];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            f[2 * i] = FQ == 2 ? f16_lo(w[i]) : bf16_lo(w[i]);
+                            f[2 * i + 1] = FQ == 2 ? f16_hi(w[i]) : bf16_hi(w[i]);
+                        }
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                        const float sc = group_scale(amax, 1);
+                        // sc = 2^e exactly: x * (1/sc) is the correctly rounded x / sc
+                        const float rs = __fdiv_rn(1.0f, sc);
+                        uint32_t cw[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) cw[i] = cvt2_e4m3(f[2 * i] * rs, f[2 * i + 1] * rs);
+                        // 128-byte swizzle: chunk c of row r at chunk c ^ (r % 8)
+                        *reinterpret_cast<uint4*>(bs + row * BK + ((c16 ^ (row & 7)) << 4)) =
+                            make_uint4(cw[0] | (cw[1] << 16), cw[2] | (cw[3] << 16),
+                                       cw[4] | (cw[5] << 16), cw[6] | (cw[7] << 16));
+                        if (c16 == 0) es[row] = (__float_as_uint(sc) >> 23) & 0xFFu;
+                    }
+                    // the codes are read by the tensor core (async proxy)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&full[stage]);
+                        mbar_arrive(&qdone[stage]);
+                    }
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&ffull[r]);
-                    mbar_arrive(&sempty[slot]);
-                }
-                if (++slot == SR) {
-                    slot = 0;
-                    sphase ^= 1u;
-                }
-                if (++r == C::RF) {
-                    r = 0;
-                    rphase ^= 1u;
+            }
+        } else {
+            // -------------------------------------------------- factor writers
+            int slot = 0, r = 0;
+            uint32_t sphase = 0, rphase = 0;
+            WorkIter wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (kb != sg.kb0 && (kb & 3) != 0) continue;
+                    if (!warp_wait(&sfull[slot], sphase, abort_flag, a.status, tmo, code) ||
+                        !warp_wait(&fempty[r], rphase ^ 1u, abort_flag, a.status, tmo, code)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* sl = ring + slot * SLOT_BYTES;
+                    // weight words: byte j = E8M0 exponent of the block's scale of
+                    // slab 4*(kb/4)+j (the fp32 scales are powers of two)
+                    uint32_t ww[C::WBLK];
+    #pragma unroll
+                    for (int b = 0; b < C::WBLK; ++b) {
+                        const float* swc = reinterpret_cast<const float*>(sl + SLOT_SW + b * SLOT_SW_STEP);
+                        ww[b] = 0;
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            ww[b] |= ((__float_as_uint(swc[j]) >> 23) & 0xFFu) << (8 * j);
+                    }
+                    const uint32_t* tw = reinterpret_cast<const uint32_t*>(sl);
+                    const uint32_t col = static_cast<uint32_t>(C::SF_BASE + r * C::SF_COLS);
+                    if constexpr (SWAP) {
+                        tmem_st4(t_quarter + col, ww[0], ww[0], ww[0], ww[0]);
+    #pragma unroll
+                        for (int c = 0; c < C::NC; ++c) {
+                            const int t = 32 * c + lane;
+                            tmem_st1(t_quarter + col + C::SF_B + c, t < BN ? tw[t] : 0u);
+                        }
+                    } else {
+                        tmem_st4(t_quarter + col, tw[lane], tw[32 + lane], tw[64 + lane], tw[96 + lane]);
+    #pragma unroll
+                        for (int b = 0; b < C::WBLK; ++b)
+                            tmem_st4(t_quarter + col + C::SF_B + 4 * b, ww[b], ww[b], ww[b], ww[b]);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&ffull[r]);
+                        mbar_arrive(&sempty[slot]);
+                    }
+                    if (++slot == SR) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
+                    if (++r == C::RF) {
+                        r = 0;
+                        rphase ^= 1u;
+                    }
                 }
             }
         }
@@ -1119,8 +1236,62 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN>::THREADS, 1)
                 }
             }
         };
+        // FQ: the factor ring, written here slab by slab
+        int fstage = 0, fr = 0;
+        uint32_t fphase = 0, frphase = 0;
         while (ok && wi.next(a, sg)) {
             const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            if constexpr (FQ > 0) {
+                // per 4-slab group (as the packed words of the unfused path):
+                // byte j of the weight word = the block's exponent of slab
+                // 4w+j, byte j of token t's word = its exponent in that slab
+                const uint32_t t_quarter = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+                const float* wrow = a.w_s + static_cast<int64_t>(o.w0 / BK) * a.G;
+                auto wload = [&](int kb) { return kb < sg.kb1 ? __ldg(wrow + kb) : 0.0f; };
+                float w_cur = wload(sg.kb0 + lane);
+                float w_nxt = wload(sg.kb0 + 32 + lane);
+                uint32_t ww = 0, tw = 0;
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    const int wi32 = (kb - sg.kb0) & 31;
+                    if (wi32 == 0 && kb != sg.kb0) {
+                        w_cur = w_nxt;
+                        w_nxt = wload(kb + 32 + lane);
+                    }
+                    if (!warp_wait(&qdone[fstage], fphase, abort_flag, a.status, tmo, code)) {
+                        ok = false;
+                        break;
+                    }
+                    const int byte = 8 * (kb & 3);
+                    ww |= ((__float_as_uint(__shfl_sync(0xFFFFFFFFu, w_cur, wi32)) >> 23) & 0xFFu)
+                          << byte;
+                    if (lane < BN) tw |= sE[fstage * BN + lane] << byte;
+                    if (++fstage == C::STAGES) {
+                        fstage = 0;
+                        fphase ^= 1u;
+                    }
+                    if ((kb & 3) != 3 && kb != sg.kb1 - 1) continue;
+                    // the group is complete: write its ring entry
+                    if (!warp_wait(&fempty[fr], frphase ^ 1u, abort_flag, a.status, tmo, code)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t col = static_cast<uint32_t>(C::SF_BASE + fr * C::SF_COLS);
+                    tmem_st4(t_quarter + col, ww, ww, ww, ww);
+                    tmem_st1(t_quarter + col + C::SF_B, tw);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ffull[fr]);
+                    ww = 0;
+                    tw = 0;
+                    if (++fr == C::RF) {
+                        fr = 0;
+                        frphase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
             if (!warp_wait(&tfull[acc], aphase, abort_flag, a.status, tmo, code)) {
                 ok = false;
                 break;
@@ -1285,10 +1456,20 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     if constexpr (WM == BM) {
         static int mx_attr_done[64] = {0};
         if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
-            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN>,
+            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MxCfg<SWAP, BN>::SMEM);
+                                       MxCfg<SWAP, BN, 0>::SMEM);
             if (err != cudaSuccess) return err;
+            if constexpr (SWAP && BN <= 32) {
+                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 1>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           MxCfg<SWAP, BN, 1>::SMEM);
+                if (err != cudaSuccess) return err;
+                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 2>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           MxCfg<SWAP, BN, 2>::SMEM);
+                if (err != cudaSuccess) return err;
+            }
             mx_attr_done[dev] = 1;
         }
     }
@@ -1300,8 +1481,18 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     CUtensorMap tm_m, tm_n, tm_sa, tm_sw;
     bool ok;
     if (swap) {
-        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), WM) &&
-             encode_operand(&tm_n, g.a_q, K, static_cast<uint64_t>(g.M), BN);
+        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), WM);
+        if (g.x) {
+            // fused quant: raw 2-byte activations [M, K], boxes of BN rows x 128
+            // elements (256 bytes, unswizzled), rows past M read as zero
+            const cuuint64_t dims[2] = {K, static_cast<cuuint64_t>(g.M)};
+            const cuuint64_t strides[1] = {K * 2};
+            const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(BN)};
+            ok = ok && encode(&tm_n, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.x, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+        } else {
+            ok = ok && encode_operand(&tm_n, g.a_q, K, static_cast<uint64_t>(g.M), BN);
+        }
     } else {
         ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
              encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(g.N), BN);
@@ -1311,9 +1502,12 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         const cuuint64_t dims[2] = {Mp, static_cast<cuuint64_t>(g.ue8m0 ? (G + 3) / 4 : G)};
         const cuuint64_t strides[1] = {Mp * 4};
         const cuuint32_t box[2] = {static_cast<cuuint32_t>(swap ? BN : BM), 1};
-        ok = ok && encode(&tm_sa, g.ue8m0 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
-                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          2, g.a_s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (g.x)
+            tm_sa = tm_n;  // fused quant: the kernel computes the scales itself
+        else
+            ok = ok && encode(&tm_sa, g.ue8m0 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              2, g.a_s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
         // weight scales: the flat [NB*G] fp32 array as one row, 16-byte boxes
         const cuuint64_t flat = static_cast<cuuint64_t>(NB) * G;
         const cuuint64_t wdims[2] = {flat, 1};
@@ -1341,6 +1535,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     a.ue8m0 = g.ue8m0;
     a.out_dtype = g.out_dtype;
     a.prefetch_w = g.prefetch_w;
+    a.w_s = g.w_s;
     a.out = g.out;
     // workspace: [tile counters: fixed kCounterRegion prefix] [fp32 partial tiles]
     a.counters = p.ws_bytes ? static_cast<unsigned*>(g.workspace) : nullptr;
@@ -1362,9 +1557,24 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cfg.numAttrs = 1;
     if constexpr (WM == BM) {
         if (p.mx) {
-            cfg.blockDim = dim3(MxCfg<SWAP, BN>::THREADS);
-            cfg.dynamicSmemBytes = MxCfg<SWAP, BN>::SMEM;
-            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN>, tm_m, tm_n, tm_sa, tm_sw, a);
+            if constexpr (SWAP && BN <= 32) {
+                if (g.x) {
+                    if (g.x_fp16) {
+                        cfg.blockDim = dim3(MxCfg<SWAP, BN, 2>::THREADS);
+                        cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 2>::SMEM;
+                        return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 2>, tm_m, tm_n,
+                                                  tm_n, tm_n, a);
+                    }
+                    cfg.blockDim = dim3(MxCfg<SWAP, BN, 1>::THREADS);
+                    cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 1>::SMEM;
+                    return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 1>, tm_m, tm_n, tm_n,
+                                              tm_n, a);
+                }
+            }
+            cfg.blockDim = dim3(MxCfg<SWAP, BN, 0>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0>, tm_m, tm_n, tm_sa, tm_sw,
+                                      a);
         }
     }
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM>, tm_m, tm_n, tm_sa, tm_sw, a);

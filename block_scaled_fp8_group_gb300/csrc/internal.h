@@ -81,9 +81,12 @@ struct GemmLaunch {
     int* status;
     uint64_t timeout_ns;
     // Weights may be read before the previous kernel in the stream has
-    // finished: only when that kernel cannot have written them (the fused
-    // linear path, where it is this library's activation quant).
+    // finished (the linear path; see fp8bq_linear's contract).
     int prefetch_w;
+    // Fused quant (linear path, UE8M0, swap-AB token tiles of 16/32): raw
+    // bf16/fp16 activations [M, K] instead of a_q / a_s.
+    const void* x;
+    int x_fp16;
 };
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmLaunch& g, cudaStream_t stream);
 

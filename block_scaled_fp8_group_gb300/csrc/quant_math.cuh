@@ -1,0 +1,48 @@
+// quant_math.cuh -- the per-group quantisation arithmetic, shared by the
+// standalone quant kernels (quant.cu) and the GEMM that quantises its own
+// activation tiles (gemm.cu), so both produce the same codes and scales.
+//
+// "vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.1: s = max(amax, eps) / fp8_max,
+// rounded up to a power of two for UE8M0; codes = e4m3 RNE of clamp(x/s, +-448).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace fp8bq {
+
+// Power-of-two round-up of a positive normal fp32 scale, on its bits.
+__device__ __forceinline__ float ceil_pow2(float s) {
+    uint32_t u = __float_as_uint(s);
+    uint32_t e = (u >> 23) & 0xFFu;
+    if (u & 0x7FFFFFu) e += 1u;
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ float group_scale(float amax, int ue8m0) {
+    float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+    return ue8m0 ? ceil_pow2(s) : s;
+}
+
+// Two fp32 values -> two e4m3 codes (low byte = first), saturating RNE.
+__device__ __forceinline__ uint32_t cvt2_e4m3(float a, float b) {
+    a = fminf(fmaxf(a, -kFp8Max), kFp8Max);
+    b = fminf(fmaxf(b, -kFp8Max), kFp8Max);
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                          __NV_E4M3));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+}  // namespace fp8bq

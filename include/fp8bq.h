@@ -178,7 +178,11 @@ fp8bq_status fp8bq_gemm_variant(int64_t M, int64_t N, int64_t K, const void* a_q
 
 /* Activation quant followed by the GEMM, one call, two launches on `stream`
  * (the whole W8A8 linear layer for a bf16/fp16 input x [M,K]).  The codes and
- * scales go to the front of `workspace`; see fp8bq_linear_workspace_bytes. */
+ * scales go to the front of `workspace`; see fp8bq_linear_workspace_bytes.
+ * With the environment variable FP8BQ_LINEAR_FUSE=1, UE8M0 problems whose
+ * selected variant is swap-AB with a 16/32-token tile run as one block-scaled
+ * launch that quantises its own activation tiles instead (bit-identical
+ * output; slower on GB300 at the shapes measured, hence off by default). */
 fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N, int64_t K,
                           const void* w_q, const float* w_s, int group, int block_n,
                           int block_k, fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,

@@ -223,6 +223,41 @@ def test_linear_full_grid(fp8bq, N, K, M):
         check_gemm(o.float().cpu().numpy()[rows], ref, out, f"linear {M}x{N}x{K} {out}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (5, 384, 1024), (16, 1024, 2048),
+                                   (24, 640, 1536), (32, 4096, 7168), (16, 18432, 7168)])
+@pytest.mark.parametrize("xdt", ["bf16", "fp16"])
+def test_linear_fused_quant(fp8bq, M, N, K, xdt, monkeypatch):
+    """UE8M0 with a swap-AB tile of 16/32 tokens and FP8BQ_LINEAR_FUSE=1:
+    fp8bq_linear runs one block-scaled launch that quantises its own
+    activation tiles.  Its output equals (bit for bit) the standalone quant
+    followed by the block-scaled GEMM of the same tile and split, and matches
+    the oracle; the default (unfused) path matches the oracle too."""
+    tdt = torch.bfloat16 if xdt == "bf16" else torch.float16
+    xb = synth.act_full_grid(M, K)
+    if xdt == "fp16":  # the same values as fp16 bit patterns
+        xb = synth.f32_to_f16_bits((xb.astype(np.uint32) << 16).view(np.float32))
+    wb = synth.weight_bf16(N, K)
+    x = to_dev_bits(xb, tdt)
+    wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
+    sel = fp8bq.fp8bq_select_variant(M, N, K, "ue8m0", "bf16")
+    if sel["kind"] != "swap" or sel["block_n"] > 32:
+        pytest.skip("the table picks a tile the fused path does not cover")
+    monkeypatch.setenv("FP8BQ_LINEAR_FUSE", "1")
+    fused = fp8bq.fp8bq_linear(x, wq, ws, fmt="ue8m0", out_dtype=torch.bfloat16)
+    monkeypatch.delenv("FP8BQ_LINEAR_FUSE")
+    aq, as_ = fp8bq.fp8bq_quant_act(x, "ue8m0")
+    v = fp8bq.make_variant("swap", sel["block_n"], sel["split"], sel["grid"], 1)
+    two = fp8bq.fp8bq_gemm_variant(aq, as_, wq, ws, v, fmt="ue8m0", out_dtype=torch.bfloat16)
+    unfused = fp8bq.fp8bq_linear(x, wq, ws, fmt="ue8m0", out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, two), "fused linear differs from quant + block-scaled GEMM"
+    qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+    qa, sa = oracle.quant_act(xb, oracle.BF16 if xdt == "bf16" else oracle.FP16, 128, True)
+    ref = oracle_full(qa, sa, qw, sw, True)
+    check_gemm(fused.float().cpu().numpy(), ref, "bf16", f"fused linear {M}x{N}x{K} {xdt}")
+    check_gemm(unfused.float().cpu().numpy(), ref, "bf16", f"unfused linear {M}x{N}x{K} {xdt}")
+
+
 def test_empty_and_errors(fp8bq):
     a = torch.zeros((0, 256), dtype=torch.uint8, device="cuda")
     s = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
