@@ -238,6 +238,39 @@ fp8bq_variant select_variant(int64_t M, int64_t N, int64_t K, int fmt, int out,
     return default_variant(M, N, K, fmt, num_sms);
 }
 
+// Grouped problems: the tile grid counts every expert as full (the counts
+// are on the device).  Token tile from the rows per expert as for a plain
+// problem; split-K only when the experts' tiles cannot fill the GPU.
+fp8bq_variant default_grouped_variant(int64_t E, int64_t M, int64_t N, int64_t K, int fmt,
+                                      int num_sms) {
+    fp8bq_variant v = {};
+    int64_t tiles;
+    if (M <= 128) {
+        v.kind = FP8BQ_KIND_SWAP_AB;
+        v.block_n = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        tiles = E * (N / 128) * ((M + v.block_n - 1) / v.block_n);
+    } else {
+        v.kind = FP8BQ_KIND_NORMAL;
+        v.block_n = N % 256 == 0 ? 256 : 128;
+        tiles = E * (N / v.block_n) * ((M + 127) / 128);
+    }
+    const int64_t G = K / kGroup;
+    int64_t split = 1;
+    if (tiles > 0 && tiles < num_sms && tiles * 8 * 4 <= static_cast<int64_t>(kCounterRegion)) {
+        split = (num_sms + tiles - 1) / tiles;
+        if (split > 8) split = 8;
+        if (split > G) split = G;
+    }
+    v.split = static_cast<int>(split);
+    v.grid = 0;
+    v.mma_scale = (fmt == FP8BQ_SCALE_UE8M0 && K % (4 * kGroup) == 0 &&
+                   (v.kind == FP8BQ_KIND_NORMAL || v.block_n >= 64))
+                      ? 1
+                      : 0;
+    v.from_table = 0;
+    return v;
+}
+
 // ------------------------------------------------------- argument checks
 
 constexpr int64_t kMaxDim = (1LL << 31) - 4096;
@@ -268,6 +301,19 @@ fp8bq_status check_ws(const GemmPlan& plan, const void* ws, size_t ws_bytes) {
     return FP8BQ_OK;
 }
 
+// Grouped problems: E >= 1 experts of M_max token rows (a multiple of 4, so
+// every expert's scale rows start on a 16-byte boundary), weights in whole
+// 128-row blocks per expert (N % 128 == 0).
+fp8bq_status check_grouped_args(int64_t E, int64_t M_max, int64_t N, int64_t K, int fmt,
+                                int out_dtype) {
+    if (E < 1 || E > (1 << 20) || M_max < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (M_max > kMaxDim / E || N > kMaxDim / E) return FP8BQ_ERR_SHAPE;
+    fp8bq_status st = check_gemm_args(E * M_max, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (M_max % 4 != 0 || N % kGroup != 0) return FP8BQ_ERR_SHAPE;
+    return FP8BQ_OK;
+}
+
 fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, const void* a_q,
                       const void* a_s, const void* w_q, const float* w_s, int fmt, int out_dtype,
                       void* out, void* ws, size_t ws_data_offset, DeviceInfo* d,
@@ -293,6 +339,36 @@ fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, con
     g.prefetch_w = prefetch_w;
     g.x = nullptr;
     g.x_fp16 = 0;
+    return from_cuda(launch_gemm(plan, g, stream));
+}
+
+fp8bq_status run_grouped_gemm(const GemmPlan& plan, int64_t E, int64_t M_max, int64_t N,
+                              int64_t K, const int32_t* counts, const void* a_q, const void* a_s,
+                              const void* w_q, const float* w_s, int fmt, int out_dtype,
+                              void* out, void* ws, DeviceInfo* d, cudaStream_t stream) {
+    if (plan.mx && (fmt != FP8BQ_SCALE_UE8M0 || K % (4 * kGroup) != 0))
+        return FP8BQ_ERR_UNSUPPORTED;
+    GemmLaunch g;
+    g.M = E * M_max;
+    g.N = N;
+    g.K = K;
+    g.a_q = a_q;
+    g.a_s = a_s;
+    g.w_q = w_q;
+    g.w_s = w_s;
+    g.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    g.out_dtype = out_dtype;
+    g.out = out;
+    g.workspace = ws;
+    g.ws_data_offset = 0;
+    g.status = d->status;
+    g.timeout_ns = wait_timeout_ns();
+    g.prefetch_w = 0;
+    g.x = nullptr;
+    g.x_fp16 = 0;
+    g.E = E;
+    g.m_max = M_max;
+    g.counts = counts;
     return from_cuda(launch_gemm(plan, g, stream));
 }
 
@@ -513,6 +589,78 @@ fp8bq_status fp8bq_gemm(int64_t M, int64_t N, int64_t K, const void* a_q, const 
     if (st != FP8BQ_OK) return st;
     return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, workspace, 0, d, 0,
                     stream);
+}
+
+// ------------------------------------------------------------ grouped GEMM
+
+size_t fp8bq_grouped_variant_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                             const fp8bq_variant* v) {
+    if (!v || check_grouped_args(E, M_max, N, K, FP8BQ_SCALE_FP32, FP8BQ_BF16) != FP8BQ_OK)
+        return 0;
+    if (M_max == 0 || N == 0) return 0;
+    GemmPlan plan;
+    if (!make_gemm_plan(M_max, N, K, *v, 152, &plan, E)) return 0;
+    return plan.ws_bytes;
+}
+
+fp8bq_status fp8bq_select_grouped_variant(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                          fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype,
+                                          fp8bq_variant* variant) {
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    fp8bq_status st = check_grouped_args(E, M_max, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    int sms = 152;  // GB300 when no GPU is visible (host-only queries)
+    if (device_info(&d) == FP8BQ_OK) sms = d->num_sms;
+    *variant = default_grouped_variant(E, M_max, N, K, fmt, sms);
+    return FP8BQ_OK;
+}
+
+size_t fp8bq_grouped_gemm_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                          fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype) {
+    fp8bq_variant v;
+    if (fp8bq_select_grouped_variant(E, M_max, N, K, fmt, out_dtype, &v) != FP8BQ_OK) return 0;
+    return fp8bq_grouped_variant_workspace_bytes(E, M_max, N, K, &v);
+}
+
+fp8bq_status fp8bq_grouped_gemm_variant(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                        const int32_t* counts, const void* a_q, const void* a_s,
+                                        const void* w_q, const float* w_s, fp8bq_scale_fmt fmt,
+                                        fp8bq_dtype out_dtype, void* out,
+                                        const fp8bq_variant* variant, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_grouped_args(E, M_max, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    if (M_max == 0 || N == 0) return FP8BQ_OK;
+    if (!counts) return FP8BQ_ERR_INVALID_ARG;
+    st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    GemmPlan plan;
+    if (!make_gemm_plan(M_max, N, K, *variant, d->num_sms, &plan, E)) return FP8BQ_ERR_UNSUPPORTED;
+    st = check_ws(plan, workspace, workspace_bytes);
+    if (st != FP8BQ_OK) return st;
+    return run_grouped_gemm(plan, E, M_max, N, K, counts, a_q, a_s, w_q, w_s, fmt, out_dtype, out,
+                            workspace, d, stream);
+}
+
+fp8bq_status fp8bq_grouped_gemm(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                const int32_t* counts, const void* a_q, const void* a_s,
+                                const void* w_q, const float* w_s, int group, int block_n,
+                                int block_k, fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_grouped_args(E, M_max, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (M_max == 0 || N == 0) return FP8BQ_OK;
+    fp8bq_variant v;
+    st = fp8bq_select_grouped_variant(E, M_max, N, K, fmt, out_dtype, &v);
+    if (st != FP8BQ_OK) return st;
+    return fp8bq_grouped_gemm_variant(E, M_max, N, K, counts, a_q, a_s, w_q, w_s, fmt, out_dtype,
+                                      out, &v, workspace, workspace_bytes, stream);
 }
 
 fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N, int64_t K,

@@ -130,6 +130,13 @@ struct KArgs {
     unsigned* counters;
     int* status;
     unsigned long long timeout_ns;
+    // grouped problem (E > 0): E stacked problems of m_max token rows each;
+    // M = E * m_max, N is one expert's width (and the output row length)
+    int E;
+    int m_max;
+    int tiles_e;        // tiles per expert (tiles_tok * weight tiles)
+    int tok_tile;       // tokens per tile (BN when swap, BM otherwise)
+    const int* counts;  // valid token rows of each expert (device)
 };
 
 // One contiguous run of K slabs of one tile.
@@ -146,6 +153,20 @@ __device__ __forceinline__ long long sk_begin(long long c, long long T, long lon
 }
 __device__ __forceinline__ int sk_owner(long long u, long long T, long long P) {
     return static_cast<int>(((u + 1) * P - 1) / T);
+}
+
+// Grouped problems: valid token rows of expert e (its count clamped to
+// [0, m_max]), and whether a tile holds none of them (such tiles are skipped
+// by every role alike).
+__device__ __forceinline__ int expert_rows(const KArgs& a, int e) {
+    const int c = __ldg(a.counts + e);
+    return c < 0 ? 0 : (c > a.m_max ? a.m_max : c);
+}
+__device__ __forceinline__ bool tile_empty(const KArgs& a, int tile) {
+    const int e = tile / a.tiles_e;
+    const int r = tile - e * a.tiles_e;
+    const int tt = r - (r / a.tiles_tok) * a.tiles_tok;
+    return tt * a.tok_tile >= expert_rows(a, e);
 }
 
 // Iterates this CTA's segments in order (identically in every role).
@@ -177,14 +198,17 @@ struct WorkIter {
             u += s.kb1 - s.kb0;
             return true;
         }
-        if (item >= a.num_items) return false;
-        s.tile = item / a.split;
-        s.part = item - s.tile * a.split;
-        s.nparts = a.split;
-        s.kb0 = static_cast<int>((static_cast<long long>(s.part) * a.G) / a.split);
-        s.kb1 = static_cast<int>((static_cast<long long>(s.part + 1) * a.G) / a.split);
-        item += gridDim.x;
-        return true;
+        for (;;) {
+            if (item >= a.num_items) return false;
+            s.tile = item / a.split;
+            s.part = item - s.tile * a.split;
+            item += gridDim.x;
+            if (a.E > 0 && tile_empty(a, s.tile)) continue;
+            s.nparts = a.split;
+            s.kb0 = static_cast<int>((static_cast<long long>(s.part) * a.G) / a.split);
+            s.kb1 = static_cast<int>((static_cast<long long>(s.part + 1) * a.G) / a.split);
+            return true;
+        }
     }
 };
 
@@ -200,21 +224,35 @@ __device__ __forceinline__ int64_t part_slot(const KArgs& a, int tile, int p) {
 }
 
 struct TileOrigin {
-    int tok0;  // first token
-    int w0;    // first weight row (n)
+    int tok0;     // first token (row of the stacked operand)
+    int w0;       // first weight row (row of the stacked weights)
+    int tok_end;  // tokens [tok0, tok_end) are stored
+    int w_end;    // weight rows [w0, w_end) are stored
+    int col0;     // output column of weight row n: n - col0
 };
 
 template <bool SWAP, int BN, int WM = BM>
 __device__ __forceinline__ TileOrigin tile_origin(const KArgs& a, int tile) {
+    int tok_base = 0, w_base = 0;
+    TileOrigin o;
+    o.tok_end = a.M;
+    if (a.E > 0) {
+        const int e = tile / a.tiles_e;
+        tile -= e * a.tiles_e;
+        tok_base = e * a.m_max;
+        w_base = e * a.N;
+        o.tok_end = tok_base + expert_rows(a, e);
+    }
+    o.w_end = w_base + a.N;
+    o.col0 = w_base;
     const int wt = tile / a.tiles_tok;       // weight tile (slow)
     const int tt = tile - wt * a.tiles_tok;  // token tile (fast: neighbours share weights)
-    TileOrigin o;
     if (SWAP) {
-        o.w0 = wt * WM;
-        o.tok0 = tt * BN;
+        o.w0 = w_base + wt * WM;
+        o.tok0 = tok_base + tt * BN;
     } else {
-        o.w0 = wt * BN;
-        o.tok0 = tt * BM;
+        o.w0 = w_base + wt * BN;
+        o.tok0 = tok_base + tt * BM;
     }
     return o;
 }
@@ -538,7 +576,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                     const float sam = a.ue8m0
                                           ? ue8m0_value(reinterpret_cast<const uint32_t*>(sl)[row], kb)
                                           : reinterpret_cast<const float*>(sl)[row];
-                    f_norm = (o.tok0 + row < a.M) ? sam * swv : 0.0f;
+                    f_norm = (o.tok0 + row < o.tok_end) ? sam * swv : 0.0f;
                 } else {
                     // per-column (token) factors sa[t] * sw, computed once per
                     // slab by the warp's lanes and read back as broadcasts
@@ -546,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                         const int t = chalf * C::CPT + c;
                         const uint32_t w = reinterpret_cast<const uint32_t*>(sl)[t];
                         const float sv = a.ue8m0 ? ue8m0_value(w, kb) : __uint_as_float(w);
-                        fw[c] = (o.tok0 + t < a.M) ? sv * swv : 0.0f;
+                        fw[c] = (o.tok0 + t < o.tok_end) ? sv * swv : 0.0f;
                     }
                     __syncwarp();
                 }
@@ -664,26 +702,30 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
             }
 
             // ------------------------------------------------------- store
+            // (the tile's bounds are recomputed here rather than held in
+            // registers across the slab loop)
+            const TileOrigin os = tile_origin<SWAP, BN, WM>(a, sg.tile);
             if (!SWAP) {
-                const int m = o.tok0 + row;
-                if (m < a.M) {
-                    const int n0 = o.w0 + chalf * C::CPT;
+                const int m = os.tok0 + row;
+                if (m < os.tok_end) {
+                    const int n0 = os.w0 + chalf * C::CPT;
 #pragma unroll
                     for (int j = 0; j < C::CPT; j += 8)
-                        if (n0 + j < a.N)
-                            store_out8(a.out, a.out_dtype, static_cast<int64_t>(m) * a.N + n0 + j,
-                                       acc[j], acc[j + 1], acc[j + 2], acc[j + 3], acc[j + 4],
-                                       acc[j + 5], acc[j + 6], acc[j + 7]);
+                        if (n0 + j < os.w_end)
+                            store_out8(a.out, a.out_dtype,
+                                       static_cast<int64_t>(m) * a.N + (n0 + j - os.col0), acc[j],
+                                       acc[j + 1], acc[j + 2], acc[j + 3], acc[j + 4], acc[j + 5],
+                                       acc[j + 6], acc[j + 7]);
                 }
             } else {
-                const int n = o.w0 + row;
-                const int t0 = o.tok0 + chalf * C::CPT;
-                if (row_ok && n < a.N) {
+                const int n = os.w0 + row;
+                const int t0 = os.tok0 + chalf * C::CPT;
+                if (row_ok && n < os.w_end) {
 #pragma unroll
                     for (int j = 0; j < C::CPT; ++j)
-                        if (t0 + j < a.M)
-                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t0 + j) * a.N + n,
-                                       acc[j]);
+                        if (t0 + j < os.tok_end)
+                            store_out1(a.out, a.out_dtype,
+                                       static_cast<int64_t>(t0 + j) * a.N + (n - os.col0), acc[j]);
                 }
             }
         }
@@ -1188,22 +1230,24 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         auto store_chunk = [&](const TileOrigin& o, int c0, const float* v) {
             if constexpr (SWAP) {
                 const int n = o.w0 + row;
-                if (n < a.N) {
+                if (n < o.w_end) {
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; ++j) {
                         const int t = o.tok0 + c0 + j;
-                        if (t < a.M)
-                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, v[j]);
+                        if (t < o.tok_end)
+                            store_out1(a.out, a.out_dtype,
+                                       static_cast<int64_t>(t) * a.N + (n - o.col0), v[j]);
                     }
                 }
             } else {
                 const int m = o.tok0 + row;
-                if (m < a.M) {
+                if (m < o.tok_end) {
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; j += 8) {
                         const int n0 = o.w0 + c0 + j;
-                        if (n0 < a.N)
-                            store_out8(a.out, a.out_dtype, static_cast<int64_t>(m) * a.N + n0, v[j],
+                        if (n0 < o.w_end)
+                            store_out8(a.out, a.out_dtype,
+                                       static_cast<int64_t>(m) * a.N + (n0 - o.col0), v[j],
                                        v[j + 1], v[j + 2], v[j + 3], v[j + 4], v[j + 5], v[j + 6],
                                        v[j + 7]);
                     }
@@ -1214,22 +1258,24 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         auto store_rc = [&](const TileOrigin& o, int c0, const float* v) {
             if constexpr (SWAP) {
                 const int n = o.w0 + row;
-                if (n < a.N) {
+                if (n < o.w_end) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int t = o.tok0 + c0 + j;
-                        if (t < a.M)
-                            store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, v[j]);
+                        if (t < o.tok_end)
+                            store_out1(a.out, a.out_dtype,
+                                       static_cast<int64_t>(t) * a.N + (n - o.col0), v[j]);
                     }
                 }
             } else {
                 const int m = o.tok0 + row;
-                if (m < a.M) {
+                if (m < o.tok_end) {
 #pragma unroll
                     for (int j = 0; j < 16; j += 8) {
                         const int n0 = o.w0 + c0 + j;
-                        if (n0 < a.N)
-                            store_out8(a.out, a.out_dtype, static_cast<int64_t>(m) * a.N + n0, v[j],
+                        if (n0 < o.w_end)
+                            store_out8(a.out, a.out_dtype,
+                                       static_cast<int64_t>(m) * a.N + (n0 - o.col0), v[j],
                                        v[j + 1], v[j + 2], v[j + 3], v[j + 4], v[j + 5], v[j + 6],
                                        v[j + 7]);
                     }
@@ -1476,12 +1522,14 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     const bool swap = SWAP;
     const uint64_t K = static_cast<uint64_t>(g.K);
     const int G = static_cast<int>(g.K / BK);
-    const int NB = static_cast<int>((g.N + BK - 1) / BK);
+    // grouped: E stacked [N, K] weights (N % 128 == 0), E * m_max token rows
+    const int64_t w_rows = g.E > 0 ? g.E * g.N : g.N;
+    const int NB = static_cast<int>((w_rows + BK - 1) / BK);
     const uint64_t Mp = static_cast<uint64_t>(pad_rows4(g.M));
     CUtensorMap tm_m, tm_n, tm_sa, tm_sw;
     bool ok;
     if (swap) {
-        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(g.N), WM);
+        ok = encode_operand(&tm_m, g.w_q, K, static_cast<uint64_t>(w_rows), WM);
         if (g.x) {
             // fused quant: raw 2-byte activations [M, K], boxes of BN rows x 128
             // elements (256 bytes, unswizzled), rows past M read as zero
@@ -1495,7 +1543,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         }
     } else {
         ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
-             encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(g.N), BN);
+             encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(w_rows), BN);
     }
     {
         // activation scales: [cols][Mp] of 4-byte words; box = the tile's tokens of one column
@@ -1528,13 +1576,20 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     a.NB = NB;
     a.swap = swap ? 1 : 0;
     a.tiles_tok = p.tiles_tok;
-    a.tiles = p.tiles_tok * p.tiles_w;
+    a.tiles_e = p.tiles_tok * p.tiles_w;
+    a.tiles = a.tiles_e * (p.experts > 0 ? p.experts : 1);
     a.split = p.split;
     a.num_items = p.num_items;
     a.units = static_cast<long long>(a.tiles) * G;
     a.ue8m0 = g.ue8m0;
     a.out_dtype = g.out_dtype;
-    a.prefetch_w = g.prefetch_w;
+    // grouped tiles are skipped by the counts, which the previous kernel may
+    // write: nothing is read before the dependency wait
+    a.prefetch_w = g.E > 0 ? 0 : g.prefetch_w;
+    a.E = static_cast<int>(g.E);
+    a.m_max = static_cast<int>(g.m_max);
+    a.tok_tile = swap ? BN : BM;
+    a.counts = g.counts;
     a.w_s = g.w_s;
     a.out = g.out;
     // workspace: [tile counters: fixed kCounterRegion prefix] [fp32 partial tiles]
@@ -1583,7 +1638,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
 }  // namespace
 
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
-                    GemmPlan* p) {
+                    GemmPlan* p, int64_t experts) {
     const int G = static_cast<int>(K / BK);
     const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
     const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
@@ -1602,6 +1657,11 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (v.mma_scale != 0 && v.mma_scale != 1) return false;
     // block-scaled MMA: 128-row tiles (swap-AB or normal), M = 128 MMAs only
     if (v.mma_scale && v.kind == FP8BQ_KIND_SWAP_AB_64) return false;
+    // grouped: split-K round robin only (stream-K shares would include the
+    // tiles of empty experts), weights in whole 128-row blocks per expert
+    if (experts < 0 || experts > (1 << 20)) return false;
+    if (experts > 0 && (v.split == 0 || N % BK != 0 || M % 4 != 0)) return false;
+    p->experts = static_cast<int>(experts);
     p->mx = v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;
@@ -1613,7 +1673,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
         p->tiles_tok = static_cast<int>((M + BM - 1) / BM);
         p->tiles_w = static_cast<int>((N + v.block_n - 1) / v.block_n);
     }
-    const long long tiles = static_cast<long long>(p->tiles_tok) * p->tiles_w;
+    const long long tiles =
+        static_cast<long long>(p->tiles_tok) * p->tiles_w * (experts > 0 ? experts : 1);
     if (tiles <= 0 || tiles > (1LL << 30)) return false;
     const int g = v.grid > 0 ? v.grid : num_sms;
     const size_t tile_bytes = static_cast<size_t>(swap ? wm : BM) * v.block_n * sizeof(float);

@@ -59,13 +59,16 @@ struct GemmPlan {
     int tiles_tok; // token tiles
     int tiles_w;   // weight tiles
     int num_items; // tiles * split
+    int experts;   // grouped: experts (0: one plain problem)
     size_t ws_bytes;
 };
 
 // Fills the derived fields of a plan for (M, N, K) and the chosen variant;
-// returns false if the variant is not supported.
+// returns false if the variant is not supported.  With experts > 0 the plan
+// is for a grouped problem: `experts` independent (M, N, K) problems whose
+// token rows, weight rows and outputs are stacked (M is the rows per expert).
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
-                    GemmPlan* plan);
+                    GemmPlan* plan, int64_t experts = 0);
 
 struct GemmLaunch {
     int64_t M, N, K;
@@ -87,6 +90,13 @@ struct GemmLaunch {
     // bf16/fp16 activations [M, K] instead of a_q / a_s.
     const void* x;
     int x_fp16;
+    // Grouped problem (E > 0): M = E * m_max stacked token rows, w_q/w_s hold
+    // E stacked [N, K] weights, out is [E * m_max, N]; expert e's valid rows
+    // are [e * m_max, e * m_max + counts[e]) (device array, clamped to
+    // [0, m_max]).
+    int64_t E = 0;
+    int64_t m_max = 0;
+    const int* counts = nullptr;
 };
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmLaunch& g, cudaStream_t stream);
 

@@ -34,7 +34,9 @@ EXPORTS = (
     "fp8bq_quant_weight", "fp8bq_gemm", "fp8bq_gemm_variant", "fp8bq_linear",
     "fp8bq_select_variant", "fp8bq_reload_table", "fp8bq_device_status",
     "fp8bq_selftest_wait_timeout", "fp8bq_status_string", "fp8bq_abi_version",
-    "fp8bq_gemm_noalloc",
+    "fp8bq_gemm_noalloc", "fp8bq_grouped_gemm", "fp8bq_grouped_gemm_variant",
+    "fp8bq_select_grouped_variant", "fp8bq_grouped_gemm_workspace_bytes",
+    "fp8bq_grouped_variant_workspace_bytes",
 )
 
 
@@ -83,6 +85,15 @@ def _load():
         "fp8bq_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp]),
         "fp8bq_gemm_noalloc": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                      vp]),
+        "fp8bq_grouped_gemm": (i32, [i64, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                     i32, vp, vp, sz, vp]),
+        "fp8bq_grouped_gemm_variant": (i32, [i64, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32,
+                                             vp, ctypes.POINTER(Variant), vp, sz, vp]),
+        "fp8bq_select_grouped_variant": (i32, [i64, i64, i64, i64, i32, i32,
+                                               ctypes.POINTER(Variant)]),
+        "fp8bq_grouped_gemm_workspace_bytes": (sz, [i64, i64, i64, i64, i32, i32]),
+        "fp8bq_grouped_variant_workspace_bytes": (sz, [i64, i64, i64, i64,
+                                                       ctypes.POINTER(Variant)]),
         "fp8bq_status_string": (ctypes.c_char_p, [i32]),
         "fp8bq_abi_version": (i32, []),
     }
@@ -293,6 +304,66 @@ def fp8bq_linear(x, w_q, w_s, fmt="ue8m0", out_dtype=torch.bfloat16, out=None, w
                            block_n, block_k, _fmt(fmt), _dtype_code(out.dtype), _ptr(out),
                            _ptr(workspace), wsz, _stream(stream))
     _check(st, "fp8bq_linear")
+    return out
+
+
+# ---------------------------------------------------------------- grouped GEMM
+
+def fp8bq_select_grouped_variant(E: int, M_max: int, N: int, K: int, fmt="fp32",
+                                 out_dtype=torch.bfloat16) -> dict:
+    v = Variant()
+    st = _lib.fp8bq_select_grouped_variant(E, M_max, N, K, _fmt(fmt), _dtype_code(out_dtype),
+                                           ctypes.byref(v))
+    _check(st, "fp8bq_select_grouped_variant")
+    return v.as_dict()
+
+
+def fp8bq_grouped_gemm_workspace_bytes(E, M_max, N, K, fmt="fp32", out_dtype=torch.bfloat16):
+    return _lib.fp8bq_grouped_gemm_workspace_bytes(E, M_max, N, K, _fmt(fmt),
+                                                   _dtype_code(out_dtype))
+
+
+def fp8bq_grouped_variant_workspace_bytes(E, M_max, N, K, variant: Variant) -> int:
+    return _lib.fp8bq_grouped_variant_workspace_bytes(E, M_max, N, K, ctypes.byref(variant))
+
+
+def fp8bq_grouped_gemm(a_q, a_s, w_q, w_s, counts, fmt="fp32", out_dtype=torch.bfloat16,
+                       out=None, workspace=None, variant: Variant | None = None, stream=None):
+    """Grouped (MoE) GEMM, masked layout.  E = counts.numel() experts;
+    a_q: [E*M_max, K] codes (a_s their scales); w_q: [E, N, K] (or [E*N, K])
+    codes, w_s: [E, N/128, K/128] fp32; counts: int32 [E] on the GPU.  Rows of
+    expert e at or past counts[e] of ``out`` [E*M_max, N] are left as they are."""
+    for t, n in ((a_q, "a_q"), (a_s, "a_s"), (w_q, "w_q"), (w_s, "w_s"), (counts, "counts")):
+        _need(t, n)
+    if counts.dtype != torch.int32:
+        raise ValueError("counts must be int32")
+    E = counts.numel()
+    rows, K = a_q.shape
+    if E == 0 or rows % E:
+        raise ValueError("a_q rows must be E * M_max")
+    M_max = rows // E
+    N = w_q.numel() // (E * K)
+    out = _out(rows, N, out_dtype, a_q.device, out)
+    if variant is None:
+        nbytes = fp8bq_grouped_gemm_workspace_bytes(E, M_max, N, K, fmt, out.dtype)
+    else:
+        nbytes = fp8bq_grouped_variant_workspace_bytes(E, M_max, N, K, variant)
+    if workspace is None:
+        workspace = _workspace(nbytes, a_q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant is None:
+        st = _lib.fp8bq_grouped_gemm(E, M_max, N, K, _ptr(counts), _ptr(a_q), _ptr(a_s),
+                                     _ptr(w_q), _ptr(w_s), 128, 128, 128, _fmt(fmt),
+                                     _dtype_code(out.dtype), _ptr(out), _ptr(workspace), wsz,
+                                     _stream(stream))
+        _check(st, "fp8bq_grouped_gemm")
+    else:
+        st = _lib.fp8bq_grouped_gemm_variant(E, M_max, N, K, _ptr(counts), _ptr(a_q), _ptr(a_s),
+                                             _ptr(w_q), _ptr(w_s), _fmt(fmt),
+                                             _dtype_code(out.dtype), _ptr(out),
+                                             ctypes.byref(variant), _ptr(workspace), wsz,
+                                             _stream(stream))
+        _check(st, "fp8bq_grouped_gemm_variant")
     return out
 
 

@@ -19,6 +19,10 @@ N/K, "vLLM é‡åŒ– Kernel é…ç½®æœºåˆ¶" Â§3.2 and "vLLM DeepGEMM FP8 Block GEMM å
   quant      act N(0,1); every 8th row (m % 8 == 3) holds one +-1000 spike per
              128-group (position and sign seeded)
   full grid  act N(0,1), 0.5% of K-channels x50; weight N(0,0.02)
+  moe        grouped GEMM: tokens routed top-k over E_total experts with a
+             seeded popularity (Dirichlet(0.5) over the experts), counts of
+             the first E local experts; per expert act as decode (1% of
+             K-channels x30), weights N(0,0.02) seeded per expert
 """
 from __future__ import annotations
 
@@ -136,3 +140,36 @@ PREFILL_NK = ((24576, 7168), (4096, 7168), (7168, 18432))
 QUANT_M = (1, 64, 1024, 4096, 16384)
 QUANT_K = (1536, 7168, 18432)
 FULL_NK = ((1536, 7168), (7168, 1536), (4096, 7168), (7168, 18432), (18432, 7168), (24576, 7168))
+
+
+# Grouped (MoE) workload: DeepSeek-V3 routed-expert projections (hidden 7168,
+# expert width 2048: gate+up N=4096 K=7168, down N=7168 K=2048), 256 routed
+# experts with top-8 routing, 32 of them on this GPU.
+MOE_NK = ((4096, 7168), (7168, 2048))
+MOE_E_TOTAL = 256
+MOE_E_LOCAL = 32
+MOE_TOP_K = 8
+MOE_TOKENS = (128, 4096)  # decode batch, prefill chunk
+
+
+def moe_counts(E: int, tokens: int, E_total: int = MOE_E_TOTAL, top_k: int = MOE_TOP_K,
+               seed: int = SEED_STRUCT) -> np.ndarray:
+    """Tokens routed to each of the first E experts (int32 [E]) when `tokens`
+    tokens each pick top_k distinct experts of E_total, drawn with a seeded
+    popularity vector (Dirichlet(0.5))."""
+    g = _rng(seed)
+    pop = g.dirichlet(np.full(E_total, 0.5))
+    hits = np.zeros(E_total, dtype=np.int64)
+    for _ in range(tokens):
+        hits[g.choice(E_total, size=top_k, replace=False, p=pop)] += 1
+    return hits[:E].astype(np.int32)
+
+
+def moe_act(E: int, M_max: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    """Token rows of E experts, M_max rows each (bf16 bits [E*M_max, K])."""
+    return act_decode(E * M_max, K, seed=seed)
+
+
+def moe_weight_bf16(E: int, N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
+    """E stacked expert weights (bf16 bits [E, N, K]), expert e seeded seed+e."""
+    return np.stack([weight_bf16(N, K, seed=seed + 1000 * e) for e in range(E)])

@@ -176,6 +176,53 @@ fp8bq_status fp8bq_gemm_variant(int64_t M, int64_t N, int64_t K, const void* a_q
                                 const fp8bq_variant* variant, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------- grouped GEMM */
+
+/* Grouped (mixture-of-experts) GEMM, masked layout: E independent
+ * fp8bq_gemm problems of the same (N, K), one per expert, in one launch.
+ * The pages apply the same per-shape kernel-config scheme to the MoE
+ * kernels, with the expert count added to the key ("vLLM 量化 Kernel
+ * 配置机制" §5, 同构机制的延伸), and name an MoE backend as the next target
+ * ("用 Helion 为 vLLM 构建高性能可移植线性后端", 未来工作); neither spells the
+ * kernel out.  The reading taken: expert e multiplies its own token rows by
+ * its own 128x128-block-quantised weights, exactly as fp8bq_gemm does.
+ *   rows of expert e: [e*M_max, e*M_max + c_e), c_e = counts[e] clamped to
+ *   [0, M_max]; out[e*M_max + m, n] = fp8bq_gemm of (a rows, w_q[e], w_s[e]).
+ * counts: int32 [E] in DEVICE memory (a routing kernel may write it just
+ *   before; it is read after the preceding work in `stream` has finished).
+ * a_q: [E*M_max, K] e4m3; a_s: fp8bq_quant_act scales of all E*M_max rows.
+ * w_q: [E][N][K] e4m3 (E stacked fp8bq_quant_weight outputs);
+ * w_s: fp32 [E][N/128][K/128].
+ * out: [E*M_max, N]; rows of an expert at or past its count are not written.
+ * Preconditions (else FP8BQ_ERR_SHAPE): M_max % 4 == 0 (each expert's scale
+ * rows start 16-byte aligned), N % 128 == 0, K % 128 == 0.  E >= 1.
+ * M_max == 0 or N == 0 is a no-op.  The kernel shape comes from
+ * fp8bq_select_grouped_variant (every expert counted as full). */
+fp8bq_status fp8bq_grouped_gemm(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                const int32_t* counts, const void* a_q, const void* a_s,
+                                const void* w_q, const float* w_s, int group, int block_n,
+                                int block_k, fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/* fp8bq_grouped_gemm with an explicit kernel shape.  Stream-K (split 0) is
+ * not accepted for grouped problems (FP8BQ_ERR_UNSUPPORTED). */
+fp8bq_status fp8bq_grouped_gemm_variant(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                        const int32_t* counts, const void* a_q,
+                                        const void* a_s, const void* w_q, const float* w_s,
+                                        fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                                        const fp8bq_variant* variant, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+
+/* The kernel shape fp8bq_grouped_gemm uses, and workspace sizes. */
+fp8bq_status fp8bq_select_grouped_variant(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                          fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype,
+                                          fp8bq_variant* variant);
+size_t fp8bq_grouped_gemm_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                          fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype);
+size_t fp8bq_grouped_variant_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                             const fp8bq_variant* variant);
+
 /* Activation quant followed by the GEMM, one call, two launches on `stream`
  * (the whole W8A8 linear layer for a bf16/fp16 input x [M,K]).  The codes and
  * scales go to the front of `workspace`; see fp8bq_linear_workspace_bytes.

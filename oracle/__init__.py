@@ -182,6 +182,38 @@ def gemm_elem(qa, sa, qw, sw, ue8m0: bool, m: int, n: int, group: int = 128, bn:
                                   _ptr(sw), group, bn, bk, m, n)
 
 
+def grouped_gemm(qa, sa, qw, sw, counts, ue8m0: bool, out=None, group: int = 128,
+                 bn: int = 128, bk: int = 128) -> np.ndarray:
+    """Grouped (MoE) GEMM, masked layout: E = len(counts) experts; expert e
+    owns token rows [e*M_max, e*M_max + c_e) of qa (c_e = counts[e] clamped
+    to [0, M_max]) and weights qw[e] [N,K] with scales sw[e].  Each expert's
+    rows are the plain block-scaled GEMM of those rows and its own weights
+    ("vLLM 量化 Kernel 配置机制" §5 applies the linear path's kernel scheme to
+    MoE experts; the per-expert product is "vLLM DeepGEMM FP8 Block GEMM
+    基准测试" §4.2's fp8_gemm_nt).  Rows past an expert's count keep the
+    value they have in ``out`` (NaN when out is None).
+
+    qa [E*M_max, K] codes, sa their scales in the quant layout of all
+    E*M_max rows; qw [E, N, K]; sw [E, ceil(N/128), K/128]."""
+    counts = np.asarray(counts)
+    E = counts.shape[0]
+    rows, K = qa.shape
+    M_max = rows // E
+    N = qw.shape[1]
+    if out is None:
+        out = np.full((rows, N), np.nan)
+    for e in range(E):
+        c = int(min(max(int(counts[e]), 0), M_max))
+        if c == 0:
+            continue
+        # the plain GEMM over all rows' scales, restricted to this expert's
+        # rows and weights
+        out[e * M_max:e * M_max + c] = gemm(qa, sa, np.ascontiguousarray(qw[e]),
+                                            np.ascontiguousarray(sw[e]), ue8m0, group, bn, bk,
+                                            rows=(e * M_max, c))
+    return out
+
+
 def calc_diff(x: np.ndarray, y: np.ndarray) -> float:
     x = np.ascontiguousarray(x, dtype=np.float64).ravel()
     y = np.ascontiguousarray(y, dtype=np.float64).ravel()

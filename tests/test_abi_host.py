@@ -175,3 +175,41 @@ def test_variant_workspace_bytes():
         256, 7168, 18432, fp8bq.make_variant("normal", 128, 2, 0, 1)) > 0
     assert fp8bq.fp8bq_variant_workspace_bytes(
         8, 7168, 18432, fp8bq.make_variant("swap64", 16, 2, 0, 1)) == 0
+
+
+def call_grouped(E=4, M_max=8, N=128, K=256, ptr=4096, counts=4096, fmt=0, out=0):
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(ptr)
+    c = None if counts is None else ctypes.c_void_p(counts)
+    return lib.fp8bq_grouped_gemm(E, M_max, N, K, c, p, p, p, p, 128, 128, 128, fmt, out, p,
+                                  None, 0, None)
+
+
+def test_grouped_argument_errors_on_host():
+    assert call_grouped(E=0) == 1          # no experts
+    assert call_grouped(M_max=-4) == 1
+    assert call_grouped(M_max=6) == 2      # rows per expert not a multiple of 4
+    assert call_grouped(N=192) == 2        # weights not in whole 128-row blocks
+    assert call_grouped(K=100) == 2
+    assert call_grouped(counts=None) == 1  # counts pointer missing
+    assert call_grouped(ptr=4100) == 3
+    assert call_grouped(M_max=0) == 0      # empty: no-op
+    assert call_grouped(N=0) == 0
+
+
+def test_grouped_variant_selection_and_workspace():
+    # decode-sized experts: swap-AB token tiles from the rows per expert
+    v = fp8bq.fp8bq_select_grouped_variant(32, 24, 4096, 7168, "ue8m0", "bf16")
+    assert (v["kind"], v["block_n"], v["split"]) == ("swap", 32, 1)
+    assert fp8bq.fp8bq_grouped_gemm_workspace_bytes(32, 24, 4096, 7168, "ue8m0", "bf16") == 0
+    v = fp8bq.fp8bq_select_grouped_variant(8, 512, 7168, 2048, "fp32", "bf16")
+    assert (v["kind"], v["block_n"], v["split"]) == ("normal", 256, 1)
+    # few tiles: split K until the GPU's 152 SMs have work (at most 8, at most G)
+    v = fp8bq.fp8bq_select_grouped_variant(2, 8, 256, 4096, "fp32", "bf16")
+    assert (v["kind"], v["block_n"], v["split"]) == ("swap", 16, 8)
+    tiles = 2 * 2 * 1
+    assert fp8bq.fp8bq_grouped_gemm_workspace_bytes(2, 8, 256, 4096, "fp32", "bf16") == \
+        65536 + tiles * 8 * 128 * 16 * 4
+    # stream-K is not offered for grouped problems
+    assert fp8bq.fp8bq_grouped_variant_workspace_bytes(
+        2, 8, 256, 4096, fp8bq.make_variant("swap", 16, 0)) == 0
