@@ -134,7 +134,8 @@ struct KArgs {
     // M = E * m_max, N is one expert's width (and the output row length)
     int E;
     int m_max;
-    int tiles_e;        // tiles per expert (tiles_tok * weight tiles)
+    int tiles_e;        // tiles per expert (tiles_tok * tiles_w)
+    int tiles_w;        // weight tiles per expert
     int tok_tile;       // tokens per tile (BN when swap, BM otherwise)
     const int* counts;  // valid token rows of each expert (device)
 };
@@ -156,23 +157,25 @@ __device__ __forceinline__ int sk_owner(long long u, long long T, long long P) {
 }
 
 // Grouped problems: valid token rows of expert e (its count clamped to
-// [0, m_max]), and whether a tile holds none of them (such tiles are skipped
-// by every role alike).
+// [0, m_max]).
 __device__ __forceinline__ int expert_rows(const KArgs& a, int e) {
     const int c = __ldg(a.counts + e);
     return c < 0 ? 0 : (c > a.m_max ? a.m_max : c);
 }
-__device__ __forceinline__ bool tile_empty(const KArgs& a, int tile) {
-    const int e = tile / a.tiles_e;
-    const int r = tile - e * a.tiles_e;
-    const int tt = r - (r / a.tiles_tok) * a.tiles_tok;
-    return tt * a.tok_tile >= expert_rows(a, e);
-}
 
 // Iterates this CTA's segments in order (identically in every role).
+//
+// Grouped problems number only the tiles that hold rows: expert by expert,
+// within an expert weight tile by weight tile and its occupied token tiles,
+// and (tile, split part) items go round robin over the CTAs, so every CTA
+// gets the same number of items to within one whatever the counts are.  An
+// iterator walks the experts forward as its item index grows.
 struct WorkIter {
     long long u, u_end;  // stream-K
     int item;            // split-K
+    int ge;              // grouped: expert of the current items
+    int gbase;           // grouped: index of expert ge's first item
+    int gnt;             // grouped: token tiles of expert ge holding rows
 
     __device__ void init(const KArgs& a) {
         if (a.split == 0) {
@@ -180,6 +183,9 @@ struct WorkIter {
             u_end = sk_begin(blockIdx.x + 1, a.units, gridDim.x);
         } else {
             item = blockIdx.x;
+            ge = -1;
+            gbase = 0;
+            gnt = 0;
         }
     }
 
@@ -198,17 +204,36 @@ struct WorkIter {
             u += s.kb1 - s.kb0;
             return true;
         }
-        for (;;) {
+        if (a.E > 0) {
+            if (ge >= a.E) return false;
+            for (;;) {
+                if (ge >= 0) {
+                    const int n_items = gnt * a.tiles_w * a.split;
+                    if (item < gbase + n_items) break;
+                    gbase += n_items;
+                }
+                if (ge >= a.E - 1) {
+                    ge = a.E;
+                    return false;
+                }
+                ++ge;
+                gnt = (expert_rows(a, ge) + a.tok_tile - 1) / a.tok_tile;
+            }
+            const int local = item - gbase;
+            const int tl = local / a.split;
+            s.part = local - tl * a.split;
+            const int wt = tl / gnt;
+            s.tile = ge * a.tiles_e + wt * a.tiles_tok + (tl - wt * gnt);
+        } else {
             if (item >= a.num_items) return false;
             s.tile = item / a.split;
             s.part = item - s.tile * a.split;
-            item += gridDim.x;
-            if (a.E > 0 && tile_empty(a, s.tile)) continue;
-            s.nparts = a.split;
-            s.kb0 = static_cast<int>((static_cast<long long>(s.part) * a.G) / a.split);
-            s.kb1 = static_cast<int>((static_cast<long long>(s.part + 1) * a.G) / a.split);
-            return true;
         }
+        item += gridDim.x;
+        s.nparts = a.split;
+        s.kb0 = static_cast<int>((static_cast<long long>(s.part) * a.G) / a.split);
+        s.kb1 = static_cast<int>((static_cast<long long>(s.part + 1) * a.G) / a.split);
+        return true;
     }
 };
 
@@ -1577,6 +1602,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     a.swap = swap ? 1 : 0;
     a.tiles_tok = p.tiles_tok;
     a.tiles_e = p.tiles_tok * p.tiles_w;
+    a.tiles_w = p.tiles_w;
     a.tiles = a.tiles_e * (p.experts > 0 ? p.experts : 1);
     a.split = p.split;
     a.num_items = p.num_items;
