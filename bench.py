@@ -14,6 +14,13 @@ per-problem GEMM us / TFLOPS / GB/s / roofline fraction, the roofline of the
 dominant kernel (the GEMM) against the measured HBM copy bandwidth, an
 end-to-end number through fp8bq_linear with pinned host buffers, and the CPU
 oracle timed on a bounded sample.  `--impl reference` times the oracle alone.
+
+`--workload moe` times the grouped (mixture-of-experts) path instead: 32 local
+experts of DeepSeek-V3's routed-expert projections (gate+up N=4096 K=7168,
+down N=7168 K=2048), tokens routed top-8 of 256 experts with a seeded skewed
+popularity, a decode batch (128 tokens) and a prefill chunk (4096 tokens);
+per problem one fp8bq_grouped_linear call (quant of the occupied rows +
+grouped GEMM).
 """
 from __future__ import annotations
 
@@ -232,6 +239,246 @@ def run_reference(args, rank, world):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------- MoE workload
+
+MOE_WORKLOAD = ("moe: 32 local experts, DeepSeek-V3 routed-expert projections (N,K) in "
+                "{(4096,7168),(7168,2048)}; tokens {128, 4096} routed top-8 of 256 experts "
+                "(seeded Dirichlet(0.5) popularity), rows per expert padded to the largest "
+                "count (multiple of 4); act bf16 N(0,1) 1% channels x30; weights bf16 "
+                "N(0,0.02) 128x128 UE8M0; bf16 out; fp8bq_grouped_linear per problem")
+
+
+def moe_problems():
+    """(tokens, N, K, counts, M_max) of the MoE step."""
+    out = []
+    for T in synth.MOE_TOKENS:
+        counts = synth.moe_counts(synth.MOE_E_LOCAL, T)
+        M_max = int((counts.max() + 3) // 4 * 4)
+        for (N, K) in synth.MOE_NK:
+            out.append((T, N, K, counts, M_max))
+    return out
+
+
+def moe_bytes(N, K, counts, linear):
+    """Algorithmic bytes of one grouped problem: the weights and weight scales
+    of the experts that hold tokens, and the occupied rows (bf16 in for the
+    linear layer; e4m3 codes + packed scales for the GEMM alone), bf16 out."""
+    G = K // 128
+    ne = int((counts > 0).sum())
+    toks = int(counts.sum())
+    w = ne * (N * K + 4 * (N // 128) * G)
+    a = 2 * toks * K if linear else toks * K + 4 * ((G + 3) // 4) * toks
+    return w + a + 2 * toks * N
+
+
+def run_gpu_moe(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    E = synth.MOE_E_LOCAL
+    probs = moe_problems()
+    wq, ws, xs, cnts, outs, variants = [], [], [], [], [], []
+    w_cache = {}
+    for (T, N, K, counts, M_max) in probs:
+        if (N, K) not in w_cache:
+            q = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+            s = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
+            wb = synth.moe_weight_bf16(E, N, K)
+            for e in range(E):
+                wd = torch.from_numpy(wb[e].view(np.int16)).view(torch.bfloat16).to(dev)
+                fp8bq.fp8bq_quant_weight(wd, "ue8m0", q=q[e], s=s[e])
+            del wb
+            w_cache[(N, K)] = (q, s)
+        q, s = w_cache[(N, K)]
+        wq.append(q.clone())  # every problem reads its own copy (> L2 each)
+        ws.append(s)
+        xb = synth.moe_act(E, M_max, K)
+        xs.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev))
+        cnts.append(torch.from_numpy(counts).to(dev))
+        outs.append(torch.empty((E * M_max, N), dtype=torch.bfloat16, device=dev))
+        variants.append(fp8bq.fp8bq_select_grouped_variant(E, M_max, N, K, "ue8m0"))
+    del w_cache
+    ws_bytes = max(fp8bq.fp8bq_grouped_linear_workspace_bytes(E, p[4], p[1], p[2], "ue8m0")
+                   for p in probs)
+    wspace = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
+    aqs = [torch.empty((E * p[4], p[2]), dtype=torch.uint8, device=dev) for p in probs]
+    ass = [torch.empty(fp8bq.act_scale_shape(E * p[4], p[2], 128, "ue8m0")[0],
+                       dtype=torch.int32, device=dev) for p in probs]
+    gws = torch.zeros(max(fp8bq.fp8bq_grouped_gemm_workspace_bytes(E, p[4], p[1], p[2], "ue8m0")
+                          for p in probs) + (1 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        for i in range(len(probs)):
+            fp8bq.fp8bq_grouped_linear(xs[i], wq[i], ws[i], cnts[i], fmt="ue8m0", out=outs[i],
+                                       workspace=wspace)
+
+    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in probs]
+    ev_s, ev_e, ev2_s, ev2_e = mk(), mk(), mk(), mk()
+
+    def step_split():
+        for i in range(len(probs)):
+            fp8bq.fp8bq_quant_act(xs[i], "ue8m0", q=aqs[i], s=ass[i])
+            ev[i][0].record()
+            fp8bq.fp8bq_grouped_gemm(aqs[i], ass[i], wq[i], ws[i], cnts[i], fmt="ue8m0",
+                                     out=outs[i], workspace=gws)
+            ev[i][1].record()
+
+    step()
+    step_split()
+    torch.cuda.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g1, stream=side):
+            ev_s.record()
+            step()
+            ev_e.record()
+        with torch.cuda.graph(g2, stream=side):
+            ev2_s.record()
+            step_split()
+            ev2_e.record()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g1.replay()
+        g2.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    step_ms = []
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        g1.replay()
+        ev_e.synchronize()
+        step_ms.append(ev_s.elapsed_time(ev_e))
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    step_s = float(np.mean(step_ms)) / 1e3
+    n_instr = max(1, min(args.steps, args.instr_steps))
+    gemm_ms = np.zeros(len(probs))
+    for _ in range(n_instr):
+        g2.replay()
+        ev2_e.synchronize()
+        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev])
+    gemm_us = gemm_ms / n_instr * 1e3
+    assert fp8bq.fp8bq_device_status() == 0
+
+    # end to end: activations and counts from pinned host memory, outputs back
+    hx = [x.cpu().pin_memory() for x in xs]
+    hc = [c.cpu().pin_memory() for c in cnts]
+    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(x.numel() * 2 + c.numel() * 4 for x, c in zip(hx, hc))
+    d2h = sum(o.numel() * 2 for o in ho)
+
+    def e2e_step():
+        for i in range(len(probs)):
+            xs[i].copy_(hx[i], non_blocking=True)
+            cnts[i].copy_(hc[i], non_blocking=True)
+            fp8bq.fp8bq_grouped_linear(xs[i], wq[i], ws[i], cnts[i], fmt="ue8m0", out=outs[i],
+                                       workspace=wspace)
+            ho[i].copy_(outs[i], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    g3 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g3, stream=side):
+            e2e_step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g3.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(args.steps, args.e2e_steps))
+    a.record()
+    for _ in range(n_e2e):
+        g3.replay()
+    b.record()
+    b.synchronize()
+    e2e_s = a.elapsed_time(b) / 1e3 / n_e2e
+    step_total = sum(moe_bytes(p[1], p[2], p[3], True) for p in probs)
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
+    per = []
+    for i, (T, N, K, counts, M_max) in enumerate(probs):
+        t = gemm_us[i] * 1e-6
+        byt = moe_bytes(N, K, counts, False)
+        fl = 2.0 * int(counts.sum()) * N * K
+        t_roof = max(byt / (peaks["hbm_gbs"] * 1e9), fl / (fp8_peak * 1e12))
+        per.append({"tokens": T, "n": N, "k": K, "experts": E, "m_max": M_max,
+                    "experts_with_tokens": int((counts > 0).sum()),
+                    "token_rows": int(counts.sum()), "us": round(gemm_us[i], 3),
+                    "tflops": round(fl / t / 1e12, 2), "gbs_alg": round(byt / t / 1e9, 1),
+                    "roofline_frac": round(t_roof / t, 3),
+                    "variant": variant_name(variants[i])})
+    tot_gemm = sum(moe_bytes(p[1], p[2], p[3], False) for p in probs)
+    achieved = tot_gemm / (gemm_us.sum() * 1e-6) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        est, sample_s, desc = moe_oracle_sample()
+        cpu = {"value": step_total / est / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f" (sample took {sample_s:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": MOE_WORKLOAD, "problems_per_step": len(probs),
+                   "l2": "inputs larger than L2: every problem reads its own weight copy "
+                         "(0.47-0.94 GB each)",
+                   "timing": "graph: step = fp8bq_grouped_linear per problem, CUDA events on "
+                             "the launching stream; per-GEMM durations from an instrumented "
+                             "pass (quant and grouped GEMM as separate calls)",
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None,
+                     "kernel": "grouped block-FP8 GEMM (gemm_kernel / gemm_mx_kernel, grouped "
+                               "tiles), 4 launches per step",
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": step_total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
+                "api": "fp8bq_grouped_linear per problem (graph), activations and counts "
+                       "copied in from pinned host memory and outputs copied back each step"},
+        "gpu_launches": args.steps * 2 * len(probs), "clocks": clk, "per_shape": per,
+        "wall_timed_s": round(t_wall, 3), "gemm_source_sha256_16": gemm_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def moe_oracle_sample():
+    """The oracle on one thread over one token row of each MoE problem (quant
+    of the row + its GEMM row against its expert's weights), extrapolated
+    linearly to the problem's token rows."""
+    import oracle
+    est, sample_s = 0.0, 0.0
+    for (T, N, K, counts, M_max) in moe_problems():
+        e = int(np.argmax(counts > 0))
+        wb = synth.moe_weight_bf16(1, N, K, seed=synth.SEED_WEIGHT + 1000 * e)[0]
+        qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+        xb = synth.act_decode(1, K)
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
+        oracle.gemm(qa, sa, qw, sw, True)
+        dt = time.perf_counter() - t0
+        sample_s += dt
+        est += dt * int(counts.sum())
+    return est, sample_s, ("one token row per MoE problem through oracle quant + fp64 GEMM "
+                           "(all N columns of its expert), single thread; extrapolated "
+                           "linearly to each problem's token rows")
 
 
 # ------------------------------------------------------------- GPU arm
@@ -518,6 +765,7 @@ def main():
     ap.add_argument("--steps-ref", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("decode", "moe"), default="decode")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -525,6 +773,10 @@ def main():
         args.steps_ref = max(1, min(args.steps, 10))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.workload == "moe":
+        if world > 1 and rank != 0:
+            return 0
+        return run_gpu_moe(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

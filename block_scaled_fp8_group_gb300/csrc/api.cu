@@ -345,7 +345,8 @@ fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, con
 fp8bq_status run_grouped_gemm(const GemmPlan& plan, int64_t E, int64_t M_max, int64_t N,
                               int64_t K, const int32_t* counts, const void* a_q, const void* a_s,
                               const void* w_q, const float* w_s, int fmt, int out_dtype,
-                              void* out, void* ws, DeviceInfo* d, cudaStream_t stream) {
+                              void* out, void* ws, size_t ws_data_offset, DeviceInfo* d,
+                              cudaStream_t stream) {
     if (plan.mx && (fmt != FP8BQ_SCALE_UE8M0 || K % (4 * kGroup) != 0))
         return FP8BQ_ERR_UNSUPPORTED;
     GemmLaunch g;
@@ -360,7 +361,7 @@ fp8bq_status run_grouped_gemm(const GemmPlan& plan, int64_t E, int64_t M_max, in
     g.out_dtype = out_dtype;
     g.out = out;
     g.workspace = ws;
-    g.ws_data_offset = 0;
+    g.ws_data_offset = ws_data_offset;
     g.status = d->status;
     g.timeout_ns = wait_timeout_ns();
     g.prefetch_w = 0;
@@ -644,7 +645,7 @@ fp8bq_status fp8bq_grouped_gemm_variant(int64_t E, int64_t M_max, int64_t N, int
     st = check_ws(plan, workspace, workspace_bytes);
     if (st != FP8BQ_OK) return st;
     return run_grouped_gemm(plan, E, M_max, N, K, counts, a_q, a_s, w_q, w_s, fmt, out_dtype, out,
-                            workspace, d, stream);
+                            workspace, 0, d, stream);
 }
 
 fp8bq_status fp8bq_grouped_gemm(int64_t E, int64_t M_max, int64_t N, int64_t K,
@@ -661,6 +662,64 @@ fp8bq_status fp8bq_grouped_gemm(int64_t E, int64_t M_max, int64_t N, int64_t K,
     if (st != FP8BQ_OK) return st;
     return fp8bq_grouped_gemm_variant(E, M_max, N, K, counts, a_q, a_s, w_q, w_s, fmt, out_dtype,
                                       out, &v, workspace, workspace_bytes, stream);
+}
+
+size_t fp8bq_grouped_linear_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                            fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype) {
+    if (check_grouped_args(E, M_max, N, K, fmt, out_dtype) != FP8BQ_OK) return 0;
+    const int64_t rows = E * M_max;
+    const size_t g = fp8bq_grouped_gemm_workspace_bytes(E, M_max, N, K, fmt, out_dtype);
+    return kCounterRegion + align256(static_cast<size_t>(rows * K)) +
+           align256(fp8bq_act_scale_bytes(rows, K, kGroup, fmt)) + (g ? g - kCounterRegion : 0);
+}
+
+fp8bq_status fp8bq_grouped_linear(const void* x, fp8bq_dtype x_dtype, int64_t E, int64_t M_max,
+                                  int64_t N, int64_t K, const int32_t* counts, const void* w_q,
+                                  const float* w_s, int group, int block_n, int block_k,
+                                  fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_grouped_args(E, M_max, N, K, fmt, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (M_max == 0 || N == 0) return FP8BQ_OK;
+    if (!x || !counts) return FP8BQ_ERR_INVALID_ARG;
+    st = check_gemm_ptrs(x, x, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    if ((K / kGroup + 3) / 4 > 65535) return FP8BQ_ERR_SHAPE;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8BQ_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = default_grouped_variant(E, M_max, N, K, fmt, d->num_sms);
+    GemmPlan plan;
+    if (!make_gemm_plan(M_max, N, K, v, d->num_sms, &plan, E)) return FP8BQ_ERR_UNSUPPORTED;
+    // workspace: [counter prefix][codes][scales][split-K partials], as fp8bq_linear
+    const int64_t rows = E * M_max;
+    const size_t q_bytes = align256(static_cast<size_t>(rows * K));
+    const size_t s_bytes = align256(fp8bq_act_scale_bytes(rows, K, kGroup, fmt));
+    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
+    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
+        return FP8BQ_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* a_q = base + kCounterRegion;
+    void* a_s = base + kCounterRegion + q_bytes;
+    QuantActArgs qa;
+    qa.x = x;
+    qa.q = static_cast<uint8_t*>(a_q);
+    qa.s = a_s;
+    qa.M = rows;
+    qa.Mp = pad_rows4(rows);
+    qa.K = K;
+    qa.G = static_cast<int>(K / kGroup);
+    qa.ue8m0 = fmt == FP8BQ_SCALE_UE8M0;
+    qa.fp16 = x_dtype == FP8BQ_FP16;
+    qa.counts = counts;
+    qa.m_max = M_max;
+    st = from_cuda(launch_quant_act(qa, stream));
+    if (st != FP8BQ_OK) return st;
+    return run_grouped_gemm(plan, E, M_max, N, K, counts, a_q, a_s, w_q, w_s, fmt, out_dtype, out,
+                            base, q_bytes + s_bytes, d, stream);
 }
 
 fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N, int64_t K,

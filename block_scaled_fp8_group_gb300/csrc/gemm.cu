@@ -169,7 +169,9 @@ __device__ __forceinline__ int expert_rows(const KArgs& a, int e) {
 // within an expert weight tile by weight tile and its occupied token tiles,
 // and (tile, split part) items go round robin over the CTAs, so every CTA
 // gets the same number of items to within one whatever the counts are.  An
-// iterator walks the experts forward as its item index grows.
+// iterator walks the experts forward as its item index grows.  GR (grouped)
+// is a template parameter, so the plain kernels carry none of this.
+template <bool GR>
 struct WorkIter {
     long long u, u_end;  // stream-K
     int item;            // split-K
@@ -204,7 +206,7 @@ struct WorkIter {
             u += s.kb1 - s.kb0;
             return true;
         }
-        if (a.E > 0) {
+        if constexpr (GR) {
             if (ge >= a.E) return false;
             for (;;) {
                 if (ge >= 0) {
@@ -256,12 +258,12 @@ struct TileOrigin {
     int col0;     // output column of weight row n: n - col0
 };
 
-template <bool SWAP, int BN, int WM = BM>
+template <bool SWAP, int BN, int WM, bool GR>
 __device__ __forceinline__ TileOrigin tile_origin(const KArgs& a, int tile) {
     int tok_base = 0, w_base = 0;
     TileOrigin o;
     o.tok_end = a.M;
-    if (a.E > 0) {
+    if constexpr (GR) {
         const int e = tile / a.tiles_e;
         tile -= e * a.tiles_e;
         tok_base = e * a.m_max;
@@ -338,7 +340,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
 }
 
-template <bool SWAP, int BN, int WM>
+template <bool SWAP, int BN, int WM, bool GR>
 __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
@@ -415,11 +417,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
     // else is read or written only after the previous grid has finished.
     int prefetched = 0;
     if (a.prefetch_w && warp == 0 && lane == 0) {
-        WorkIter wi;
+        WorkIter<GR> wi;
         wi.init(a);
         Seg sg;
         if (wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, WM, GR>(a, sg.tile);
             const int nslab = sg.kb1 - sg.kb0;
             prefetched = nslab < C::STAGES ? nslab : C::STAGES;
             for (int i = 0; i < prefetched; ++i) {
@@ -452,12 +454,12 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
             int stage = 0, slot = 0;
             uint32_t phase = 0, sphase = 0;
             long long fills = 0, sfills = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
             while (ok && wi.next(a, sg)) {
-                const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
+                const TileOrigin o = tile_origin<SWAP, BN, WM, GR>(a, sg.tile);
                 const int row_m = SWAP ? o.w0 : o.tok0;
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(C::MR, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, bphase = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
@@ -570,12 +572,12 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                                 static_cast<uint32_t>(chalf * C::CPT);
         int buf = 0, slot = 0;
         uint32_t bphase = 0, sphase = 0;
-        WorkIter wi;
+        WorkIter<GR> wi;
         wi.init(a);
         Seg sg;
         bool ok = true;
         while (ok && wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN, WM>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, WM, GR>(a, sg.tile);
             const int nb = o.w0 / BK;
             float acc[C::CPT];
 #pragma unroll
@@ -729,7 +731,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
             // ------------------------------------------------------- store
             // (the tile's bounds are recomputed here rather than held in
             // registers across the slab loop)
-            const TileOrigin os = tile_origin<SWAP, BN, WM>(a, sg.tile);
+            const TileOrigin os = tile_origin<SWAP, BN, WM, GR>(a, sg.tile);
             if (!SWAP) {
                 const int m = os.tok0 + row;
                 if (m < os.tok_end) {
@@ -852,7 +854,7 @@ struct MxCfg {
                   "scale slot layout");
 };
 
-template <bool SWAP, int BN, int FQ>
+template <bool SWAP, int BN, int FQ, bool GR>
 __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                    const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
@@ -931,11 +933,11 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
     // be read before the previous grid has finished.
     int prefetched = 0;
     if (a.prefetch_w && warp == 0 && lane == 0) {
-        WorkIter wi;
+        WorkIter<GR> wi;
         wi.init(a);
         Seg sg;
         if (wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, BM, GR>(a, sg.tile);
             const int nslab = sg.kb1 - sg.kb0;
             prefetched = nslab < C::STAGES ? nslab : C::STAGES;
             for (int i = 0; i < prefetched; ++i) {
@@ -961,12 +963,12 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
             int stage = 0, slot = 0;
             uint32_t phase = 0, sphase = 0;
             long long fills = 0, sfills = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
             while (ok && wi.next(a, sg)) {
-                const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+                const TileOrigin o = tile_origin<SWAP, BN, BM, GR>(a, sg.tile);
                 const int row_m = SWAP ? o.w0 : o.tok0;
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
@@ -1050,7 +1052,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         if (lane == 0) {
             int stage = 0, r = 0, acc = 0;
             uint32_t phase = 0, rphase = 0, aphase = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
@@ -1122,7 +1124,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
             const int c16 = lane & 7;        // 16-element chunk within the row
             int stage = 0;
             uint32_t phase = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
@@ -1182,7 +1184,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
             // -------------------------------------------------- factor writers
             int slot = 0, r = 0;
             uint32_t sphase = 0, rphase = 0;
-            WorkIter wi;
+            WorkIter<GR> wi;
             wi.init(a);
             Seg sg;
             bool ok = true;
@@ -1246,7 +1248,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         const int row = quad * 32 + lane;  // MMA-M row: weight row (swap-AB) or token
         int acc = 0;
         uint32_t aphase = 0;
-        WorkIter wi;
+        WorkIter<GR> wi;
         wi.init(a);
         Seg sg;
         bool ok = true;
@@ -1311,7 +1313,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         int fstage = 0, fr = 0;
         uint32_t fphase = 0, frphase = 0;
         while (ok && wi.next(a, sg)) {
-            const TileOrigin o = tile_origin<SWAP, BN>(a, sg.tile);
+            const TileOrigin o = tile_origin<SWAP, BN, BM, GR>(a, sg.tile);
             if constexpr (FQ > 0) {
                 // per 4-slab group (as the packed words of the unfused path):
                 // byte j of the weight word = the block's exponent of slab
@@ -1507,19 +1509,20 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        err = cudaFuncSetAttribute(gemm_kernel<SWAP, BN, WM>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (err != cudaSuccess) return err;
-        if (C::REGSPLIT) {
-            // the register split asks for REG_ROLE/REG_EPI per warpgroup; a
-            // launch that provides fewer registers in total would never
-            // satisfy setmaxnreg.inc, so refuse it
-            cudaFuncAttributes fa;
-            err = cudaFuncGetAttributes(&fa, gemm_kernel<SWAP, BN, WM>);
+        for (auto fn : {gemm_kernel<SWAP, BN, WM, false>, gemm_kernel<SWAP, BN, WM, true>}) {
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
             if (err != cudaSuccess) return err;
-            if (fa.numRegs < C::REG_MIN_LAUNCH) {
-                log_error("GEMM kernel compiled with too few registers for its register split");
-                return cudaErrorInvalidConfiguration;
+            if (C::REGSPLIT) {
+                // the register split asks for REG_ROLE/REG_EPI per warpgroup;
+                // a launch that provides fewer registers in total would never
+                // satisfy setmaxnreg.inc, so refuse it
+                cudaFuncAttributes fa;
+                err = cudaFuncGetAttributes(&fa, fn);
+                if (err != cudaSuccess) return err;
+                if (fa.numRegs < C::REG_MIN_LAUNCH) {
+                    log_error("GEMM kernel compiled with too few registers for its register split");
+                    return cudaErrorInvalidConfiguration;
+                }
             }
         }
         attr_done[dev] = 1;
@@ -1527,16 +1530,17 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     if constexpr (WM == BM) {
         static int mx_attr_done[64] = {0};
         if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
-            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MxCfg<SWAP, BN, 0>::SMEM);
-            if (err != cudaSuccess) return err;
+            for (auto fn : {gemm_mx_kernel<SWAP, BN, 0, false>, gemm_mx_kernel<SWAP, BN, 0, true>}) {
+                err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           MxCfg<SWAP, BN, 0>::SMEM);
+                if (err != cudaSuccess) return err;
+            }
             if constexpr (SWAP && BN <= 32) {
-                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 1>,
+                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 1, false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            MxCfg<SWAP, BN, 1>::SMEM);
                 if (err != cudaSuccess) return err;
-                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 2>,
+                err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 2, false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            MxCfg<SWAP, BN, 2>::SMEM);
                 if (err != cudaSuccess) return err;
@@ -1643,22 +1647,28 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
                     if (g.x_fp16) {
                         cfg.blockDim = dim3(MxCfg<SWAP, BN, 2>::THREADS);
                         cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 2>::SMEM;
-                        return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 2>, tm_m, tm_n,
+                        return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 2, false>, tm_m, tm_n,
                                                   tm_n, tm_n, a);
                     }
                     cfg.blockDim = dim3(MxCfg<SWAP, BN, 1>::THREADS);
                     cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 1>::SMEM;
-                    return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 1>, tm_m, tm_n, tm_n,
+                    return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 1, false>, tm_m, tm_n, tm_n,
                                               tm_n, a);
                 }
             }
             cfg.blockDim = dim3(MxCfg<SWAP, BN, 0>::THREADS);
             cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0>::SMEM;
-            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0>, tm_m, tm_n, tm_sa, tm_sw,
-                                      a);
+            if (g.E > 0)
+                return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, true>, tm_m, tm_n,
+                                          tm_sa, tm_sw, a);
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, false>, tm_m, tm_n, tm_sa,
+                                      tm_sw, a);
         }
     }
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM>, tm_m, tm_n, tm_sa, tm_sw, a);
+    if (g.E > 0)
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM, true>, tm_m, tm_n, tm_sa, tm_sw,
+                                  a);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM, false>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
 }  // namespace

@@ -34,6 +34,11 @@ struct QuantActArgs {
     int G;       // groups per row
     int ue8m0;
     int fp16;    // input is fp16 (else bf16)
+    // Grouped rows (optional): row r belongs to expert r / m_max and is
+    // quantised only if r % m_max < counts[expert] (device array, clamped to
+    // [0, m_max]); other rows are neither read nor written.
+    const int* counts = nullptr;
+    int64_t m_max = 0;
 };
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream);
 

@@ -29,7 +29,7 @@ namespace {
 // or sum of those with compile-time constants.
 constexpr int kQuantRows = 8;  // warps per CTA = rows per CTA
 
-template <bool kFp16>
+template <bool kFp16, bool kGrouped>
 __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantActArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantRows + (threadIdx.x >> 5);
@@ -42,6 +42,12 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
     pdl_wait_prior_grid();
     pdl_launch_dependents();
     if (row >= a.Mp) return;
+    if (kGrouped && row < a.M) {
+        // grouped rows: skip the rows past the expert's count (warp-uniform)
+        const int64_t e = row / a.m_max;
+        const int c = __ldg(a.counts + e);
+        if (row - e * a.m_max >= (c < 0 ? 0 : c)) return;
+    }
 
     const int64_t off = row * a.K + static_cast<int64_t>(quad) * 512 + lane * 16;
     uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
@@ -222,8 +228,12 @@ cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.fp16) return cudaLaunchKernelEx(&cfg, quant_act_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, quant_act_kernel<false>, a);
+    if (a.counts != nullptr) {
+        if (a.fp16) return cudaLaunchKernelEx(&cfg, quant_act_kernel<true, true>, a);
+        return cudaLaunchKernelEx(&cfg, quant_act_kernel<false, true>, a);
+    }
+    if (a.fp16) return cudaLaunchKernelEx(&cfg, quant_act_kernel<true, false>, a);
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel<false, false>, a);
 }
 
 cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream) {

@@ -36,7 +36,8 @@ EXPORTS = (
     "fp8bq_selftest_wait_timeout", "fp8bq_status_string", "fp8bq_abi_version",
     "fp8bq_gemm_noalloc", "fp8bq_grouped_gemm", "fp8bq_grouped_gemm_variant",
     "fp8bq_select_grouped_variant", "fp8bq_grouped_gemm_workspace_bytes",
-    "fp8bq_grouped_variant_workspace_bytes",
+    "fp8bq_grouped_variant_workspace_bytes", "fp8bq_grouped_linear",
+    "fp8bq_grouped_linear_workspace_bytes",
 )
 
 
@@ -94,6 +95,9 @@ def _load():
         "fp8bq_grouped_gemm_workspace_bytes": (sz, [i64, i64, i64, i64, i32, i32]),
         "fp8bq_grouped_variant_workspace_bytes": (sz, [i64, i64, i64, i64,
                                                        ctypes.POINTER(Variant)]),
+        "fp8bq_grouped_linear": (i32, [vp, i32, i64, i64, i64, i64, vp, vp, vp, i32, i32, i32,
+                                       i32, i32, vp, vp, sz, vp]),
+        "fp8bq_grouped_linear_workspace_bytes": (sz, [i64, i64, i64, i64, i32, i32]),
         "fp8bq_status_string": (ctypes.c_char_p, [i32]),
         "fp8bq_abi_version": (i32, []),
     }
@@ -364,6 +368,39 @@ def fp8bq_grouped_gemm(a_q, a_s, w_q, w_s, counts, fmt="fp32", out_dtype=torch.b
                                              ctypes.byref(variant), _ptr(workspace), wsz,
                                              _stream(stream))
         _check(st, "fp8bq_grouped_gemm_variant")
+    return out
+
+
+def fp8bq_grouped_linear_workspace_bytes(E, M_max, N, K, fmt="ue8m0", out_dtype=torch.bfloat16):
+    return _lib.fp8bq_grouped_linear_workspace_bytes(E, M_max, N, K, _fmt(fmt),
+                                                     _dtype_code(out_dtype))
+
+
+def fp8bq_grouped_linear(x, w_q, w_s, counts, fmt="ue8m0", out_dtype=torch.bfloat16, out=None,
+                         workspace=None, stream=None):
+    """Grouped W8A8 linear layer: quantise the experts' occupied rows of x
+    [E*M_max, K] (bf16/fp16) and run the grouped GEMM with w_q [E, N, K],
+    w_s [E, N/128, K/128]; counts int32 [E] on the GPU."""
+    for t, n in ((x, "x"), (w_q, "w_q"), (w_s, "w_s"), (counts, "counts")):
+        _need(t, n)
+    if counts.dtype != torch.int32:
+        raise ValueError("counts must be int32")
+    E = counts.numel()
+    rows, K = x.shape
+    if E == 0 or rows % E:
+        raise ValueError("x rows must be E * M_max")
+    M_max = rows // E
+    N = w_q.numel() // (E * K)
+    out = _out(rows, N, out_dtype, x.device, out)
+    nbytes = fp8bq_grouped_linear_workspace_bytes(E, M_max, N, K, fmt, out.dtype)
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.fp8bq_grouped_linear(_ptr(x), _dtype_code(x.dtype), E, M_max, N, K, _ptr(counts),
+                                   _ptr(w_q), _ptr(w_s), 128, 128, 128, _fmt(fmt),
+                                   _dtype_code(out.dtype), _ptr(out), _ptr(workspace), wsz,
+                                   _stream(stream))
+    _check(st, "fp8bq_grouped_linear")
     return out
 
 

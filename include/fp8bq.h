@@ -214,6 +214,21 @@ fp8bq_status fp8bq_grouped_gemm_variant(int64_t E, int64_t M_max, int64_t N, int
                                         const fp8bq_variant* variant, void* workspace,
                                         size_t workspace_bytes, cudaStream_t stream);
 
+/* Grouped W8A8 linear layer: the activation quant of the experts' occupied
+ * rows followed by fp8bq_grouped_gemm, one call, two launches on `stream`.
+ * x: [E*M_max, K] bf16/fp16, 16-byte aligned; rows of expert e at or past
+ * counts[e] are not read.  The codes and scales go to the front of
+ * `workspace` (fp8bq_grouped_linear_workspace_bytes; counter prefix, codes,
+ * scales, split-K partials, as fp8bq_linear); their padding rows are not
+ * written.  Other arguments and preconditions as fp8bq_grouped_gemm. */
+fp8bq_status fp8bq_grouped_linear(const void* x, fp8bq_dtype x_dtype, int64_t E, int64_t M_max,
+                                  int64_t N, int64_t K, const int32_t* counts, const void* w_q,
+                                  const float* w_s, int group, int block_n, int block_k,
+                                  fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t fp8bq_grouped_linear_workspace_bytes(int64_t E, int64_t M_max, int64_t N, int64_t K,
+                                            fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype);
+
 /* The kernel shape fp8bq_grouped_gemm uses, and workspace sizes. */
 fp8bq_status fp8bq_select_grouped_variant(int64_t E, int64_t M_max, int64_t N, int64_t K,
                                           fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype,

@@ -143,3 +143,43 @@ def test_grouped_moe_decode_full_size_sampled(fp8bq, N, K):
         for r in sorted({r0, r0 + c - 1}):
             ref = oracle.gemm(qa, sa, qw, sw, True, rows=(r, 1))
             check_gemm(got[r:r + 1], ref, "bf16", f"moe {N}x{K} expert {e} row {r - r0}")
+
+
+@pytest.mark.parametrize("E,M_max,N,K,xdt", [(5, 136, 256, 1024, "bf16"), (4, 24, 384, 512, "fp16"),
+                                             (3, 260, 768, 2048, "bf16")])
+def test_grouped_linear(fp8bq, E, M_max, N, K, xdt):
+    """Quant of the occupied rows + grouped GEMM in one call.  The rows past
+    each count hold NaN: they must be neither read nor stored."""
+    rng = np.random.default_rng(E + M_max)
+    counts = rng.integers(0, M_max + 1, size=E).astype(np.int32)
+    counts[0] = M_max
+    if E > 2:
+        counts[1] = 0
+    xb = synth.moe_act(E, M_max, K)
+    if xdt == "fp16":
+        xb = synth.f32_to_f16_bits((xb.astype(np.uint32) << 16).view(np.float32))
+    nan_bits = 0x7FC0 if xdt == "bf16" else 0x7E00
+    for e in range(E):
+        xb[e * M_max + counts[e]:(e + 1) * M_max] = nan_bits
+    wb = synth.moe_weight_bf16(E, N, K)
+    tdt = torch.bfloat16 if xdt == "bf16" else torch.float16
+    wq = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        fp8bq.fp8bq_quant_weight(to_dev_bits(wb[e]), "ue8m0", q=wq[e], s=ws[e])
+    o = torch.full((E * M_max, N), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    fp8bq.fp8bq_grouped_linear(to_dev_bits(xb, tdt), wq, ws, torch.from_numpy(counts).cuda(),
+                               fmt="ue8m0", out_dtype=torch.bfloat16, out=o)
+    torch.cuda.synchronize()
+    assert fp8bq.fp8bq_device_status() == 0
+    got = o.float().cpu().numpy()
+    # the oracle quantises the occupied rows (padding rows set to 0 so that its
+    # finite-input precondition holds; they are not used)
+    xo = xb.copy()
+    for e in range(E):
+        xo[e * M_max + counts[e]:(e + 1) * M_max] = 0
+    qa, sa = oracle.quant_act(xo, oracle.BF16 if xdt == "bf16" else oracle.FP16, 128, True)
+    qs = [oracle.quant_weight(wb[e], oracle.BF16, 128, 128, True) for e in range(E)]
+    ref = oracle.grouped_gemm(qa, sa, np.stack([q for q, _ in qs]), np.stack([s for _, s in qs]),
+                              counts, True)
+    check_grouped(got, ref, counts, M_max, "bf16", f"grouped linear {E}x{M_max}x{N}x{K} {xdt}")
