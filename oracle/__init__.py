@@ -70,6 +70,12 @@ def lib():
         l.oracle_gemm.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, i32, i32, i64, i64, vp]
         l.oracle_gemm_elem.restype = dp
         l.oracle_gemm_elem.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32, i32, i32, i64, i64]
+        l.oracle_quant_rows.restype = i32
+        l.oracle_quant_rows.argtypes = [vp, i32, i64, i64, i32, vp, vp]
+        l.oracle_int8_value.restype = ctypes.c_int8
+        l.oracle_int8_value.argtypes = [ctypes.c_float, ctypes.c_float]
+        l.oracle_gemm_rowcol.restype = i32
+        l.oracle_gemm_rowcol.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, i64, i64, vp]
         l.oracle_calc_diff.restype = dp
         l.oracle_calc_diff.argtypes = [vp, vp, i64]
         _lib = l
@@ -211,6 +217,45 @@ def grouped_gemm(qa, sa, qw, sw, counts, ue8m0: bool, out=None, group: int = 128
         out[e * M_max:e * M_max + c] = gemm(qa, sa, np.ascontiguousarray(qw[e]),
                                             np.ascontiguousarray(sw[e]), ue8m0, group, bn, bk,
                                             rows=(e * M_max, c))
+    return out
+
+
+# ---------------------------------------------- per-token x per-channel --
+
+def quant_rows(x: np.ndarray, x_dtype: int, int8: bool = False):
+    """One scale per row ("用 Helion 为 vLLM 构建高性能可移植线性后端", 范围:
+    FP8_Dynamic and W8A8_INT8 use per-token activation and per-channel weight
+    scales).  x: [R,K] float32 (FP32) or uint16 bit patterns (BF16/FP16).
+    Returns (q [R,K]: uint8 e4m3 codes, or int8 when int8=True; s float32 [R])."""
+    x = np.ascontiguousarray(x)
+    R, K = x.shape
+    q = np.empty((R, K), dtype=np.int8 if int8 else np.uint8)
+    s = np.empty(R, dtype=np.float32)
+    rc = lib().oracle_quant_rows(_ptr(x), x_dtype, R, K, int(bool(int8)), _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quant_rows: bad arguments")
+    return q, s
+
+
+def int8_value(x: float, s: float) -> int:
+    return int(lib().oracle_int8_value(float(x), float(s)))
+
+
+def gemm_rowcol(qa, sa, qw, sw, int8: bool = False, rows=None) -> np.ndarray:
+    """fp64 reference of the per-token x per-channel GEMM:
+    (sa[m] * sw[n]) * sum_k dec(qa[m,k]) * dec(qw[n,k]); rows=(row0, count)."""
+    qa = np.ascontiguousarray(qa)
+    qw = np.ascontiguousarray(qw)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    row0, cnt = (0, M) if rows is None else rows
+    out = np.empty((cnt, N), dtype=np.float64)
+    rc = lib().oracle_gemm_rowcol(M, N, K, _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw),
+                                  int(bool(int8)), row0, cnt, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_gemm_rowcol: bad arguments")
     return out
 
 

@@ -243,6 +243,63 @@ double oracle_gemm_elem(int64_t M, int64_t N, int64_t K, const uint8_t* qa, cons
     return gemm_one(M, N, K, qa, sa, ue8m0, qw, sw, group, bn, bk, m, n);
 }
 
+/* --------------------------------------------- per-token x per-channel -- */
+
+static const float kInt8Max = 127.0f; /* symmetric int8 range */
+
+int8_t oracle_int8_value(float x, float s) {
+    float y = x / s; /* fp32 IEEE division */
+    if (y > kInt8Max) y = kInt8Max;
+    if (y < -kInt8Max) y = -kInt8Max;
+    return (int8_t)rintf(y); /* default rounding mode: half to even */
+}
+
+int oracle_quant_rows(const void* x, int x_dtype, int64_t R, int64_t K, int int8, uint8_t* q,
+                      float* s) {
+    if (R < 0 || K <= 0) return -1;
+    if (x_dtype != ORACLE_FP32 && x_dtype != ORACLE_BF16 && x_dtype != ORACLE_FP16) return -1;
+    for (int64_t r = 0; r < R; ++r) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = fabsf(load_elem(x, x_dtype, r * K + k));
+            if (v > amax) amax = v;
+        }
+        float m = amax > kEps ? amax : kEps;
+        float sc = m / (int8 ? kInt8Max : kFp8Max); /* fp32 IEEE division */
+        s[r] = sc;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = load_elem(x, x_dtype, r * K + k);
+            q[r * K + k] = int8 ? (uint8_t)oracle_int8_value(v, sc) : oracle_quant_value(v, sc);
+        }
+    }
+    return 0;
+}
+
+int oracle_gemm_rowcol(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const float* sa,
+                       const uint8_t* qw, const float* sw, int int8, int64_t row0, int64_t rows,
+                       double* out) {
+    if (M < 0 || N < 0 || K <= 0 || row0 < 0 || rows < 0 || row0 + rows > M) return -1;
+    init_dec_table();
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t m = row0 + r;
+        for (int64_t n = 0; n < N; ++n) {
+            double S;
+            if (int8) {
+                int64_t acc = 0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (int64_t)(int8_t)qa[m * K + k] * (int64_t)(int8_t)qw[n * K + k];
+                S = (double)acc; /* |acc| <= K * 127^2 < 2^53 */
+            } else {
+                S = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    S += dec_table[qa[m * K + k]] * dec_table[qw[n * K + k]];
+            }
+            out[r * N + n] = ((double)sa[m] * (double)sw[n]) * S;
+        }
+    }
+    return 0;
+}
+
 /* -------------------------------------------------------------- calc_diff -- */
 
 double oracle_calc_diff(const double* x, const double* y, int64_t n) {

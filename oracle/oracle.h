@@ -94,6 +94,39 @@ double oracle_gemm_elem(int64_t M, int64_t N, int64_t K, const uint8_t* qa, cons
                         int ue8m0, const uint8_t* qw, const float* sw, int group, int bn, int bk,
                         int64_t m, int64_t n);
 
+/* ------------------------------------------------------------------------
+ * Per-token x per-channel formats.  [HL] ("用 Helion 为 vLLM 构建高性能可移植
+ * 线性后端", 范围) lists, beside Block_FP8, FP8_Dynamic (FP8 codes, one scale
+ * per activation token and one per weight output channel) and W8A8_INT8 (the
+ * same scaling with INT8 codes).  The pages give no formula for them; the
+ * readings taken are the block path's with the block widened to a whole row:
+ *   e4m3: s = fp32(max(amax_row, 1e-10) / 448), q = e4m3_rne(clamp(x/s, +-448))
+ *   int8: s = fp32(max(amax_row, 1e-10) / 127), q = rne(clamp(x/s, +-127))
+ * x/s is the IEEE fp32 division, rne rounds half to even, int8 is symmetric
+ * (-128 is never produced).
+ * ------------------------------------------------------------------------ */
+
+/* One scale per row of x [R,K] (fp32, bf16 or fp16): per-token activation
+ * scales, or per-channel weight scales when x is a weight [N,K].
+ * q: [R,K] codes (e4m3, or int8 two's complement when int8 != 0); s: fp32 [R].
+ * Returns 0, or -1 on bad arguments. */
+int oracle_quant_rows(const void* x, int x_dtype, int64_t R, int64_t K, int int8, uint8_t* q,
+                      float* s);
+/* The int8 code of one element with scale s: rne(clamp(fp32(x / s), -127, 127)). */
+int8_t oracle_int8_value(float x, float s);
+
+/* Per-token x per-channel GEMM, rows [row0, row0+rows) of
+ *   ref[m,n] = (sa[m] * sw[n]) * S[m,n],   S[m,n] = sum_k dec(qa[m,k]) * dec(qw[n,k])
+ * (dec = e4m3 value, or the int8 integer).  S is exact in fp64 for the sizes
+ * used (e4m3 products are multiples of 2^-18 below 2^18, so a K <= 2^16 sum
+ * needs at most 52 bits; int8 sums are accumulated in int64), sa*sw is exact
+ * (two fp32 significands), so ref is the correctly rounded value of the exact
+ * product.  [HL] 内核实现: the quantised kernels apply the scales after the
+ * matmul's dot product. */
+int oracle_gemm_rowcol(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const float* sa,
+                       const uint8_t* qw, const float* sw, int int8, int64_t row0, int64_t rows,
+                       double* out);
+
 /* calc_diff of [DG §4.4]: 1 - 2*sum(x*y) / sum(x*x + y*y), in fp64. */
 double oracle_calc_diff(const double* x, const double* y, int64_t n);
 
