@@ -314,6 +314,53 @@ fp8bq_status check_grouped_args(int64_t E, int64_t M_max, int64_t N, int64_t K, 
     return FP8BQ_OK;
 }
 
+// Rowwise (per-token x per-channel) formats: K in whole 16-byte code rows,
+// N a multiple of 16 (16-byte aligned output rows for every dtype).
+fp8bq_status check_rowwise_args(int64_t M, int64_t N, int64_t K, int code, int out_dtype) {
+    if (M < 0 || N < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (code != FP8BQ_CODE_E4M3 && code != FP8BQ_CODE_INT8) return FP8BQ_ERR_INVALID_ARG;
+    if (out_dtype != FP8BQ_BF16 && out_dtype != FP8BQ_FP16 && out_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_INVALID_ARG;
+    if (K == 0 || K % 16 != 0 || N % 16 != 0) return FP8BQ_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    return FP8BQ_OK;
+}
+
+fp8bq_status check_rowwise_ptrs(const void* a_q, const float* a_s, const void* w_q,
+                                const float* w_s, const void* out) {
+    if (!a_q || !a_s || !w_q || !w_s || !out) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(a_s) & 3u) || (reinterpret_cast<uintptr_t>(w_s) & 3u))
+        return FP8BQ_ERR_ALIGNMENT;
+    return FP8BQ_OK;
+}
+
+// Kernel shape of a rowwise problem.  e4m3: the tile and split the block path
+// uses for UE8M0 scales (its table when it has the shape; the rowwise kernel
+// is the block-scaled one without factors), on the promotion-free kernel.
+// int8: swap-AB with the token tile covering M up to 128, otherwise as the
+// default variant.
+fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out_dtype,
+                              const std::string& device_name, int num_sms) {
+    fp8bq_variant v = code == FP8BQ_CODE_E4M3
+                          ? select_variant(M, N, K, FP8BQ_SCALE_UE8M0, out_dtype, device_name,
+                                           num_sms)
+                          : default_variant(M, N, K, FP8BQ_SCALE_FP32, num_sms);
+    v.mma_scale = 0;
+    if (v.kind == FP8BQ_KIND_SWAP_AB_64) v.kind = FP8BQ_KIND_SWAP_AB;
+    if (code == FP8BQ_CODE_INT8 && v.kind != FP8BQ_KIND_SWAP_AB) {
+        v.kind = FP8BQ_KIND_SWAP_AB;
+        v.block_n = 128;
+        const int64_t tiles = ((N + 127) / 128) * ((M + 127) / 128);
+        const bool whole_waves = tiles % num_sms == 0 || tiles >= 4 * int64_t(num_sms);
+        v.split = (!whole_waves && tiles * 8 * 4 <= static_cast<int64_t>(kCounterRegion)) ? 0 : 1;
+        v.grid = 0;
+    }
+    const int64_t G = (K + kGroup - 1) / kGroup;
+    if (v.split > G) v.split = static_cast<int>(G);
+    return v;
+}
+
 fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, const void* a_q,
                       const void* a_s, const void* w_q, const float* w_s, int fmt, int out_dtype,
                       void* out, void* ws, size_t ws_data_offset, DeviceInfo* d,
@@ -780,6 +827,158 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
     st = from_cuda(launch_quant_act(qa, stream));
     if (st != FP8BQ_OK) return st;
     return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, fmt, out_dtype, out, base,
+                    q_bytes + s_bytes, d, 1, stream);
+}
+
+// ----------------------------------------------- per-token x per-channel
+
+fp8bq_status fp8bq_quant_rows(const void* x, fp8bq_dtype x_dtype, int64_t R, int64_t K,
+                              fp8bq_code code, void* q, float* s, cudaStream_t stream) {
+    if (R < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16 && x_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_INVALID_ARG;
+    if (code != FP8BQ_CODE_E4M3 && code != FP8BQ_CODE_INT8) return FP8BQ_ERR_INVALID_ARG;
+    if (K == 0 || K % 16 != 0 || R > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    if (R == 0) return FP8BQ_OK;
+    if (!x || !q || !s) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u))
+        return FP8BQ_ERR_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    QuantRowsArgs a;
+    a.x = x;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.R = R;
+    a.K = K;
+    a.dtype = x_dtype;
+    a.int8 = code == FP8BQ_CODE_INT8;
+    return from_cuda(launch_quant_rows(a, stream));
+}
+
+size_t fp8bq_rowwise_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                             const fp8bq_variant* v) {
+    if (!v || check_rowwise_args(M, N, K, code, FP8BQ_BF16) != FP8BQ_OK) return 0;
+    DeviceInfo* d = nullptr;
+    int sms = 152;  // GB300 when no GPU is visible (host-only queries)
+    if (device_info(&d) == FP8BQ_OK) sms = d->num_sms;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *v, sms, &plan, 0, code == FP8BQ_CODE_INT8 ? 2 : 1)) return 0;
+    return plan.ws_bytes;
+}
+
+fp8bq_status fp8bq_select_rowwise_variant(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                          fp8bq_dtype out_dtype, fp8bq_variant* variant) {
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    fp8bq_status st = check_rowwise_args(M, N, K, code, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    std::string name;
+    int sms = 152;  // GB300 when no GPU is visible (host-only queries)
+    if (device_info(&d) == FP8BQ_OK) {
+        name = d->name;
+        sms = d->num_sms;
+    }
+    *variant = rowwise_variant(M, N, K, code, out_dtype, name, sms);
+    return FP8BQ_OK;
+}
+
+size_t fp8bq_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                     fp8bq_dtype out_dtype) {
+    fp8bq_variant v;
+    if (fp8bq_select_rowwise_variant(M, N, K, code, out_dtype, &v) != FP8BQ_OK) return 0;
+    return fp8bq_rowwise_variant_workspace_bytes(M, N, K, code, &v);
+}
+
+fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                        const float* a_s, const void* w_q, const float* w_s,
+                                        fp8bq_code code, fp8bq_dtype out_dtype, void* out,
+                                        const fp8bq_variant* variant, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_rowwise_args(M, N, K, code, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_rowwise_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *variant, d->num_sms, &plan, 0, code == FP8BQ_CODE_INT8 ? 2 : 1))
+        return FP8BQ_ERR_UNSUPPORTED;
+    st = check_ws(plan, workspace, workspace_bytes);
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out,
+                    workspace, 0, d, 0, stream);
+}
+
+fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                const float* a_s, const void* w_q, const float* w_s,
+                                fp8bq_code code, fp8bq_dtype out_dtype, void* out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_rowwise_args(M, N, K, code, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_rowwise_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = rowwise_variant(M, N, K, code, out_dtype, d->name, d->num_sms);
+    return fp8bq_gemm_rowwise_variant(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, &v,
+                                      workspace, workspace_bytes, stream);
+}
+
+size_t fp8bq_linear_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                            fp8bq_dtype out_dtype) {
+    if (check_rowwise_args(M, N, K, code, out_dtype) != FP8BQ_OK) return 0;
+    const size_t g = fp8bq_rowwise_workspace_bytes(M, N, K, code, out_dtype);
+    return kCounterRegion + align256(static_cast<size_t>(M * K)) +
+           align256(static_cast<size_t>(4 * M)) + (g ? g - kCounterRegion : 0);
+}
+
+fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N,
+                                  int64_t K, const void* w_q, const float* w_s, fp8bq_code code,
+                                  fp8bq_dtype out_dtype, void* out, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_rowwise_args(M, N, K, code, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    if (!x) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(x)) return FP8BQ_ERR_ALIGNMENT;
+    st = check_rowwise_ptrs(x, w_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8BQ_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const int rw = code == FP8BQ_CODE_INT8 ? 2 : 1;
+    const fp8bq_variant v = rowwise_variant(M, N, K, code, out_dtype, d->name, d->num_sms);
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan, 0, rw)) return FP8BQ_ERR_UNSUPPORTED;
+    // workspace: [counter prefix][codes][scales][split parts]
+    const size_t q_bytes = align256(static_cast<size_t>(M * K));
+    const size_t s_bytes = align256(static_cast<size_t>(4 * M));
+    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
+    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
+        return FP8BQ_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* a_q = base + kCounterRegion;
+    float* a_s = reinterpret_cast<float*>(base + kCounterRegion + q_bytes);
+    QuantRowsArgs qa;
+    qa.x = x;
+    qa.q = static_cast<uint8_t*>(a_q);
+    qa.s = a_s;
+    qa.R = M;
+    qa.K = K;
+    qa.dtype = x_dtype;
+    qa.int8 = rw == 2;
+    st = from_cuda(launch_quant_rows(qa, stream));
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out, base,
                     q_bytes + s_bytes, d, 1, stream);
 }
 

@@ -124,7 +124,9 @@ struct KArgs {
     int ue8m0;
     int out_dtype;
     int prefetch_w;  // weights may be read before the previous grid finishes
-    const float* w_s;  // weight scales [NB][G] (read directly by the fused-quant path)
+    const float* w_s;  // weight scales [NB][G] (read directly by the fused-quant path);
+                       // rowwise scales: one per weight row [N]
+    const float* s_tok;  // rowwise scales: one per token [M]
     void* out;
     float* partials;
     unsigned* counters;
@@ -282,6 +284,31 @@ __device__ __forceinline__ TileOrigin tile_origin(const KArgs& a, int tile) {
         o.tok0 = tok_base + tt * BM;
     }
     return o;
+}
+
+// Rowwise scales: v[j] *= s_tok[token] * w_s[weight row] for accumulator row
+// `row` and columns [c0, c0 + NC) of the tile (positions outside the tile's
+// stored range get 0 and are not stored).
+template <bool SWAP, int NC>
+__device__ __forceinline__ void rowwise_scale(const KArgs& a, const TileOrigin& o, int row,
+                                              int c0, float* v) {
+    if constexpr (SWAP) {
+        const int n = o.w0 + row;
+        const float sw = n < o.w_end ? __ldg(a.w_s + n) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            const int t = o.tok0 + c0 + j;
+            v[j] *= (t < o.tok_end ? __ldg(a.s_tok + t) : 0.0f) * sw;
+        }
+    } else {
+        const int m = o.tok0 + row;
+        const float st = m < o.tok_end ? __ldg(a.s_tok + m) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            const int n = o.w0 + c0 + j;
+            v[j] *= st * (n < o.w_end ? __ldg(a.w_s + n) : 0.0f);
+        }
+    }
 }
 
 __device__ __forceinline__ float ue8m0_value(uint32_t word, int kb) {
@@ -811,16 +838,25 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
 // into the same factor words as the unfused path (byte kb % 4) and write the
 // group's TMEM ring entry, each into its own lane quarter.  K % 128 suffices:
 // a group cut by a segment boundary is written when the segment ends.
-template <bool SWAP, int BN, int FQ = 0>
+//
+// RW (rowwise scales; FP8_Dynamic of "用 Helion 为 vLLM 构建高性能可移植线性
+// 后端", 范围: one fp32 scale per token and one per weight output channel):
+// no factors at all.  Warp 1 issues plain kind::f8f6f4 MMAs that accumulate a
+// whole segment in TMEM, warps 2-5 idle, and the epilogue multiplies each
+// finished sum by s_tok[m] * w_s[n] before it stores (split parts are summed
+// unscaled, then scaled once).  K needs only whole 16-byte rows: the last
+// slab's columns past K are TMA zero fill.
+template <bool SWAP, int BN, int FQ = 0, bool RW = false>
 struct MxCfg {
     static_assert(FQ == 0 || (SWAP && BN <= 32), "fused quant: swap-AB token tiles of 16/32");
+    static_assert(!(FQ && RW), "rowwise scales take quantised tokens");
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int X_BYTES = FQ ? BN * BK * 2 : 0;  // raw activation tile (fused quant)
     static constexpr int E_BYTES = FQ ? BN * 4 : 0;       // the tile rows' scale exponents
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + X_BYTES + E_BYTES;
     static constexpr int STAGES = FQ ? (BN <= 16 ? 9 : 7) : Cfg<SWAP, BN>::STAGES;
-    static constexpr int SRM = FQ ? 0 : SR;  // scale-ring slots (the fused path has none)
+    static constexpr int SRM = (FQ || RW) ? 0 : SR;  // scale-ring slots (fused, rowwise: none)
     static constexpr int NC = (BN + 31) / 32;       // factor columns of the MMA-N operand
     static constexpr int TOK_WORDS = SWAP ? BN : BM;  // token factor words per group
     static constexpr int WBLK = SWAP ? 1 : BN / BK;   // weight blocks per tile
@@ -832,9 +868,9 @@ struct MxCfg {
     static constexpr int RF = 8;                    // factor-ring entries (groups in flight)
     // accumulators: two (the next segment's MMAs overlap this one's read-out)
     // when they fit beside the factor ring
-    static constexpr int NACC = 2 * BN + RF * SF_COLS <= 512 ? 2 : 1;
+    static constexpr int NACC = (RW || 2 * BN + RF * SF_COLS <= 512) ? 2 : 1;
     static constexpr int SF_BASE = NACC * BN;       // after the accumulators
-    static constexpr int TMEM_NEED = SF_BASE + RF * SF_COLS;
+    static constexpr int TMEM_NEED = SF_BASE + (RW ? 0 : RF * SF_COLS);
     static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                      : TMEM_NEED <= 64  ? 64
                                      : TMEM_NEED <= 128 ? 128
@@ -854,15 +890,15 @@ struct MxCfg {
                   "scale slot layout");
 };
 
-template <bool SWAP, int BN, int FQ, bool GR>
-__global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
+template <bool SWAP, int BN, int FQ, bool GR, bool RW = false>
+__global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                    const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
                                                                   // (FQ: raw activations, 2-byte)
                    const __grid_constant__ CUtensorMap tm_sa,     // packed act words [G/4][Mp]
                    const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                    const KArgs a) {
-    using C = MxCfg<SWAP, BN, FQ>;
+    using C = MxCfg<SWAP, BN, FQ, RW>;
     constexpr int SR = C::SRM;  // scale-ring slots of this configuration
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -973,7 +1009,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                 const int row_n = SWAP ? o.tok0 : o.w0;
                 const int nb = o.w0 / BK;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!FQ && (kb == sg.kb0 || (kb & 3) == 0)) {
+                    if (!FQ && !RW && (kb == sg.kb0 || (kb & 3) == 0)) {
                         // the group's factors: BN token words, four weight scales
                         if (!mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag, a.status,
                                                tmo, code)) {
@@ -1066,7 +1102,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                 const uint32_t d_addr = tmem_base + static_cast<uint32_t>(acc * BN);
                 int cur = 0;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (kb == sg.kb0 || (kb & 3) == 0) {
+                    if (!RW && (kb == sg.kb0 || (kb & 3) == 0)) {
                         if (!mbar_wait_bounded(&ffull[r], rphase, abort_flag, a.status, tmo,
                                                code)) {
                             ok = false;
@@ -1085,20 +1121,32 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t a_addr = smem_addr(sA + stage * C::A_BYTES);
                     const uint32_t b_addr = smem_addr(sB + stage * C::B_BYTES);
-                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(C::SF_BASE + cur * C::SF_COLS);
-                    // factor byte kb % 4 of the group's words
-                    const uint32_t idesc = idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(kb & 3));
+                    if constexpr (RW) {
+                        // rowwise scales: the plain FP8 MMA, scaled in the epilogue
+                        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; ++kk)
-                        mma_mxf8(d_addr, smem_desc_k128_sw128(a_addr + kk * 32),
-                                 smem_desc_k128_sw128(b_addr + kk * 32), idesc, sfa, sfa + C::SF_B,
-                                 (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / 32; ++kk)
+                            mma_f8f6f4(d_addr, smem_desc_k128_sw128(a_addr + kk * 32),
+                                       smem_desc_k128_sw128(b_addr + kk * 32), idesc,
+                                       (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint32_t sfa =
+                            tmem_base + static_cast<uint32_t>(C::SF_BASE + cur * C::SF_COLS);
+                        // factor byte kb % 4 of the group's words
+                        const uint32_t idesc =
+                            idesc_mx_e4m3(BM, BN, static_cast<uint32_t>(kb & 3));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 32; ++kk)
+                            mma_mxf8(d_addr, smem_desc_k128_sw128(a_addr + kk * 32),
+                                     smem_desc_k128_sw128(b_addr + kk * 32), idesc, sfa,
+                                     sfa + C::SF_B, (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                    }
                     mma_commit(&empty[stage]);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if ((kb & 3) == 3 || kb == sg.kb1 - 1) mma_commit(&fempty[cur]);
+                    if (!RW && ((kb & 3) == 3 || kb == sg.kb1 - 1)) mma_commit(&fempty[cur]);
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -1180,7 +1228,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                     }
                 }
             }
-        } else {
+        } else if constexpr (!RW) {
             // -------------------------------------------------- factor writers
             int slot = 0, r = 0;
             uint32_t sphase = 0, rphase = 0;
@@ -1397,6 +1445,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                     float f[C::CHUNK];
 #pragma unroll
                     for (int j = 0; j < C::CHUNK; ++j) f[j] = __uint_as_float(v[j]);
+                    if constexpr (RW) rowwise_scale<SWAP, C::CHUNK>(a, o, row, c * C::CHUNK, f);
                     store_chunk(o, c * C::CHUNK, f);
                 }
             }
@@ -1445,6 +1494,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
                             }
                         }
                     }
+                    if constexpr (RW) rowwise_scale<SWAP, RC>(a, o, row, c0, r);
                     store_rc(o, c0, r);
                 }
             } else {
@@ -1461,6 +1511,7 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < C::CHUNK; ++j) r[j] = (p == 0) ? t[j] : r[j] + t[j];
                     }
+                    if constexpr (RW) rowwise_scale<SWAP, C::CHUNK>(a, o, row, c * C::CHUNK, r);
                     store_chunk(o, c * C::CHUNK, r);
                 }
             }
@@ -1475,6 +1526,233 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ>::THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- INT8 GEMM
+//
+// W8A8_INT8 ("用 Helion 为 vLLM 构建高性能可移植线性后端", 范围): int8 codes with
+// one scale per token and one per weight output channel,
+//   out[m,n] = s_tok[m] * w_s[n] * sum_k a[m,k] * w[n,k]    (int32 sums, exact).
+// tcgen05 has no integer kind on sm_103a, so the products run on the
+// warp-level int8 tensor-core instruction (mma.sync m16n8k32, s8 x s8 -> s32).
+// Tiles are swap-AB shaped, 128 weight rows x BN tokens:
+//   warp 0      TMA producer: per K slab the 128x128 weight tile and the
+//               BNx128 token tile (128-byte swizzle) into a STAGES-deep ring;
+//   warps 1-8   consumer warp w owns weight rows 16(w-1)..16(w-1)+15: per
+//               32-byte K step one ldmatrix.x4 of its rows, one per 16 tokens,
+//               and BN/8 MMAs into int32 registers.  At a segment's end it
+//               scales and stores its 16 x BN block, or writes it as an int32
+//               split part; the last part to arrive (ticket per warp and tile,
+//               as in the FP8 kernels) adds the parts in K order and stores.
+// The swizzle puts 16-byte chunk c of row r at chunk c ^ (r % 8), so the eight
+// row addresses of every ldmatrix fall in distinct bank groups.
+template <int BN>
+struct I8Cfg {
+    static constexpr int CW = 8;  // consumer warps
+    static constexpr int THREADS = 32 * (1 + CW);
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int SMEM = 1024 + BAR_OFF + 8 * 2 * STAGES + 16;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
+    gemm_i8_kernel(const __grid_constant__ CUtensorMap tm_w,  // weights [N, K] int8
+                   const __grid_constant__ CUtensorMap tm_t,  // tokens [M, K] int8
+                   const KArgs a) {
+    using C = I8Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                           // STAGES x [128 weight rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN tokens x 128 B]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* empty = full + C::STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::STAGES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::CW);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_t);
+    }
+    __syncthreads();
+    const uint64_t tmo = a.timeout_ns;
+    const int code = static_cast<int>(FP8BQ_ERR_DEVICE_TIMEOUT);
+
+    // Programmatic dependent launch, as in the FP8 kernels: only weight tiles
+    // may be read before the previous grid has finished.
+    int prefetched = 0;
+    if (a.prefetch_w && warp == 0 && lane == 0) {
+        WorkIter<false> wi;
+        wi.init(a);
+        Seg sg;
+        if (wi.next(a, sg)) {
+            const TileOrigin o = tile_origin<true, BN, BM, false>(a, sg.tile);
+            const int nslab = sg.kb1 - sg.kb0;
+            prefetched = nslab < C::STAGES ? nslab : C::STAGES;
+            for (int i = 0; i < prefetched; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+                tma_load_2d_hint(sA + i * C::A_BYTES, &tm_w, &full[i], (sg.kb0 + i) * BK, o.w0,
+                                 policy_evict_first());
+            }
+        }
+    }
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_t = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            WorkIter<false> wi;
+            wi.init(a);
+            Seg sg;
+            bool ok = true;
+            while (ok && wi.next(a, sg)) {
+                const TileOrigin o = tile_origin<true, BN, BM, false>(a, sg.tile);
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (fills >= prefetched) {
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                               tmo, code)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_w, &full[stage], kb * BK,
+                                         o.w0, pol_w);
+                    }
+                    tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_t, &full[stage], kb * BK,
+                                     o.tok0, pol_t);
+                    ++fills;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (long long f = fills > C::STAGES ? fills - C::STAGES : 0; f < fills; ++f)
+                mbar_wait_drain(&full[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1),
+                                tmo);
+        }
+    } else {
+        // ------------------------------------------------------- consumers
+        const int cw = warp - 1;  // weight rows 16 cw .. 16 cw + 15 of the tile
+        const int g = lane >> 2, t4 = lane & 3;
+        // ldmatrix row addresses: weight matrices (rows 0-7 | 8-15) x (bytes
+        // 0-15 | 16-31) of the K step; token matrices (tokens 0-7 | 8-15) x
+        // (bytes 0-15 | 16-31)
+        const int a_row = cw * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int a_half = lane >> 4;
+        const int b_row = (lane >> 4) * 8 + (lane & 7);
+        const int b_half = (lane >> 3) & 1;
+        int stage = 0;
+        uint32_t phase = 0;
+        WorkIter<false> wi;
+        wi.init(a);
+        Seg sg;
+        bool ok = true;
+        while (ok && wi.next(a, sg)) {
+            int acc[BN / 8][4];
+#pragma unroll
+            for (int j = 0; j < BN / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0;
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (!warp_wait(&full[stage], phase, abort_flag, a.status, tmo, code)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_base = smem_addr(sA + stage * C::A_BYTES) + a_row * BK;
+                const uint32_t b_base = smem_addr(sB + stage * C::B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 32; ++kk) {
+                    uint32_t af[4];
+                    ldmatrix_x4(af, a_base + (((2 * kk + a_half) ^ (a_row & 7)) << 4));
+#pragma unroll
+                    for (int j = 0; j < BN / 16; ++j) {
+                        const int tr = j * 16 + b_row;
+                        uint32_t bf[4];
+                        ldmatrix_x4(bf, b_base + tr * BK + (((2 * kk + b_half) ^ (tr & 7)) << 4));
+                        mma_s8_16x8x32(acc[2 * j], af, bf[0], bf[1]);
+                        mma_s8_16x8x32(acc[2 * j + 1], af, bf[2], bf[3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+
+            const TileOrigin o = tile_origin<true, BN, BM, false>(a, sg.tile);
+            // element (j, i) of this thread: weight row w0 + 16 cw + g + 8 (i / 2),
+            // token tok0 + 8 j + 2 t4 + (i % 2)
+            auto store = [&](int j, int i, int v) {
+                const int n = o.w0 + cw * 16 + g + 8 * (i >> 1);
+                const int t = o.tok0 + 8 * j + 2 * t4 + (i & 1);
+                if (n < o.w_end && t < o.tok_end)
+                    store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n,
+                               static_cast<float>(v) * (__ldg(a.s_tok + t) * __ldg(a.w_s + n)));
+            };
+            if (sg.nparts == 1) {
+#pragma unroll
+                for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) store(j, i, acc[j][i]);
+                continue;
+            }
+            // split parts: int32 [column][row] tiles in the workspace
+            constexpr int64_t TILE = BM * BN;
+            int* mine = reinterpret_cast<int*>(a.partials) + part_slot(a, sg.tile, sg.part) * TILE;
+            auto pidx = [&](int j, int i) {
+                return (8 * j + 2 * t4 + (i & 1)) * BM + cw * 16 + g + 8 * (i >> 1);
+            };
+#pragma unroll
+            for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) __stcg(mine + pidx(j, i), acc[j][i]);
+            __threadfence();
+            __syncwarp();
+            unsigned* ctr = a.counters + static_cast<int64_t>(sg.tile) * kCountersPerTile + cw;
+            unsigned prev = 0;
+            if (lane == 0) prev = atomicAdd(ctr, 1u);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
+            __threadfence();
+#pragma unroll
+            for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[j][i] = 0;
+            for (int p = 0; p < sg.nparts; ++p) {
+                const int* src = reinterpret_cast<const int*>(a.partials) + part_slot(a, sg.tile, p) * TILE;
+#pragma unroll
+                for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[j][i] += __ldcg(src + pidx(j, i));
+            }
+#pragma unroll
+            for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) store(j, i, acc[j][i]);
+            if (lane == 0) *ctr = 0u;  // ready for the next call
+        }
     }
 }
 
@@ -1547,10 +1825,18 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
             }
             mx_attr_done[dev] = 1;
         }
+        static int rw_attr_done[64] = {0};
+        if (p.rowwise && dev >= 0 && dev < 64 && !rw_attr_done[dev]) {
+            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0, false, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       MxCfg<SWAP, BN, 0, true>::SMEM);
+            if (err != cudaSuccess) return err;
+            rw_attr_done[dev] = 1;
+        }
     }
     const bool swap = SWAP;
     const uint64_t K = static_cast<uint64_t>(g.K);
-    const int G = static_cast<int>(g.K / BK);
+    const int G = static_cast<int>(p.rowwise ? (g.K + BK - 1) / BK : g.K / BK);
     // grouped: E stacked [N, K] weights (N % 128 == 0), E * m_max token rows
     const int64_t w_rows = g.E > 0 ? g.E * g.N : g.N;
     const int NB = static_cast<int>((w_rows + BK - 1) / BK);
@@ -1574,7 +1860,11 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
              encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(w_rows), BN);
     }
-    {
+    if (p.rowwise) {
+        // rowwise scales are read by the epilogue directly: no scale maps
+        tm_sa = tm_m;
+        tm_sw = tm_m;
+    } else {
         // activation scales: [cols][Mp] of 4-byte words; box = the tile's tokens of one column
         const cuuint64_t dims[2] = {Mp, static_cast<cuuint64_t>(g.ue8m0 ? (G + 3) / 4 : G)};
         const cuuint64_t strides[1] = {Mp * 4};
@@ -1621,6 +1911,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     a.tok_tile = swap ? BN : BM;
     a.counts = g.counts;
     a.w_s = g.w_s;
+    a.s_tok = p.rowwise ? static_cast<const float*>(g.a_s) : nullptr;
     a.out = g.out;
     // workspace: [tile counters: fixed kCounterRegion prefix] [fp32 partial tiles]
     a.counters = p.ws_bytes ? static_cast<unsigned*>(g.workspace) : nullptr;
@@ -1641,6 +1932,12 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if constexpr (WM == BM) {
+        if (p.rowwise) {
+            cfg.blockDim = dim3(MxCfg<SWAP, BN, 0, true>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0, true>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, false, true>, tm_m, tm_n,
+                                      tm_sa, tm_sw, a);
+        }
         if (p.mx) {
             if constexpr (SWAP && BN <= 32) {
                 if (g.x) {
@@ -1671,11 +1968,77 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM, false>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
+// INT8 rowwise GEMM (plan.rowwise == 2): swap-AB tiles of 128 weight rows x BN tokens.
+template <int BN>
+cudaError_t launch_i8(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
+    using C = I8Cfg<BN>;
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        err = cudaFuncSetAttribute(gemm_i8_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::SMEM);
+        if (err != cudaSuccess) return err;
+        attr_done[dev] = 1;
+    }
+    const uint64_t K = static_cast<uint64_t>(g.K);
+    const int G = static_cast<int>((g.K + BK - 1) / BK);
+    CUtensorMap tm_w, tm_t;
+    if (!encode_operand(&tm_w, g.w_q, K, static_cast<uint64_t>(g.N), BM) ||
+        !encode_operand(&tm_t, g.a_q, K, static_cast<uint64_t>(g.M), BN)) {
+        log_error("tensor-map encoding failed for the INT8 GEMM operands");
+        return cudaErrorInvalidValue;
+    }
+    KArgs a = {};
+    a.M = static_cast<int>(g.M);
+    a.N = static_cast<int>(g.N);
+    a.G = G;
+    a.NB = static_cast<int>((g.N + BK - 1) / BK);
+    a.swap = 1;
+    a.tiles_tok = p.tiles_tok;
+    a.tiles_w = p.tiles_w;
+    a.tiles_e = p.tiles_tok * p.tiles_w;
+    a.tiles = a.tiles_e;
+    a.split = p.split;
+    a.num_items = p.num_items;
+    a.units = static_cast<long long>(a.tiles) * G;
+    a.out_dtype = g.out_dtype;
+    a.prefetch_w = g.prefetch_w;
+    a.tok_tile = BN;
+    a.w_s = g.w_s;
+    a.s_tok = static_cast<const float*>(g.a_s);
+    a.out = g.out;
+    a.counters = p.ws_bytes ? static_cast<unsigned*>(g.workspace) : nullptr;
+    a.partials = p.ws_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(g.workspace) +
+                                                       kCounterRegion + g.ws_data_offset)
+                            : nullptr;
+    a.status = g.status;
+    a.timeout_ns = g.timeout_ns;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_i8_kernel<BN>, tm_w, tm_t, a);
+}
+
 }  // namespace
 
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
-                    GemmPlan* p, int64_t experts) {
-    const int G = static_cast<int>(K / BK);
+                    GemmPlan* p, int64_t experts, int rowwise) {
+    // K slabs (rowwise: the last one may be partly past K, read as zeros)
+    const int G = static_cast<int>(rowwise ? (K + BK - 1) / BK : K / BK);
+    if (rowwise && (experts != 0 || v.mma_scale != 0 || v.kind == FP8BQ_KIND_SWAP_AB_64))
+        return false;
+    // INT8 (rowwise == 2): swap-AB tiles only
+    if (rowwise == 2 && v.kind != FP8BQ_KIND_SWAP_AB) return false;
     const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
     const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
     if (v.kind != FP8BQ_KIND_SWAP_AB && v.kind != FP8BQ_KIND_NORMAL &&
@@ -1698,6 +2061,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (experts < 0 || experts > (1 << 20)) return false;
     if (experts > 0 && (v.split == 0 || N % BK != 0 || M % 4 != 0)) return false;
     p->experts = static_cast<int>(experts);
+    p->rowwise = rowwise;
     p->mx = v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;
@@ -1734,6 +2098,15 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
+    if (p.rowwise == 2) {
+        switch (p.bn) {
+            case 16: return launch_i8<16>(p, g, stream);
+            case 32: return launch_i8<32>(p, g, stream);
+            case 64: return launch_i8<64>(p, g, stream);
+            case 128: return launch_i8<128>(p, g, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (p.kind == FP8BQ_KIND_SWAP_AB_64) {
         switch (p.bn) {
             case 16: return launch_bn<true, 16, 64>(p, g, stream);

@@ -14,6 +14,7 @@ namespace fp8bq {
 constexpr int kGroup = 128;  // activation group / weight block edge
 constexpr float kEps = 1e-10f;
 constexpr float kFp8Max = 448.0f;
+constexpr float kInt8Max = 127.0f;  // symmetric int8 codes
 
 inline int64_t pad_rows4(int64_t m) { return (m + 3) / 4 * 4; }
 
@@ -53,6 +54,17 @@ struct QuantWeightArgs {
 };
 cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream);
 
+// One scale per row of x [R, K] (per-token activations, per-channel weights).
+struct QuantRowsArgs {
+    const void* x;
+    uint8_t* q;  // [R, K] e4m3 or int8 codes
+    float* s;    // [R]
+    int64_t R, K;
+    int dtype;   // fp8bq_dtype of x
+    int int8;    // codes are int8 (else e4m3)
+};
+cudaError_t launch_quant_rows(const QuantRowsArgs& a, cudaStream_t stream);
+
 // ----------------------------------------------------------------- GEMM
 
 struct GemmPlan {
@@ -65,6 +77,8 @@ struct GemmPlan {
     int tiles_w;   // weight tiles
     int num_items; // tiles * split
     int experts;   // grouped: experts (0: one plain problem)
+    int rowwise;   // one scale per token and per weight row: 1 e4m3 (gemm_mx_kernel, RW),
+                   // 2 int8 (gemm_i8_kernel); 0 block scales
     size_t ws_bytes;
 };
 
@@ -72,8 +86,11 @@ struct GemmPlan {
 // returns false if the variant is not supported.  With experts > 0 the plan
 // is for a grouped problem: `experts` independent (M, N, K) problems whose
 // token rows, weight rows and outputs are stacked (M is the rows per expert).
+// With rowwise != 0 the plan is for the rowwise-scaled GEMM (1: e4m3, 2:
+// int8; 128-row tiles, promotion-free; K in whole 16-byte rows, the last
+// slab zero-filled).
 bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int num_sms,
-                    GemmPlan* plan, int64_t experts = 0);
+                    GemmPlan* plan, int64_t experts = 0, int rowwise = 0);
 
 struct GemmLaunch {
     int64_t M, N, K;
@@ -102,6 +119,8 @@ struct GemmLaunch {
     int64_t E = 0;
     int64_t m_max = 0;
     const int* counts = nullptr;
+    // Rowwise scales (plan.rowwise): a_s is fp32 [M] (one per token), w_s
+    // fp32 [N] (one per weight row).
 };
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmLaunch& g, cudaStream_t stream);
 

@@ -297,4 +297,29 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------ warp-level int8 tensor core
+
+// Four 8x8 matrices of 16-byte rows from shared memory: lanes 8i..8i+7 give
+// the row addresses of matrix i; thread T receives bytes 4(T%4)..4(T%4)+3 of
+// row T/4 of matrix i in r[i].
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+
+// D (16x8 s32) += A (16x32 s8, row-major) * B (32x8 s8, column-major).
+//   a[0]: row g, k 4t..4t+3      a[1]: row g+8, k 4t..      a[2], a[3]: k + 16
+//   b0:   k 4t..4t+3, column g   b1: k + 16
+//   d[0], d[1]: row g, columns 2t, 2t+1   d[2], d[3]: row g+8
+// (g = lane / 4, t = lane % 4)
+__device__ __forceinline__ void mma_s8_16x8x32(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 }  // namespace fp8bq

@@ -198,6 +198,90 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs
     }
 }
 
+// ------------------------------------------------------------ per-row quant
+//
+// FP8_Dynamic / W8A8_INT8 ("用 Helion 为 vLLM 构建高性能可移植线性后端", 范围):
+// one scale per row, s = max(amax_row, eps) / 448 (e4m3) or / 127 (int8),
+// codes = round-half-even of clamp(x / s).  One CTA per row: 256 threads take
+// 16-element chunks round robin (16 B bf16 loads, 16 B code stores), keep up
+// to kRowCache chunks in registers between the amax pass and the code pass and
+// re-read any further ones (an L2 hit: the row was just read).
+constexpr int kRowThreads = 256;
+constexpr int kRowCache = 5;  // rows up to 5 * 256 * 16 = 20480 elements stay in registers
+
+template <bool kInt8>
+__device__ __forceinline__ uint4 encode16(const float (&f)[16], float s) {
+    uint32_t c[4];
+    if constexpr (kInt8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float y = fminf(fmaxf(__fdiv_rn(f[4 * i + j], s), -kInt8Max), kInt8Max);
+                w |= (static_cast<uint32_t>(__float2int_rn(y)) & 0xFFu) << (8 * j);
+            }
+            c[i] = w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = cvt2_e4m3(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s)) |
+                   (cvt2_e4m3(__fdiv_rn(f[4 * i + 2], s), __fdiv_rn(f[4 * i + 3], s)) << 16);
+    }
+    return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
+template <typename T, bool kInt8>
+__global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const QuantRowsArgs a) {
+    __shared__ float warp_max[kRowThreads / 32];
+    const int t = threadIdx.x;
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const T* x = static_cast<const T*>(a.x) + row * a.K;
+    uint8_t* q = a.q + row * a.K;
+    const int nc = static_cast<int>(a.K / 16);
+
+    float f[kRowCache][16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kRowCache; ++i) {
+        const int c = t + i * kRowThreads;
+        if (c < nc) {
+            load16<T>(x + static_cast<int64_t>(c) * 16, f[i]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[i][j]));
+        }
+    }
+    for (int c = t + kRowCache * kRowThreads; c < nc; c += kRowThreads) {
+        float g[16];
+        load16<T>(x + static_cast<int64_t>(c) * 16, g);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(g[j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((t & 31) == 0) warp_max[t >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < kRowThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
+    const float s = __fdiv_rn(fmaxf(amax, kEps), kInt8 ? kInt8Max : kFp8Max);
+    if (t == 0) a.s[row] = s;
+
+#pragma unroll
+    for (int i = 0; i < kRowCache; ++i) {
+        const int c = t + i * kRowThreads;
+        if (c < nc) *reinterpret_cast<uint4*>(q + static_cast<int64_t>(c) * 16) = encode16<kInt8>(f[i], s);
+    }
+    for (int c = t + kRowCache * kRowThreads; c < nc; c += kRowThreads) {
+        float g[16];
+        load16<T>(x + static_cast<int64_t>(c) * 16, g);
+        *reinterpret_cast<uint4*>(q + static_cast<int64_t>(c) * 16) = encode16<kInt8>(g, s);
+    }
+}
+
 // ------------------------------------------------------ bounded-wait test
 
 __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
@@ -245,6 +329,30 @@ cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream) {
     else
         quant_weight_kernel<__half><<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+namespace {
+template <bool kInt8>
+cudaError_t launch_rows(const QuantRowsArgs& a, cudaLaunchConfig_t* cfg) {
+    if (a.dtype == FP8BQ_FP32) return cudaLaunchKernelEx(cfg, quant_rows_kernel<float, kInt8>, a);
+    if (a.dtype == FP8BQ_BF16)
+        return cudaLaunchKernelEx(cfg, quant_rows_kernel<__nv_bfloat16, kInt8>, a);
+    return cudaLaunchKernelEx(cfg, quant_rows_kernel<__half, kInt8>, a);
+}
+}  // namespace
+
+cudaError_t launch_quant_rows(const QuantRowsArgs& a, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.R));
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return a.int8 ? launch_rows<true>(a, &cfg) : launch_rows<false>(a, &cfg);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream) {

@@ -24,6 +24,7 @@ STATUS_NAMES = {
     7: "FP8BQ_ERR_DEVICE_TIMEOUT", 8: "FP8BQ_ERR_CUDA",
 }
 SCALE_FP32, SCALE_UE8M0 = 0, 1
+CODE_E4M3, CODE_INT8 = 0, 1
 BF16, FP16, FP32 = 0, 1, 2
 KIND_NORMAL, KIND_SWAP_AB, KIND_SWAP_AB_64 = 0, 1, 2
 _KIND_NAMES = {KIND_NORMAL: "normal", KIND_SWAP_AB: "swap", KIND_SWAP_AB_64: "swap64"}
@@ -37,7 +38,10 @@ EXPORTS = (
     "fp8bq_gemm_noalloc", "fp8bq_grouped_gemm", "fp8bq_grouped_gemm_variant",
     "fp8bq_select_grouped_variant", "fp8bq_grouped_gemm_workspace_bytes",
     "fp8bq_grouped_variant_workspace_bytes", "fp8bq_grouped_linear",
-    "fp8bq_grouped_linear_workspace_bytes",
+    "fp8bq_grouped_linear_workspace_bytes", "fp8bq_quant_rows", "fp8bq_gemm_rowwise",
+    "fp8bq_gemm_rowwise_variant", "fp8bq_select_rowwise_variant",
+    "fp8bq_rowwise_workspace_bytes", "fp8bq_rowwise_variant_workspace_bytes",
+    "fp8bq_linear_rowwise", "fp8bq_linear_rowwise_workspace_bytes",
 )
 
 
@@ -98,6 +102,18 @@ def _load():
         "fp8bq_grouped_linear": (i32, [vp, i32, i64, i64, i64, i64, vp, vp, vp, i32, i32, i32,
                                        i32, i32, vp, vp, sz, vp]),
         "fp8bq_grouped_linear_workspace_bytes": (sz, [i64, i64, i64, i64, i32, i32]),
+        "fp8bq_quant_rows": (i32, [vp, i32, i64, i64, i32, vp, vp, vp]),
+        "fp8bq_gemm_rowwise": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp]),
+        "fp8bq_gemm_rowwise_variant": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32, vp,
+                                             ctypes.POINTER(Variant), vp, sz, vp]),
+        "fp8bq_select_rowwise_variant": (i32, [i64, i64, i64, i32, i32,
+                                               ctypes.POINTER(Variant)]),
+        "fp8bq_rowwise_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "fp8bq_rowwise_variant_workspace_bytes": (sz, [i64, i64, i64, i32,
+                                                       ctypes.POINTER(Variant)]),
+        "fp8bq_linear_rowwise": (i32, [vp, i32, i64, i64, i64, vp, vp, i32, i32, vp, vp, sz,
+                                       vp]),
+        "fp8bq_linear_rowwise_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "fp8bq_status_string": (ctypes.c_char_p, [i32]),
         "fp8bq_abi_version": (i32, []),
     }
@@ -401,6 +417,100 @@ def fp8bq_grouped_linear(x, w_q, w_s, counts, fmt="ue8m0", out_dtype=torch.bfloa
                                    _dtype_code(out.dtype), _ptr(out), _ptr(workspace), wsz,
                                    _stream(stream))
     _check(st, "fp8bq_grouped_linear")
+    return out
+
+
+# ------------------------------------------------ per-token x per-channel
+
+def _code(code) -> int:
+    if isinstance(code, str):
+        return {"e4m3": CODE_E4M3, "int8": CODE_INT8}[code]
+    return int(code)
+
+
+def fp8bq_quant_rows(x: torch.Tensor, code="e4m3", q=None, s=None, stream=None):
+    """One scale per row of x [R,K] (bf16/fp16/fp32): per-token activation or
+    per-channel weight quant -> (q [R,K] uint8 e4m3 or int8 codes, s fp32 [R])."""
+    _need(x, "x")
+    R, K = x.shape
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.int8 if _code(code) == CODE_INT8 else torch.uint8,
+                        device=x.device)
+    if s is None:
+        s = torch.empty(R, dtype=torch.float32, device=x.device)
+    st = _lib.fp8bq_quant_rows(_ptr(x), _dtype_code(x.dtype), R, K, _code(code), _ptr(q),
+                               _ptr(s), _stream(stream))
+    _check(st, "fp8bq_quant_rows")
+    return q, s
+
+
+def fp8bq_select_rowwise_variant(M: int, N: int, K: int, code="e4m3",
+                                 out_dtype=torch.bfloat16) -> dict:
+    v = Variant()
+    st = _lib.fp8bq_select_rowwise_variant(M, N, K, _code(code), _dtype_code(out_dtype),
+                                           ctypes.byref(v))
+    _check(st, "fp8bq_select_rowwise_variant")
+    return v.as_dict()
+
+
+def fp8bq_rowwise_workspace_bytes(M, N, K, code="e4m3", out_dtype=torch.bfloat16) -> int:
+    return _lib.fp8bq_rowwise_workspace_bytes(M, N, K, _code(code), _dtype_code(out_dtype))
+
+
+def fp8bq_rowwise_variant_workspace_bytes(M, N, K, code, variant: Variant) -> int:
+    return _lib.fp8bq_rowwise_variant_workspace_bytes(M, N, K, _code(code),
+                                                      ctypes.byref(variant))
+
+
+def fp8bq_gemm_rowwise(a_q, a_s, w_q, w_s, code="e4m3", out_dtype=torch.bfloat16, out=None,
+                       workspace=None, variant: Variant | None = None, stream=None):
+    """Rowwise-scaled GEMM: a_q [M,K] codes, a_s fp32 [M]; w_q [N,K], w_s fp32 [N]."""
+    for t, n in ((a_q, "a_q"), (a_s, "a_s"), (w_q, "w_q"), (w_s, "w_s")):
+        _need(t, n)
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    out = _out(M, N, out_dtype, a_q.device, out)
+    if variant is None:
+        nbytes = fp8bq_rowwise_workspace_bytes(M, N, K, code, out.dtype)
+    else:
+        nbytes = fp8bq_rowwise_variant_workspace_bytes(M, N, K, code, variant)
+    if workspace is None:
+        workspace = _workspace(nbytes, a_q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant is None:
+        st = _lib.fp8bq_gemm_rowwise(M, N, K, _ptr(a_q), _ptr(a_s), _ptr(w_q), _ptr(w_s),
+                                     _code(code), _dtype_code(out.dtype), _ptr(out),
+                                     _ptr(workspace), wsz, _stream(stream))
+    else:
+        st = _lib.fp8bq_gemm_rowwise_variant(M, N, K, _ptr(a_q), _ptr(a_s), _ptr(w_q),
+                                             _ptr(w_s), _code(code), _dtype_code(out.dtype),
+                                             _ptr(out), ctypes.byref(variant), _ptr(workspace),
+                                             wsz, _stream(stream))
+    _check(st, "fp8bq_gemm_rowwise")
+    return out
+
+
+def fp8bq_linear_rowwise_workspace_bytes(M, N, K, code="e4m3", out_dtype=torch.bfloat16):
+    return _lib.fp8bq_linear_rowwise_workspace_bytes(M, N, K, _code(code), _dtype_code(out_dtype))
+
+
+def fp8bq_linear_rowwise(x, w_q, w_s, code="e4m3", out_dtype=torch.bfloat16, out=None,
+                         workspace=None, stream=None):
+    """Rowwise W8A8 linear layer: per-token quant of x [M,K] (bf16/fp16) and
+    the rowwise GEMM with w_q [N,K], w_s fp32 [N], in one call."""
+    for t, n in ((x, "x"), (w_q, "w_q"), (w_s, "w_s")):
+        _need(t, n)
+    M, K = x.shape
+    N = w_q.shape[0]
+    out = _out(M, N, out_dtype, x.device, out)
+    nbytes = fp8bq_linear_rowwise_workspace_bytes(M, N, K, code, out.dtype)
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.fp8bq_linear_rowwise(_ptr(x), _dtype_code(x.dtype), M, N, K, _ptr(w_q), _ptr(w_s),
+                                   _code(code), _dtype_code(out.dtype), _ptr(out),
+                                   _ptr(workspace), wsz, _stream(stream))
+    _check(st, "fp8bq_linear_rowwise")
     return out
 
 

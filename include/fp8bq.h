@@ -275,6 +275,66 @@ fp8bq_status fp8bq_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* a_q
                                 int block_n, int block_k, fp8bq_scale_fmt fmt,
                                 fp8bq_dtype out_dtype, void* out, cudaStream_t stream);
 
+/* ------------------------------------- per-token x per-channel formats
+ *
+ * "用 Helion 为 vLLM 构建高性能可移植线性后端", 范围, lists two more W8A8
+ * formats beside Block_FP8: FP8_Dynamic (FP8 codes, one scale per activation
+ * token and one per weight output channel) and W8A8_INT8 (the same scaling
+ * with INT8 codes).  The pages give no formulas; the rule used is the block
+ * path's with the block widened to a whole row:
+ *   s[r] = fp32(max(amax of row r, 1e-10) / Q), Q = 448 (e4m3) or 127 (int8)
+ *   q    = round-half-even(clamp(x / s, -Q, Q))   (IEEE fp32 division)
+ *   out[m,n] = a_s[m] * w_s[n] * sum_k dec(a_q[m,k]) * dec(w_q[n,k])
+ * Shapes: K > 0 and K % 16 == 0 (16-byte code rows), N % 16 == 0 for the
+ * GEMM (FP8BQ_ERR_SHAPE otherwise); M (or R) >= 0 arbitrary, 0 is a no-op. */
+typedef enum {
+    FP8BQ_CODE_E4M3 = 0, /* FP8_Dynamic: float8_e4m3fn codes, tcgen05 FP8 MMA */
+    FP8BQ_CODE_INT8 = 1  /* W8A8_INT8: two's-complement int8 codes in [-127, 127]; exact
+                          * int32 sums on the warp-level int8 tensor-core MMA (sm_103a's
+                          * tcgen05 has no integer kind) */
+} fp8bq_code;
+
+/* One scale per row of x [R,K] (bf16, fp16 or fp32, 16-byte aligned):
+ * per-token activation scales, or per-channel scales when x is a weight
+ * [N,K].  q: [R,K] codes (16-byte aligned); s: fp32 [R] (4-byte aligned).
+ * One launch on `stream`. */
+fp8bq_status fp8bq_quant_rows(const void* x, fp8bq_dtype x_dtype, int64_t R, int64_t K,
+                              fp8bq_code code, void* q, float* s, cudaStream_t stream);
+
+/* Rowwise-scaled GEMM: a_q [M,K] codes with a_s fp32 [M]; w_q [N,K] codes
+ * with w_s fp32 [N]; out [M,N] bf16/fp16/fp32.  The workspace follows the
+ * rules of fp8bq_gemm_workspace_bytes (counter prefix, then split parts).
+ * The kernel shape comes from fp8bq_select_rowwise_variant. */
+fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                const float* a_s, const void* w_q, const float* w_s,
+                                fp8bq_code code, fp8bq_dtype out_dtype, void* out,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+/* The same with an explicit kernel shape.  e4m3: swap-AB (block_n 16..128) or
+ * normal (128, 256) tiles, split >= 0 (0 = stream-K), mma_scale 0.  int8:
+ * swap-AB only, block_n 16, 32, 64 or 128.  Others: FP8BQ_ERR_UNSUPPORTED. */
+fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                        const float* a_s, const void* w_q, const float* w_s,
+                                        fp8bq_code code, fp8bq_dtype out_dtype, void* out,
+                                        const fp8bq_variant* variant, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+fp8bq_status fp8bq_select_rowwise_variant(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                          fp8bq_dtype out_dtype, fp8bq_variant* variant);
+size_t fp8bq_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                     fp8bq_dtype out_dtype);
+size_t fp8bq_rowwise_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                             const fp8bq_variant* variant);
+
+/* The rowwise linear layer: fp8bq_quant_rows of x [M,K] (bf16/fp16) followed
+ * by fp8bq_gemm_rowwise, one call, two launches on `stream`.  The codes and
+ * scales go to the front of `workspace`: [65536-byte counter prefix][codes
+ * M*K][scales 4*M][split parts], each part at a 256-byte aligned offset. */
+fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N,
+                                  int64_t K, const void* w_q, const float* w_s, fp8bq_code code,
+                                  fp8bq_dtype out_dtype, void* out, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+size_t fp8bq_linear_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
+                                            fp8bq_dtype out_dtype);
+
 /* ------------------------------------------------------------ host queries */
 
 /* The variant fp8bq_gemm would run for this shape (host only, no GPU work):

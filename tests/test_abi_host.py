@@ -213,3 +213,59 @@ def test_grouped_variant_selection_and_workspace():
     # stream-K is not offered for grouped problems
     assert fp8bq.fp8bq_grouped_variant_workspace_bytes(
         2, 8, 256, 4096, fp8bq.make_variant("swap", 16, 0)) == 0
+
+
+def call_rowwise(M=16, N=128, K=256, ptr=4096, sptr=4096, code=0, out=0):
+    lib = fp8bq.lib()
+    p, s = ctypes.c_void_p(ptr), ctypes.c_void_p(sptr)
+    return lib.fp8bq_gemm_rowwise(M, N, K, p, s, p, s, code, out, p, None, 0, None)
+
+
+def test_rowwise_argument_errors_on_host():
+    assert call_rowwise(K=100) == 2        # K % 16
+    assert call_rowwise(K=0) == 2
+    assert call_rowwise(N=120) == 2        # N % 16
+    assert call_rowwise(M=-1) == 1
+    assert call_rowwise(code=2) == 1
+    assert call_rowwise(out=3) == 1
+    assert call_rowwise(ptr=4100) == 3     # codes / out not 16-byte aligned
+    assert call_rowwise(sptr=4098) == 3    # scales not 4-byte aligned
+    assert call_rowwise(ptr=0) == 1
+    assert call_rowwise(M=0) == 0
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(4096)
+    assert lib.fp8bq_quant_rows(p, 0, 4, 100, 0, p, p, None) == 2
+    assert lib.fp8bq_quant_rows(p, 3, 4, 128, 0, p, p, None) == 1      # bad dtype
+    assert lib.fp8bq_quant_rows(p, 2, 4, 128, 5, p, p, None) == 1      # bad code
+    assert lib.fp8bq_quant_rows(ctypes.c_void_p(4104), 0, 4, 128, 0, p, p, None) == 3
+    assert lib.fp8bq_quant_rows(p, 0, 0, 128, 1, p, p, None) == 0
+    # the rowwise linear layer takes bf16/fp16 input only
+    assert lib.fp8bq_linear_rowwise(p, 2, 4, 128, 128, p, p, 0, 0, p, p, 1 << 20, None) == 4
+
+
+def test_rowwise_variant_selection_and_workspace():
+    # e4m3: promotion-free swap-AB at decode sizes; no block-scaled MMA
+    v = fp8bq.fp8bq_select_rowwise_variant(8, 7168, 18432, "e4m3", "bf16")
+    assert v["kind"] == "swap" and v["mma_scale"] == 0
+    v = fp8bq.fp8bq_select_rowwise_variant(2048, 7168, 18432, "e4m3", "bf16")
+    assert v["kind"] == "normal" and v["mma_scale"] == 0
+    # int8: swap-AB tiles at every M
+    for M in (1, 48, 2048):
+        v = fp8bq.fp8bq_select_rowwise_variant(M, 4096, 7168, "int8", "bf16")
+        assert v["kind"] == "swap" and v["mma_scale"] == 0
+    # a K that is not a multiple of 128 counts its partial last slab
+    v4 = fp8bq.make_variant("swap", 16, 4)
+    tiles = 7168 // 128
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(8, 7168, 1040, "e4m3", v4) == \
+        65536 + tiles * 4 * 128 * 16 * 4
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(8, 7168, 1040, "int8", v4) == \
+        65536 + tiles * 4 * 128 * 16 * 4
+    # more splits than the 9 K slabs of K = 1040, and int8 has no normal tiles
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(
+        8, 7168, 1040, "e4m3", fp8bq.make_variant("swap", 16, 10)) == 0
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(
+        256, 7168, 1024, "int8", fp8bq.make_variant("normal", 128, 2)) == 0
+    # the linear layer's workspace: prefix + codes + scales + parts
+    g = fp8bq.fp8bq_rowwise_workspace_bytes(8, 7168, 18432, "int8", "bf16")
+    lin = fp8bq.fp8bq_linear_rowwise_workspace_bytes(8, 7168, 18432, "int8", "bf16")
+    assert lin == 65536 + 8 * 18432 + 256 + (g - 65536 if g else 0)
