@@ -21,6 +21,11 @@ down N=7168 K=2048), tokens routed top-8 of 256 experts with a seeded skewed
 popularity, a decode batch (128 tokens) and a prefill chunk (4096 tokens);
 per problem one fp8bq_grouped_linear call (quant of the occupied rows +
 grouped GEMM).
+
+`--workload rowwise --code e4m3|int8` times the per-token x per-channel
+formats (FP8_Dynamic, W8A8_INT8) on the decode sweep's problems, one
+fp8bq_linear_rowwise per problem, and the rowwise GEMM alone at M = 2048 and
+4096 on the same (N,K).
 """
 from __future__ import annotations
 
@@ -481,6 +486,191 @@ def moe_oracle_sample():
                            "linearly to each problem's token rows")
 
 
+# ----------------------------------------------- rowwise (per-token x per-channel)
+
+ROWWISE_WORKLOAD = ("rowwise {code}: decode sweep (N,K) in {{(7168,18432),(18432,7168),(4096,7168)}} "
+                    "x M in {{1,2,4,8,16,24,32,48,64,96,128}}; act bf16 N(0,1), 1% channels x30 "
+                    "-> per-token quant; weights bf16 N(0,0.02) per-channel quant; bf16 out; "
+                    "fp8bq_linear_rowwise per problem")
+ROWWISE_PREFILL_M = (2048, 4096)
+
+
+def rowwise_gemm_bytes(M, N, K):
+    """Algorithmic bytes of one rowwise GEMM: codes of A and W (1 byte each),
+    one fp32 scale per token and per weight row, bf16 output."""
+    return M * K + N * K + 4 * M + 4 * N + 2 * M * N
+
+
+def rowwise_step_bytes(M, N, K):
+    return 2 * M * K + N * K + 4 * N + 2 * M * N
+
+
+def run_gpu_rowwise(args, rank, world):
+    import torch
+
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq
+
+    code = args.code
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    probs = problems()
+    w_q, w_s = {}, {}
+    for (N, K) in synth.DECODE_NK:
+        wd = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
+        q, s = fp8bq.fp8bq_quant_rows(wd, code)
+        del wd
+        for M in synth.DECODE_M:
+            w_q[(M, N, K)] = q.clone()  # every problem reads its own weight copy (> L2 in total)
+        w_s[(N, K)] = s
+        del q
+    xs, aqs, ass, outs = {}, {}, {}, {}
+    qdt = torch.int8 if code == "int8" else torch.uint8
+    for p in probs:
+        M, N, K = p
+        xs[p] = torch.from_numpy(synth.act_decode(M, K).view(np.int16)).view(torch.bfloat16).to(dev)
+        aqs[p] = torch.empty((M, K), dtype=qdt, device=dev)
+        ass[p] = torch.empty(M, dtype=torch.float32, device=dev)
+        outs[p] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = max(fp8bq.fp8bq_linear_rowwise_workspace_bytes(*p, code, torch.bfloat16)
+                   for p in probs)
+    ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
+    variants = {p: fp8bq.fp8bq_select_rowwise_variant(*p, code, torch.bfloat16) for p in probs}
+    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in probs]
+    ev_s, ev_e, ev2_s, ev2_e = mk(), mk(), mk(), mk()
+
+    def step():
+        for p in probs:
+            fp8bq.fp8bq_linear_rowwise(xs[p], w_q[p], w_s[(p[1], p[2])], code, torch.bfloat16,
+                                       out=outs[p], workspace=ws)
+
+    def step_split():
+        for i, p in enumerate(probs):
+            fp8bq.fp8bq_quant_rows(xs[p], code, q=aqs[p], s=ass[p])
+            ev[i][0].record()
+            fp8bq.fp8bq_gemm_rowwise(aqs[p], ass[p], w_q[p], w_s[(p[1], p[2])], code,
+                                     torch.bfloat16, out=outs[p], workspace=ws)
+            ev[i][1].record()
+
+    step()
+    step_split()
+    torch.cuda.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g1, stream=side):
+            ev_s.record()
+            step()
+            ev_e.record()
+        with torch.cuda.graph(g2, stream=side):
+            ev2_s.record()
+            step_split()
+            ev2_e.record()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g1.replay()
+        g2.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    step_ms = []
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        g1.replay()
+        ev_e.synchronize()
+        step_ms.append(ev_s.elapsed_time(ev_e))
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    step_s = float(np.mean(step_ms)) / 1e3
+    n_instr = max(1, min(args.steps, args.instr_steps))
+    gemm_ms = np.zeros(len(probs))
+    for _ in range(n_instr):
+        g2.replay()
+        ev2_e.synchronize()
+        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev])
+    gemm_us = gemm_ms / n_instr * 1e3
+    assert fp8bq.fp8bq_device_status() == 0
+
+    # large M: the GEMM alone, two weight copies alternating (each > L2 / 2)
+    prefill = []
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
+    for (N, K) in synth.DECODE_NK:
+        wq2 = [w_q[(1, N, K)], w_q[(2, N, K)]]
+        for M in ROWWISE_PREFILL_M:
+            xa = torch.from_numpy(synth.act_prefill(M, K).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+            aq, as_ = fp8bq.fp8bq_quant_rows(xa, code)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsz = fp8bq.fp8bq_rowwise_workspace_bytes(M, N, K, code, torch.bfloat16)
+            wsp = ws if wsz <= ws.numel() else torch.zeros(wsz, dtype=torch.uint8, device=dev)
+            for i in range(3):
+                fp8bq.fp8bq_gemm_rowwise(aq, as_, wq2[i % 2], w_s[(N, K)], code, torch.bfloat16,
+                                         out=o, workspace=wsp)
+            reps = 10
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for i in range(reps):
+                evs[i][0].record()
+                fp8bq.fp8bq_gemm_rowwise(aq, as_, wq2[i % 2], w_s[(N, K)], code, torch.bfloat16,
+                                         out=o, workspace=wsp)
+                evs[i][1].record()
+            torch.cuda.synchronize()
+            us = float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
+            fl = 2.0 * M * N * K
+            entry = {"m": M, "n": N, "k": K, "us": round(us, 2),
+                     "tflops": round(fl / us / 1e6, 1),
+                     "variant": variant_name(fp8bq.fp8bq_select_rowwise_variant(
+                         M, N, K, code, torch.bfloat16))}
+            if code == "e4m3":
+                entry["frac_of_fp8_peak"] = round(fl / us / 1e6 / fp8_peak, 3)
+            prefill.append(entry)
+            del xa, aq, as_, o
+    assert fp8bq.fp8bq_device_status() == 0
+
+    per = []
+    for i, (M, N, K) in enumerate(probs):
+        t = gemm_us[i] * 1e-6
+        b = rowwise_gemm_bytes(M, N, K)
+        per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
+                    "tflops": round(2.0 * M * N * K / t / 1e12, 2),
+                    "gbs_alg": round(b / t / 1e9, 1),
+                    "roofline_frac": round(b / (peaks["hbm_gbs"] * 1e9) / t, 3),
+                    "variant": variant_name(variants[(M, N, K)])})
+    tot = sum(rowwise_gemm_bytes(*p) for p in probs)
+    achieved = tot / (gemm_us.sum() * 1e-6) / 1e9
+    step_total = sum(rowwise_step_bytes(*p) for p in probs)
+    kern = ("gemm_mx_kernel (rowwise: plain kind::f8f6f4, scales in the epilogue)"
+            if code == "e4m3" else "gemm_i8_kernel (mma.sync m16n8k32 s8, TMA-fed)")
+    line = {
+        "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": code, "data": "synthetic",
+        "config": {"workload": ROWWISE_WORKLOAD.format(code=code),
+                   "problems_per_step": len(probs),
+                   "l2": "inputs larger than L2: each GEMM reads its own weight copy",
+                   "timing": "graph: step = fp8bq_linear_rowwise per problem, CUDA events on "
+                             "the launching stream; per-GEMM durations from an instrumented "
+                             "pass (quant and GEMM as separate calls)",
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None, "kernel": kern,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 2 * len(probs),
+        "clocks": clk, "per_shape": per, "prefill_gemm": prefill,
+        "wall_timed_s": round(t_wall, 3), "gemm_source_sha256_16": gemm_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world):
@@ -765,7 +955,9 @@ def main():
     ap.add_argument("--steps-ref", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("decode", "moe"), default="decode")
+    ap.add_argument("--workload", choices=("decode", "moe", "rowwise"), default="decode")
+    ap.add_argument("--code", choices=("e4m3", "int8"), default="e4m3",
+                    help="rowwise workload: FP8_Dynamic (e4m3) or W8A8_INT8 (int8) codes")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -777,6 +969,10 @@ def main():
         if world > 1 and rank != 0:
             return 0
         return run_gpu_moe(args, rank, world)
+    if args.workload == "rowwise":
+        if world > 1 and rank != 0:
+            return 0
+        return run_gpu_rowwise(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

@@ -3,6 +3,8 @@ command the profiler captures.
 
     python -m block_scaled_fp8_group_gb300.runcase --m 8 --n 18432 --k 7168 \
         --fmt ue8m0 --iters 3 [--variant swap/16/0[/grid/mma_scale]] [--op gemm|linear|quant]
+    python -m block_scaled_fp8_group_gb300.runcase --m 8 --n 18432 --k 7168 \
+        --op rowwise --code int8 --iters 3 [--variant swap/16/1]
 
 Inputs are the decode-sweep distributions from ``synth`` (bf16 N(0,1) with 1%
 outlier channels, bf16 N(0,0.02) weights), quantised on the GPU.
@@ -24,7 +26,9 @@ def main():
     ap.add_argument("--k", type=int, required=True)
     ap.add_argument("--fmt", default="ue8m0", choices=("fp32", "ue8m0"))
     ap.add_argument("--out", default="bf16", choices=("bf16", "fp16", "fp32"))
-    ap.add_argument("--op", default="gemm", choices=("gemm", "linear", "quant"))
+    ap.add_argument("--op", default="gemm", choices=("gemm", "linear", "quant", "rowwise"))
+    ap.add_argument("--code", default="e4m3", choices=("e4m3", "int8"),
+                    help="--op rowwise: per-token x per-channel codes")
     ap.add_argument("--variant", default=None,
                     help="kind/block_n/split[/grid[/mma_scale]] (default: the table's)")
     ap.add_argument("--iters", type=int, default=3)
@@ -40,14 +44,23 @@ def main():
         return
     w = torch.from_numpy(synth.weight_bf16(args.n, args.k).view(np.int16)).view(
         torch.bfloat16).to(dev)
-    wq, ws = fp8bq.fp8bq_quant_weight(w, args.fmt)
-    aq, as_ = fp8bq.fp8bq_quant_act(x, args.fmt)
     v = None
     if args.variant:
         parts = args.variant.split("/")
         v = fp8bq.make_variant(parts[0], int(parts[1]), int(parts[2]),
                                int(parts[3]) if len(parts) > 3 else 0,
                                int(parts[4]) if len(parts) > 4 else 0)
+    if args.op == "rowwise":
+        wq, ws = fp8bq.fp8bq_quant_rows(w, args.code)
+        aq, as_ = fp8bq.fp8bq_quant_rows(x, args.code)
+        for _ in range(args.iters):
+            fp8bq.fp8bq_gemm_rowwise(aq, as_, wq, ws, args.code, out_dt, variant=v)
+        torch.cuda.synchronize()
+        if fp8bq.fp8bq_device_status() != 0:
+            raise SystemExit("device wait timed out")
+        return
+    wq, ws = fp8bq.fp8bq_quant_weight(w, args.fmt)
+    aq, as_ = fp8bq.fp8bq_quant_act(x, args.fmt)
     for _ in range(args.iters):
         if args.op == "linear":
             fp8bq.fp8bq_linear(x, wq, ws, fmt=args.fmt, out_dtype=out_dt)
