@@ -335,11 +335,18 @@ fp8bq_status check_rowwise_ptrs(const void* a_q, const float* a_s, const void* w
     return FP8BQ_OK;
 }
 
+// INT8 problems with at least this many tokens run as two e4m3 planes on the
+// tcgen05 FP8 MMA (four cross products per K step); smaller ones on the
+// warp-level int8 MMA, which streams the int8 weights once.  On GB300 the
+// warp-level kernel is faster up to 64 tokens (one 64-token tile) and the
+// planes from 96 on (7168 x 18432: 129 vs 157 us at 64, 245 vs 174 us at 96).
+constexpr int64_t kInt8PlanesMinM = 65;
+
 // Kernel shape of a rowwise problem.  e4m3: the tile and split the block path
 // uses for UE8M0 scales (its table when it has the shape; the rowwise kernel
 // is the block-scaled one without factors), on the promotion-free kernel.
-// int8: swap-AB with the token tile covering M up to 128, otherwise as the
-// default variant.
+// int8, M >= kInt8PlanesMinM: the default variant's tiles with mma_scale = 1
+// (the FP8-plane kernel); smaller M: swap-AB with the token tile covering M.
 fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out_dtype,
                               const std::string& device_name, int num_sms) {
     fp8bq_variant v = code == FP8BQ_CODE_E4M3
@@ -348,7 +355,13 @@ fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out
                           : default_variant(M, N, K, FP8BQ_SCALE_FP32, num_sms);
     v.mma_scale = 0;
     if (v.kind == FP8BQ_KIND_SWAP_AB_64) v.kind = FP8BQ_KIND_SWAP_AB;
-    if (code == FP8BQ_CODE_INT8 && v.kind != FP8BQ_KIND_SWAP_AB) {
+    if (code == FP8BQ_CODE_INT8 && M >= kInt8PlanesMinM) {
+        v.mma_scale = 1;
+    } else if (code == FP8BQ_CODE_INT8 && M <= 8) {
+        // an 8-token tile halves the int8 MMA work, which bounds 16-token
+        // tiles even at decode sizes
+        v.block_n = 8;
+    } else if (code == FP8BQ_CODE_INT8 && v.kind != FP8BQ_KIND_SWAP_AB) {
         v.kind = FP8BQ_KIND_SWAP_AB;
         v.block_n = 128;
         const int64_t tiles = ((N + 127) / 128) * ((M + 127) / 128);
@@ -359,6 +372,18 @@ fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out
     const int64_t G = (K + kGroup - 1) / kGroup;
     if (v.split > G) v.split = static_cast<int>(G);
     return v;
+}
+
+// Rowwise kernel mode of a code and variant (GemmPlan::rowwise).
+int rowwise_mode(int code, const fp8bq_variant& v) {
+    if (code == FP8BQ_CODE_E4M3) return 1;
+    return v.mma_scale ? 3 : 2;
+}
+
+// INT8 as e4m3 planes: K rounded up to whole slabs, two plane bytes per column.
+int64_t planes_k(int64_t K) { return (K + kGroup - 1) / kGroup * kGroup; }
+size_t planes_bytes(int64_t rows, int64_t K) {
+    return align256(static_cast<size_t>(rows) * 2 * static_cast<size_t>(planes_k(K)));
 }
 
 fp8bq_status run_gemm(const GemmPlan& plan, int64_t M, int64_t N, int64_t K, const void* a_q,
@@ -832,6 +857,49 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
 
 // ----------------------------------------------- per-token x per-channel
 
+// The rowwise GEMM on a workspace region: ws_base holds [counter prefix]
+// [ws_skip bytes used by the caller][split parts][planes (INT8 on FP8)].
+fp8bq_status run_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q, const float* a_s,
+                         const void* w_q, const float* w_s, int code, int out_dtype, void* out,
+                         const fp8bq_variant& v, uint8_t* ws_base, size_t ws_bytes,
+                         size_t ws_skip, DeviceInfo* d, int prefetch_w, cudaStream_t stream) {
+    const int mode = rowwise_mode(code, v);
+    const int64_t Kg = mode == 3 ? planes_k(K) : K;  // the GEMM's K
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, Kg, v, d->num_sms, &plan, 0, mode)) return FP8BQ_ERR_UNSUPPORTED;
+    if (mode != 3) {
+        if (plan.ws_bytes && (!ws_base || ws_bytes < plan.ws_bytes + ws_skip ||
+                              (reinterpret_cast<uintptr_t>(ws_base) & 255u)))
+            return FP8BQ_ERR_WORKSPACE;
+        return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out,
+                        ws_base, ws_skip, d, prefetch_w, stream);
+    }
+    // INT8 as e4m3 planes: both operands are rewritten into the workspace
+    // first, so the GEMM may not read weights before its predecessor ends
+    const size_t parts = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
+    const size_t a_off = align256(kCounterRegion + ws_skip + parts);
+    const size_t need = a_off + planes_bytes(M, K) + planes_bytes(N, K);
+    if (!ws_base || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws_base) & 255u))
+        return FP8BQ_ERR_WORKSPACE;
+    uint8_t* pa = ws_base + a_off;
+    uint8_t* pw = pa + planes_bytes(M, K);
+    Int8PlanesArgs ia;
+    ia.q = static_cast<const int8_t*>(a_q);
+    ia.planes = pa;
+    ia.R = M;
+    ia.K = K;
+    ia.Kp = planes_k(K);
+    fp8bq_status st = from_cuda(launch_int8_planes(ia, stream));
+    if (st != FP8BQ_OK) return st;
+    ia.q = static_cast<const int8_t*>(w_q);
+    ia.planes = pw;
+    ia.R = N;
+    st = from_cuda(launch_int8_planes(ia, stream));
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, Kg, pa, a_s, pw, w_s, FP8BQ_SCALE_FP32, out_dtype, out, ws_base,
+                    ws_skip, d, 0, stream);
+}
+
 fp8bq_status fp8bq_quant_rows(const void* x, fp8bq_dtype x_dtype, int64_t R, int64_t K,
                               fp8bq_code code, void* q, float* s, cudaStream_t stream) {
     if (R < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
@@ -863,9 +931,13 @@ size_t fp8bq_rowwise_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, fp
     DeviceInfo* d = nullptr;
     int sms = 152;  // GB300 when no GPU is visible (host-only queries)
     if (device_info(&d) == FP8BQ_OK) sms = d->num_sms;
+    const int mode = rowwise_mode(code, *v);
     GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, *v, sms, &plan, 0, code == FP8BQ_CODE_INT8 ? 2 : 1)) return 0;
-    return plan.ws_bytes;
+    if (!make_gemm_plan(M, N, mode == 3 ? planes_k(K) : K, *v, sms, &plan, 0, mode)) return 0;
+    if (mode != 3) return plan.ws_bytes;
+    // [counter prefix][split parts][token planes][weight planes]
+    const size_t base = plan.ws_bytes ? plan.ws_bytes : kCounterRegion;
+    return align256(base) + planes_bytes(M, K) + planes_bytes(N, K);
 }
 
 fp8bq_status fp8bq_select_rowwise_variant(int64_t M, int64_t N, int64_t K, fp8bq_code code,
@@ -905,13 +977,8 @@ fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const v
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, *variant, d->num_sms, &plan, 0, code == FP8BQ_CODE_INT8 ? 2 : 1))
-        return FP8BQ_ERR_UNSUPPORTED;
-    st = check_ws(plan, workspace, workspace_bytes);
-    if (st != FP8BQ_OK) return st;
-    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out,
-                    workspace, 0, d, 0, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, *variant,
+                       static_cast<uint8_t*>(workspace), workspace_bytes, 0, d, 0, stream);
 }
 
 fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q,
@@ -934,6 +1001,8 @@ fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q
 size_t fp8bq_linear_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
                                             fp8bq_dtype out_dtype) {
     if (check_rowwise_args(M, N, K, code, out_dtype) != FP8BQ_OK) return 0;
+    // the GEMM's own layout (parts, then INT8 planes, at 256-byte offsets)
+    // follows the codes and scales, so its byte count carries over
     const size_t g = fp8bq_rowwise_workspace_bytes(M, N, K, code, out_dtype);
     return kCounterRegion + align256(static_cast<size_t>(M * K)) +
            align256(static_cast<size_t>(4 * M)) + (g ? g - kCounterRegion : 0);
@@ -955,16 +1024,11 @@ fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M,
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    const int rw = code == FP8BQ_CODE_INT8 ? 2 : 1;
     const fp8bq_variant v = rowwise_variant(M, N, K, code, out_dtype, d->name, d->num_sms);
-    GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan, 0, rw)) return FP8BQ_ERR_UNSUPPORTED;
-    // workspace: [counter prefix][codes][scales][split parts]
+    // workspace: [counter prefix][codes][scales][split parts][planes (INT8 on FP8)]
     const size_t q_bytes = align256(static_cast<size_t>(M * K));
     const size_t s_bytes = align256(static_cast<size_t>(4 * M));
-    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
-    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
-        return FP8BQ_ERR_WORKSPACE;
+    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes) return FP8BQ_ERR_WORKSPACE;
     uint8_t* base = static_cast<uint8_t*>(workspace);
     void* a_q = base + kCounterRegion;
     float* a_s = reinterpret_cast<float*>(base + kCounterRegion + q_bytes);
@@ -975,11 +1039,14 @@ fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M,
     qa.R = M;
     qa.K = K;
     qa.dtype = x_dtype;
-    qa.int8 = rw == 2;
+    qa.int8 = code == FP8BQ_CODE_INT8;
+    // check the GEMM's share of the workspace before launching anything
+    const size_t need = fp8bq_linear_rowwise_workspace_bytes(M, N, K, code, out_dtype);
+    if (need == 0 || workspace_bytes < need) return FP8BQ_ERR_WORKSPACE;
     st = from_cuda(launch_quant_rows(qa, stream));
     if (st != FP8BQ_OK) return st;
-    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out, base,
-                    q_bytes + s_bytes, d, 1, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, v, base,
+                       workspace_bytes, q_bytes + s_bytes, d, 1, stream);
 }
 
 fp8bq_status fp8bq_device_status(int* code, cudaStream_t stream) {

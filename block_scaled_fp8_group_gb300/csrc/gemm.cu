@@ -311,6 +311,17 @@ __device__ __forceinline__ void rowwise_scale(const KArgs& a, const TileOrigin& 
     }
 }
 
+// The PL planes of K slab kb of one operand (PL = 2: the two e4m3 planes of
+// INT8 codes, at K columns 256 kb and 256 kb + 128 of the planar operand).
+template <int PL>
+__device__ __forceinline__ void tma_load_slab(uint8_t* dst, const CUtensorMap* map,
+                                              uint64_t* bar, int kb, int row, uint64_t pol,
+                                              int plane_bytes) {
+#pragma unroll
+    for (int p = 0; p < PL; ++p)
+        tma_load_2d_hint(dst + p * plane_bytes, map, bar, (PL * kb + p) * BK, row, pol);
+}
+
 __device__ __forceinline__ float ue8m0_value(uint32_t word, int kb) {
     return __uint_as_float(((word >> (8 * (kb & 3))) & 0xFFu) << 23);
 }
@@ -846,16 +857,26 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
 // finished sum by s_tok[m] * w_s[n] before it stores (split parts are summed
 // unscaled, then scaled once).  K needs only whole 16-byte rows: the last
 // slab's columns past K are TMA zero fill.
-template <bool SWAP, int BN, int FQ = 0, bool RW = false>
+//
+// RW == 2 (W8A8_INT8 on the FP8 tensor core): both operands come as two e4m3
+// planes per 128-wide K slab (16 h and l of q = 16 h + l; launch_int8_planes
+// writes them), a stage holds both planes of both operands, and warp 1 issues
+// the four cross products per 32-wide K step into the one accumulator:
+// (16 h_a)(16 h_w) + (16 h_a) l_w + l_a (16 h_w) + l_a l_w = q_a q_w.
+template <bool SWAP, int BN, int FQ = 0, int RW = 0>
 struct MxCfg {
     static_assert(FQ == 0 || (SWAP && BN <= 32), "fused quant: swap-AB token tiles of 16/32");
     static_assert(!(FQ && RW), "rowwise scales take quantised tokens");
-    static constexpr int A_BYTES = BM * BK;
+    static constexpr int A_BYTES = BM * BK;  // one plane of one slab
     static constexpr int B_BYTES = BN * BK;
+    static constexpr int PL = RW == 2 ? 2 : 1;  // planes per operand and slab
+    static constexpr int A_STAGE = PL * A_BYTES;
+    static constexpr int B_STAGE = PL * B_BYTES;
     static constexpr int X_BYTES = FQ ? BN * BK * 2 : 0;  // raw activation tile (fused quant)
     static constexpr int E_BYTES = FQ ? BN * 4 : 0;       // the tile rows' scale exponents
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + X_BYTES + E_BYTES;
-    static constexpr int STAGES = FQ ? (BN <= 16 ? 9 : 7) : Cfg<SWAP, BN>::STAGES;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + X_BYTES + E_BYTES;
+    static constexpr int STAGES_X = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = FQ ? (BN <= 16 ? 9 : 7) : RW == 2 ? STAGES_X : Cfg<SWAP, BN>::STAGES;
     static constexpr int SRM = (FQ || RW) ? 0 : SR;  // scale-ring slots (fused, rowwise: none)
     static constexpr int NC = (BN + 31) / 32;       // factor columns of the MMA-N operand
     static constexpr int TOK_WORDS = SWAP ? BN : BM;  // token factor words per group
@@ -890,7 +911,7 @@ struct MxCfg {
                   "scale slot layout");
 };
 
-template <bool SWAP, int BN, int FQ, bool GR, bool RW = false>
+template <bool SWAP, int BN, int FQ, bool GR, int RW = 0>
 __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                    const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
@@ -903,9 +924,9 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                           // STAGES x [128 MMA-M rows x 128 B]
-    uint8_t* sB = smem + C::STAGES * C::A_BYTES;  // STAGES x [BN MMA-N rows x 128 B]
-    uint8_t* sX = sB + C::STAGES * C::B_BYTES;    // FQ: STAGES x [BN tokens x 256 B raw]
+    uint8_t* sA = smem;                           // STAGES x PL x [128 MMA-M rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_STAGE;  // STAGES x PL x [BN MMA-N rows x 128 B]
+    uint8_t* sX = sB + C::STAGES * C::B_STAGE;    // FQ: STAGES x [BN tokens x 256 B raw]
     uint32_t* sE = reinterpret_cast<uint32_t*>(sX + C::STAGES * C::X_BYTES);  // FQ: STAGES x BN
     uint8_t* ring = smem + C::RING_OFF;           // SR x SLOT_BYTES
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -979,11 +1000,11 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
             for (int i = 0; i < prefetched; ++i) {
                 mbar_arrive_expect_tx(&full[i], FQ ? C::A_BYTES : C::STAGE_BYTES);
                 if (SWAP)
-                    tma_load_2d_hint(sA + i * C::A_BYTES, &tm_mma_m, &full[i], (sg.kb0 + i) * BK,
-                                     o.w0, policy_evict_first());
+                    tma_load_slab<C::PL>(sA + i * C::A_STAGE, &tm_mma_m, &full[i], sg.kb0 + i,
+                                         o.w0, policy_evict_first(), C::A_BYTES);
                 else
-                    tma_load_2d_hint(sB + i * C::B_BYTES, &tm_mma_n, &full[i], (sg.kb0 + i) * BK,
-                                     o.w0, policy_evict_first());
+                    tma_load_slab<C::PL>(sB + i * C::B_STAGE, &tm_mma_n, &full[i], sg.kb0 + i,
+                                         o.w0, policy_evict_first(), C::B_BYTES);
             }
         }
     }
@@ -1047,11 +1068,11 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
                     } else if (fills < prefetched) {
                         // the weight tile of this stage is already on its way
                         if (SWAP)
-                            tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
-                                             kb * BK, row_n, pol_n);
+                            tma_load_slab<C::PL>(sB + stage * C::B_STAGE, &tm_mma_n, &full[stage],
+                                                 kb, row_n, pol_n, C::B_BYTES);
                         else
-                            tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
-                                             kb * BK, row_m, pol_m);
+                            tma_load_slab<C::PL>(sA + stage * C::A_STAGE, &tm_mma_m, &full[stage],
+                                                 kb, row_m, pol_m, C::A_BYTES);
                     } else {
                         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
                                                tmo, code)) {
@@ -1059,10 +1080,10 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage], kb * BK,
-                                         row_m, pol_m);
-                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage], kb * BK,
-                                         row_n, pol_n);
+                        tma_load_slab<C::PL>(sA + stage * C::A_STAGE, &tm_mma_m, &full[stage], kb,
+                                             row_m, pol_m, C::A_BYTES);
+                        tma_load_slab<C::PL>(sB + stage * C::B_STAGE, &tm_mma_n, &full[stage], kb,
+                                             row_n, pol_n, C::B_BYTES);
                     }
                     ++fills;
                     if (++stage == C::STAGES) {
@@ -1119,9 +1140,22 @@ __global__ void __launch_bounds__(MxCfg<SWAP, BN, FQ, RW>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(sA + stage * C::A_BYTES);
-                    const uint32_t b_addr = smem_addr(sB + stage * C::B_BYTES);
-                    if constexpr (RW) {
+                    const uint32_t a_addr = smem_addr(sA + stage * C::A_STAGE);
+                    const uint32_t b_addr = smem_addr(sB + stage * C::B_STAGE);
+                    if constexpr (RW == 2) {
+                        // INT8 as two e4m3 planes: the four cross products
+                        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 32; ++kk)
+#pragma unroll
+                            for (int pq = 0; pq < 4; ++pq)
+                                mma_f8f6f4(d_addr,
+                                           smem_desc_k128_sw128(a_addr + (pq >> 1) * C::A_BYTES +
+                                                                kk * 32),
+                                           smem_desc_k128_sw128(b_addr + (pq & 1) * C::B_BYTES +
+                                                                kk * 32),
+                                           idesc, (kb > sg.kb0 || kk > 0 || pq > 0) ? 1u : 0u);
+                    } else if constexpr (RW) {
                         // rowwise scales: the plain FP8 MMA, scaled in the epilogue
                         constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
 #pragma unroll
@@ -1558,7 +1592,7 @@ struct I8Cfg {
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 8 * 2 * STAGES + 16;
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile");
+    static_assert((BN % 16 == 0 || BN == 8) && BN <= 128, "token tile");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -1683,13 +1717,23 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
                 for (int kk = 0; kk < BK / 32; ++kk) {
                     uint32_t af[4];
                     ldmatrix_x4(af, a_base + (((2 * kk + a_half) ^ (a_row & 7)) << 4));
+                    if constexpr (BN == 8) {
+                        // one 8-token block: lanes 0-7 give bytes 0-15 of the
+                        // step, lanes 8-15 bytes 16-31
+                        const int tr = lane & 7;
+                        uint32_t bf[2];
+                        ldmatrix_x2(bf, b_base + tr * BK + (((2 * kk + b_half) ^ (tr & 7)) << 4));
+                        mma_s8_16x8x32(acc[0], af, bf[0], bf[1]);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < BN / 16; ++j) {
-                        const int tr = j * 16 + b_row;
-                        uint32_t bf[4];
-                        ldmatrix_x4(bf, b_base + tr * BK + (((2 * kk + b_half) ^ (tr & 7)) << 4));
-                        mma_s8_16x8x32(acc[2 * j], af, bf[0], bf[1]);
-                        mma_s8_16x8x32(acc[2 * j + 1], af, bf[2], bf[3]);
+                        for (int j = 0; j < BN / 16; ++j) {
+                            const int tr = j * 16 + b_row;
+                            uint32_t bf[4];
+                            ldmatrix_x4(bf,
+                                        b_base + tr * BK + (((2 * kk + b_half) ^ (tr & 7)) << 4));
+                            mma_s8_16x8x32(acc[2 * j], af, bf[0], bf[1]);
+                            mma_s8_16x8x32(acc[2 * j + 1], af, bf[2], bf[3]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -1826,16 +1870,22 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
             mx_attr_done[dev] = 1;
         }
         static int rw_attr_done[64] = {0};
-        if (p.rowwise && dev >= 0 && dev < 64 && !rw_attr_done[dev]) {
-            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0, false, true>,
+        if ((p.rowwise == 1 || p.rowwise == 3) && dev >= 0 && dev < 64 && !rw_attr_done[dev]) {
+            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0, false, 1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MxCfg<SWAP, BN, 0, true>::SMEM);
+                                       MxCfg<SWAP, BN, 0, 1>::SMEM);
+            if (err != cudaSuccess) return err;
+            err = cudaFuncSetAttribute(gemm_mx_kernel<SWAP, BN, 0, false, 2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       MxCfg<SWAP, BN, 0, 2>::SMEM);
             if (err != cudaSuccess) return err;
             rw_attr_done[dev] = 1;
         }
     }
     const bool swap = SWAP;
-    const uint64_t K = static_cast<uint64_t>(g.K);
+    // K columns of the operands: INT8 planes (rowwise 3) hold two per code
+    // column (g.K is then the logical K, a multiple of 128)
+    const uint64_t K = static_cast<uint64_t>(p.rowwise == 3 ? 2 * g.K : g.K);
     const int G = static_cast<int>(p.rowwise ? (g.K + BK - 1) / BK : g.K / BK);
     // grouped: E stacked [N, K] weights (N % 128 == 0), E * m_max token rows
     const int64_t w_rows = g.E > 0 ? g.E * g.N : g.N;
@@ -1932,10 +1982,16 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if constexpr (WM == BM) {
-        if (p.rowwise) {
-            cfg.blockDim = dim3(MxCfg<SWAP, BN, 0, true>::THREADS);
-            cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0, true>::SMEM;
-            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, false, true>, tm_m, tm_n,
+        if (p.rowwise == 1) {
+            cfg.blockDim = dim3(MxCfg<SWAP, BN, 0, 1>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0, 1>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, false, 1>, tm_m, tm_n,
+                                      tm_sa, tm_sw, a);
+        }
+        if (p.rowwise == 3) {
+            cfg.blockDim = dim3(MxCfg<SWAP, BN, 0, 2>::THREADS);
+            cfg.dynamicSmemBytes = MxCfg<SWAP, BN, 0, 2>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<SWAP, BN, 0, false, 2>, tm_m, tm_n,
                                       tm_sa, tm_sw, a);
         }
         if (p.mx) {
@@ -2035,10 +2091,12 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
                     GemmPlan* p, int64_t experts, int rowwise) {
     // K slabs (rowwise: the last one may be partly past K, read as zeros)
     const int G = static_cast<int>(rowwise ? (K + BK - 1) / BK : K / BK);
-    if (rowwise && (experts != 0 || v.mma_scale != 0 || v.kind == FP8BQ_KIND_SWAP_AB_64))
-        return false;
-    // INT8 (rowwise == 2): swap-AB tiles only
+    if (rowwise && (experts != 0 || v.kind == FP8BQ_KIND_SWAP_AB_64)) return false;
+    // e4m3 (1) and INT8 on the warp-level MMA (2, swap-AB tiles only) have no
+    // block-scaled form; INT8 as FP8 planes (3) is selected by mma_scale = 1
+    if ((rowwise == 1 || rowwise == 2) && v.mma_scale != 0) return false;
     if (rowwise == 2 && v.kind != FP8BQ_KIND_SWAP_AB) return false;
+    if (rowwise == 3 && (v.mma_scale != 1 || K % BK != 0)) return false;
     const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
     const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
     if (v.kind != FP8BQ_KIND_SWAP_AB && v.kind != FP8BQ_KIND_NORMAL &&
@@ -2047,7 +2105,10 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (v.kind == FP8BQ_KIND_SWAP_AB_64) {
         if (v.block_n != 16 && v.block_n != 32) return false;
     } else if (swap) {
-        if (v.block_n != 16 && v.block_n != 32 && v.block_n != 64 && v.block_n != 128) return false;
+        // (8-token tiles: the INT8 kernel on the warp-level MMA only)
+        if (v.block_n != 16 && v.block_n != 32 && v.block_n != 64 && v.block_n != 128 &&
+            !(v.block_n == 8 && rowwise == 2))
+            return false;
     } else {
         if (v.block_n != 128 && v.block_n != 256) return false;
     }
@@ -2062,7 +2123,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (experts > 0 && (v.split == 0 || N % BK != 0 || M % 4 != 0)) return false;
     p->experts = static_cast<int>(experts);
     p->rowwise = rowwise;
-    p->mx = v.mma_scale;
+    p->mx = rowwise ? 0 : v.mma_scale;
     p->kind = v.kind;
     p->bn = v.block_n;
     p->split = v.split;
@@ -2100,6 +2161,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
 cudaError_t launch_gemm(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
     if (p.rowwise == 2) {
         switch (p.bn) {
+            case 8: return launch_i8<8>(p, g, stream);
             case 16: return launch_i8<16>(p, g, stream);
             case 32: return launch_i8<32>(p, g, stream);
             case 64: return launch_i8<64>(p, g, stream);

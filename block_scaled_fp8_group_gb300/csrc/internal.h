@@ -65,6 +65,19 @@ struct QuantRowsArgs {
 };
 cudaError_t launch_quant_rows(const QuantRowsArgs& a, cudaStream_t stream);
 
+// INT8 codes as two e4m3 planes for the tcgen05 FP8 MMA: q = 16 h + l with
+// h = q >> 4 in [-8, 7] and l = q & 15 in [0, 15], both exact in e4m3.  Row r
+// of the output ([R, 2 Kp], Kp = K rounded up to 128) holds, for every
+// 128-wide K slab kb, the codes of 16 h at [256 kb, 256 kb + 128) and of l at
+// [256 kb + 128, 256 kb + 256); columns past K are zero codes.  Then
+//   q_a q_w = (16 h_a)(16 h_w) + (16 h_a) l_w + l_a (16 h_w) + l_a l_w.
+struct Int8PlanesArgs {
+    const int8_t* q;  // [R, K]
+    uint8_t* planes;  // [R, 2 Kp]
+    int64_t R, K, Kp;
+};
+cudaError_t launch_int8_planes(const Int8PlanesArgs& a, cudaStream_t stream);
+
 // ----------------------------------------------------------------- GEMM
 
 struct GemmPlan {
@@ -77,8 +90,9 @@ struct GemmPlan {
     int tiles_w;   // weight tiles
     int num_items; // tiles * split
     int experts;   // grouped: experts (0: one plain problem)
-    int rowwise;   // one scale per token and per weight row: 1 e4m3 (gemm_mx_kernel, RW),
-                   // 2 int8 (gemm_i8_kernel); 0 block scales
+    int rowwise;   // one scale per token and per weight row: 1 e4m3 (gemm_mx_kernel, RW 1),
+                   // 2 int8 (gemm_i8_kernel), 3 int8 as two e4m3 planes (gemm_mx_kernel,
+                   // RW 2; K is then the logical K, a multiple of 128); 0 block scales
     size_t ws_bytes;
 };
 

@@ -308,6 +308,14 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
                  : "r"(saddr));
 }
 
+// Two 8x8 matrices (row addresses from lanes 0-15; the other lanes' are not
+// used).
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(saddr));
+}
+
 // D (16x8 s32) += A (16x32 s8, row-major) * B (32x8 s8, column-major).
 //   a[0]: row g, k 4t..4t+3      a[1]: row g+8, k 4t..      a[2], a[3]: k + 16
 //   b0:   k 4t..4t+3, column g   b1: k + 16

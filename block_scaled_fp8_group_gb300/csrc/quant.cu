@@ -282,6 +282,43 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const QuantRows
     }
 }
 
+// ------------------------------------------------------------ int8 planes
+//
+// One CTA per row; a thread turns 16 int8 codes (one 16-byte load) into 16
+// codes of 16 h and 16 codes of l (two 16-byte stores).  Every value is an
+// integer of at most 4 significant bits, so the e4m3 conversion is exact.
+__global__ void __launch_bounds__(kRowThreads) int8_planes_kernel(const Int8PlanesArgs a) {
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const int8_t* q = a.q + row * a.K;
+    uint8_t* out = a.planes + row * 2 * a.Kp;
+    const int nc = static_cast<int>(a.Kp / 16);
+    for (int c = threadIdx.x; c < nc; c += kRowThreads) {
+        const int64_t k = static_cast<int64_t>(c) * 16;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (k < a.K) v = __ldcs(reinterpret_cast<const uint4*>(q + k));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float h[4], l[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int b = static_cast<int>(static_cast<int8_t>((w[i] >> (8 * j)) & 0xFFu));
+                h[j] = static_cast<float>(16 * (b >> 4));  // arithmetic shift: floor(b / 16)
+                l[j] = static_cast<float>(b & 15);
+            }
+            hi[i] = cvt2_e4m3(h[0], h[1]) | (cvt2_e4m3(h[2], h[3]) << 16);
+            lo[i] = cvt2_e4m3(l[0], l[1]) | (cvt2_e4m3(l[2], l[3]) << 16);
+        }
+        // slab kb = c / 8 starts at 256 kb; the chunk sits at 16 (c % 8) inside
+        const int64_t o = static_cast<int64_t>(c >> 3) * 256 + (c & 7) * 16;
+        *reinterpret_cast<uint4*>(out + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(out + o + 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
 // ------------------------------------------------------ bounded-wait test
 
 __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
@@ -353,6 +390,20 @@ cudaError_t launch_quant_rows(const QuantRowsArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return a.int8 ? launch_rows<true>(a, &cfg) : launch_rows<false>(a, &cfg);
+}
+
+cudaError_t launch_int8_planes(const Int8PlanesArgs& a, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.R));
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, int8_planes_kernel, a);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream) {

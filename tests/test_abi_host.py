@@ -249,10 +249,26 @@ def test_rowwise_variant_selection_and_workspace():
     assert v["kind"] == "swap" and v["mma_scale"] == 0
     v = fp8bq.fp8bq_select_rowwise_variant(2048, 7168, 18432, "e4m3", "bf16")
     assert v["kind"] == "normal" and v["mma_scale"] == 0
-    # int8: swap-AB tiles at every M
-    for M in (1, 48, 2048):
+    # int8: the warp-level int8 MMA (swap-AB) up to 64 tokens, the FP8-plane
+    # kernel (mma_scale = 1) above
+    for M in (1, 48, 64):
         v = fp8bq.fp8bq_select_rowwise_variant(M, 4096, 7168, "int8", "bf16")
         assert v["kind"] == "swap" and v["mma_scale"] == 0
+    for M, kind in ((65, "swap"), (2048, "normal")):
+        v = fp8bq.fp8bq_select_rowwise_variant(M, 4096, 7168, "int8", "bf16")
+        assert v["kind"] == kind and v["mma_scale"] == 1
+    # its workspace holds both operands as planes: 2 * Kp bytes per row
+    vp = fp8bq.make_variant("normal", 256, 1, 0, 1)
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(256, 512, 1040, "int8", vp) == \
+        65536 + 256 * 2 * 1152 + 512 * 2 * 1152
+    # e4m3 has no block-scaled form
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(256, 512, 1024, "e4m3", vp) == 0
+    # 8-token tiles: the int8 warp-level kernel only (chosen for M <= 8)
+    v8 = fp8bq.make_variant("swap", 8, 2)
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(8, 512, 1024, "int8", v8) == \
+        65536 + 4 * 2 * 128 * 8 * 4
+    assert fp8bq.fp8bq_rowwise_variant_workspace_bytes(8, 512, 1024, "e4m3", v8) == 0
+    assert fp8bq.fp8bq_select_rowwise_variant(8, 4096, 7168, "int8", "bf16")["block_n"] == 8
     # a K that is not a multiple of 128 counts its partial last slab
     v4 = fp8bq.make_variant("swap", 16, 4)
     tiles = 7168 // 128

@@ -6,9 +6,10 @@ oracle:
   and int8 codes, rows longer than the kernel's register cache, K not a
   multiple of 128, every finite bf16 value through the converter);
 * fp8bq_gemm_rowwise: every kernel shape (e4m3: swap-AB and normal tiles,
-  split-K, stream-K; int8: swap-AB tiles, split-K, stream-K) on ragged shapes
-  that span several tiles, all output dtypes, and DeepSeek-V3 shapes at full
-  size on sampled rows;
+  split-K, stream-K; int8 on the warp-level MMA: swap-AB tiles; int8 as two
+  e4m3 planes on the tcgen05 MMA: swap-AB and normal tiles; each with split-K
+  and stream-K) on ragged shapes that span several tiles, all output dtypes,
+  the extreme int8 codes, and DeepSeek-V3 shapes at full size on sampled rows;
 * fp8bq_linear_rowwise: quant + GEMM in one call.
 """
 import numpy as np
@@ -117,7 +118,9 @@ def run_gemm(fp8bq, qa, sa, qw, sw, code, out, variant=None):
 
 E4M3_VARIANTS = ([("swap", bn, s) for bn in (16, 32, 64, 128) for s in (1, 2, 0)] +
                  [("normal", bn, s) for bn in (128, 256) for s in (1, 3, 0)])
-INT8_VARIANTS = [("swap", bn, s) for bn in (16, 32, 64, 128) for s in (1, 3, 0)]
+INT8_VARIANTS = ([("swap", bn, s, 0) for bn in (8, 16, 32, 64, 128) for s in (1, 3, 0)] +
+                 [("swap", bn, s, 1) for bn in (16, 32, 64, 128) for s in (1, 3, 0)] +
+                 [("normal", bn, s, 1) for bn in (128, 256) for s in (1, 3, 0)])
 
 
 @pytest.mark.parametrize("kind,bn,split", E4M3_VARIANTS)
@@ -133,15 +136,41 @@ def test_gemm_rowwise_e4m3_variants(fp8bq, kind, bn, split, out):
     check_gemm(got, ref, out, f"e4m3 {kind}/{bn}/s{split}")
 
 
-@pytest.mark.parametrize("kind,bn,split", INT8_VARIANTS)
+@pytest.mark.parametrize("kind,bn,split,planes", INT8_VARIANTS)
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
-def test_gemm_rowwise_int8_variants(fp8bq, kind, bn, split, out):
+def test_gemm_rowwise_int8_variants(fp8bq, kind, bn, split, planes, out):
+    """planes=0: the warp-level int8 MMA; planes=1: the codes as two e4m3
+    planes (16 h, l of q = 16 h + l) on the tcgen05 FP8 MMA."""
     M, N, K = 150, 400, 1040
     _, qa, sa, qw, sw = rowwise_problem(M, N, K, "int8", seed=bn + split,
                                         act=synth.act_prefill)
-    got = run_gemm(fp8bq, qa, sa, qw, sw, "int8", out, fp8bq.make_variant(kind, bn, split))
+    got = run_gemm(fp8bq, qa, sa, qw, sw, "int8", out,
+                   fp8bq.make_variant(kind, bn, split, 0, planes))
     ref = oracle.gemm_rowcol(qa, sa, qw, sw, True)
-    check_gemm(got, ref, out, f"int8 {kind}/{bn}/s{split}")
+    check_gemm(got, ref, out, f"int8 {kind}/{bn}/s{split}/planes={planes}")
+
+
+def test_gemm_rowwise_int8_extreme_codes(fp8bq):
+    """Codes at the ends of the range (-128 is not produced by the quant but
+    is a valid int8 input) and every code value, on both int8 kernels: the
+    plane split must reproduce q exactly."""
+    M, N, K = 64, 256, 512
+    rng = np.random.default_rng(5)
+    qa = rng.integers(-128, 128, size=(M, K), dtype=np.int16).astype(np.int8)
+    qw = rng.integers(-128, 128, size=(N, K), dtype=np.int16).astype(np.int8)
+    qa[0, :] = -128
+    qw[0, :] = -128
+    qa[1, :256] = np.arange(-128, 128, dtype=np.int16).astype(np.int8)
+    qw[1, :256] = np.arange(127, -129, -1, dtype=np.int16).astype(np.int8)
+    sa = np.full(M, 0.01, dtype=np.float32)
+    sw = np.full(N, 0.02, dtype=np.float32)
+    ref = oracle.gemm_rowcol(qa, sa, qw, sw, True)
+    for planes in (0, 1):
+        got = run_gemm(fp8bq, qa, sa, qw, sw, "int8", "fp32",
+                       fp8bq.make_variant("swap", 64, 1, 0, planes))
+        check_gemm(got, ref, "fp32", f"int8 extreme codes planes={planes}")
+        # row 0 x column 0: 512 products of (-128)(-128), the largest sum
+        assert abs(got[0, 0] - ref[0, 0]) <= 1e-6 * abs(ref[0, 0])
 
 
 @pytest.mark.parametrize("code", ["e4m3", "int8"])
