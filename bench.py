@@ -213,6 +213,38 @@ def oracle_time_sample(rows_per_shape=1, reps=1):
     return est, sample_s, desc
 
 
+def oracle_time_all_cores(threads=None):
+    """The same oracle routine over row partitions on all host cores: one row
+    per thread per (N,K), quant + fp64 GEMM row, threads around the unchanged
+    single-thread C calls (ctypes releases the GIL).  Returns (extrapolated
+    whole-step seconds, threads, description)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    n = threads or os.cpu_count() or 1
+    total_rows = sum(synth.DECODE_M)
+    est = 0.0
+    for (N, K) in synth.DECODE_NK:
+        if (N, K) not in _ORACLE_W:
+            _ORACLE_W[(N, K)] = oracle.quant_weight(synth.weight_bf16(N, K), oracle.BF16, 128,
+                                                    128, True)
+        qw, sw = _ORACLE_W[(N, K)]
+        xb = synth.act_decode(n, K)
+
+        def one(r):
+            qa, sa = oracle.quant_act(np.ascontiguousarray(xb[r:r + 1]), oracle.BF16, 128, True)
+            oracle.gemm(qa, sa, qw, sw, True)
+
+        with ThreadPoolExecutor(max_workers=n) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(one, range(n)))
+            dt = time.perf_counter() - t0
+        est += dt / n * total_rows
+    desc = (f"{n} activation rows per (N,K), one per thread on {n} threads (row partitions of "
+            "the same single-thread oracle routine); extrapolated linearly in M")
+    return est, n, desc
+
+
 def total_step_bytes():
     return sum(step_bytes(M, N, K) for (M, N, K) in problems())
 
@@ -918,6 +950,9 @@ def run_gpu(args, rank, world):
         est, sample_s, desc = oracle_time_sample(rows_per_shape=args.oracle_rows)
         cpu = {"value": total_step_bytes() / est / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": desc + f" (sample took {sample_s:.1f} s)"}
+        est_all, nthr, desc_all = oracle_time_all_cores()
+        cpu["all_cores"] = {"value": total_step_bytes() / est_all / 1e9, "unit": "GB/s",
+                            "cores": nthr, "sample": desc_all}
     value = world * total_step_bytes() / step_s / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,

@@ -302,16 +302,27 @@ fp8bq_status fp8bq_quant_rows(const void* x, fp8bq_dtype x_dtype, int64_t R, int
                               fp8bq_code code, void* q, float* s, cudaStream_t stream);
 
 /* Rowwise-scaled GEMM: a_q [M,K] codes with a_s fp32 [M]; w_q [N,K] codes
- * with w_s fp32 [N]; out [M,N] bf16/fp16/fp32.  The workspace follows the
- * rules of fp8bq_gemm_workspace_bytes (counter prefix, then split parts).
- * The kernel shape comes from fp8bq_select_rowwise_variant. */
+ * with w_s fp32 [N]; out [M,N] bf16/fp16/fp32.  The workspace
+ * (fp8bq_rowwise_workspace_bytes, 256-byte aligned) follows the rules of
+ * fp8bq_gemm_workspace_bytes: the counter prefix, then split parts, then (int8
+ * on the FP8 MMA) the two operands' planes.  The kernel shape comes from
+ * fp8bq_select_rowwise_variant. */
 fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q,
                                 const float* a_s, const void* w_q, const float* w_s,
                                 fp8bq_code code, fp8bq_dtype out_dtype, void* out,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 /* The same with an explicit kernel shape.  e4m3: swap-AB (block_n 16..128) or
- * normal (128, 256) tiles, split >= 0 (0 = stream-K), mma_scale 0.  int8:
- * swap-AB only, block_n 16, 32, 64 or 128.  Others: FP8BQ_ERR_UNSUPPORTED. */
+ * normal (128, 256) tiles, split >= 0 (0 = stream-K), mma_scale 0.  int8 has
+ * two kernels, chosen by mma_scale:
+ *   0 -- the warp-level int8 tensor-core MMA (exact int32 sums), swap-AB
+ *        tiles only, block_n 8, 16, 32, 64 or 128;
+ *   1 -- the codes split exactly into two e4m3 planes (q = 16h + l, h = q >> 4,
+ *        l = q & 15) on the tcgen05 FP8 MMA, four cross products per K step;
+ *        swap-AB or normal tiles as for e4m3.  Both operands are rewritten into
+ *        the workspace first (2 bytes per code, K rounded up to 128), so this
+ *        form needs a workspace even without split-K.
+ * fp8bq_gemm_rowwise picks the warp-level kernel up to 64 tokens and the
+ * planes above.  Other shapes: FP8BQ_ERR_UNSUPPORTED. */
 fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
                                         const float* a_s, const void* w_q, const float* w_s,
                                         fp8bq_code code, fp8bq_dtype out_dtype, void* out,
