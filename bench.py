@@ -245,6 +245,22 @@ def oracle_time_all_cores(threads=None):
     return est, n, desc
 
 
+def max_over_ranks(seconds: float, device) -> float:
+    """The slowest rank's time: replicas report the whole job's throughput as
+    the units all ranks processed over the time of the slowest one."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job GB/s of `world` replicas that each moved bytes_per_rank in
+    `seconds` (the max over ranks): weak scaling."""
+    return world * bytes_per_rank / seconds / 1e9
+
+
 def total_step_bytes():
     return sum(step_bytes(M, N, K) for (M, N, K) in problems())
 
@@ -838,9 +854,7 @@ def run_gpu(args, rank, world):
     clk = clocks.stop() if rank == 0 else None
     step_s = float(np.mean(step_ms)) / 1e3
     if world > 1:
-        t = torch.tensor([step_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_s = float(t.item())
+        step_s = max_over_ranks(step_s, dev)
     # instrumented pass (same problems, same cold weights): per-GEMM durations
     n_instr = max(1, min(args.steps, args.instr_steps))
     gemm_ms, split_ms = np.zeros(len(probs)), []
@@ -906,10 +920,8 @@ def run_gpu(args, rank, world):
         b.synchronize()
         e2e_s = a.elapsed_time(b) / 1e3 / n_e2e
         if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": world * total_step_bytes() / e2e_s / 1e9, "unit": "GB/s",
+            e2e_s = max_over_ranks(e2e_s, dev)
+        e2e = {"value": job_value(total_step_bytes(), world, e2e_s), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
                "api": f"fp8bq_linear (quant + GEMM, PDL) per problem ({mode}); the step's inputs "
@@ -953,7 +965,7 @@ def run_gpu(args, rank, world):
         est_all, nthr, desc_all = oracle_time_all_cores()
         cpu["all_cores"] = {"value": total_step_bytes() / est_all / 1e9, "unit": "GB/s",
                             "cores": nthr, "sample": desc_all}
-    value = world * total_step_bytes() / step_s / 1e9
+    value = job_value(total_step_bytes(), world, step_s)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4),
