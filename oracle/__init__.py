@@ -76,6 +76,13 @@ def lib():
         l.oracle_int8_value.argtypes = [ctypes.c_float, ctypes.c_float]
         l.oracle_gemm_rowcol.restype = i32
         l.oracle_gemm_rowcol.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, i64, i64, vp]
+        l.oracle_quant_act_int8.restype = i32
+        l.oracle_quant_act_int8.argtypes = [vp, i32, i64, i64, i32, vp, vp]
+        l.oracle_quant_weight_int8.restype = i32
+        l.oracle_quant_weight_int8.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp]
+        l.oracle_gemm_int8_block.restype = i32
+        l.oracle_gemm_int8_block.argtypes = [i64, i64, i64, vp, vp, vp, vp, i32, i32, i32, i64,
+                                             i64, vp]
         l.oracle_calc_diff.restype = dp
         l.oracle_calc_diff.argtypes = [vp, vp, i64]
         _lib = l
@@ -256,6 +263,53 @@ def gemm_rowcol(qa, sa, qw, sw, int8: bool = False, rows=None) -> np.ndarray:
                                   int(bool(int8)), row0, cnt, _ptr(out))
     if rc != 0:
         raise ValueError("oracle_gemm_rowcol: bad arguments")
+    return out
+
+
+# ------------------------------------------------------------ block INT8 --
+
+def quant_act_int8(x_bits: np.ndarray, x_dtype: int, group: int = 128):
+    """Per-token-group quant with int8 codes ("vLLM 量化 Kernel 配置机制" §1,
+    int8_w8a8 with block_shape [128,128]).  Returns (q int8 [M,K], s float32
+    [G, Mp] column-major as quant_act's fp32 mode)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    G, Mp = K // group, (M + 3) // 4 * 4
+    q = np.empty((M, K), dtype=np.int8)
+    s = np.empty((G, Mp), dtype=np.float32)
+    rc = lib().oracle_quant_act_int8(_ptr(x_bits), x_dtype, M, K, group, _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quant_act_int8: bad arguments")
+    return q, s
+
+
+def quant_weight_int8(w: np.ndarray, w_dtype: int, bn: int = 128, bk: int = 128):
+    w = np.ascontiguousarray(w)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.int8)
+    s = np.empty(((N + bn - 1) // bn, K // bk), dtype=np.float32)
+    rc = lib().oracle_quant_weight_int8(_ptr(w), w_dtype, N, K, bn, bk, _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quant_weight_int8: bad arguments")
+    return q, s
+
+
+def gemm_int8_block(qa, sa, qw, sw, group: int = 128, bn: int = 128, bk: int = 128,
+                    rows=None) -> np.ndarray:
+    """fp64 reference of the block INT8 GEMM: every K slab's exact integer sum
+    promoted by sa[m,kb] * sw[n/bn,kb], accumulated in slab order."""
+    qa = np.ascontiguousarray(qa, dtype=np.int8)
+    qw = np.ascontiguousarray(qw, dtype=np.int8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    row0, cnt = (0, M) if rows is None else rows
+    out = np.empty((cnt, N), dtype=np.float64)
+    rc = lib().oracle_gemm_int8_block(M, N, K, _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), group,
+                                      bn, bk, row0, cnt, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_gemm_int8_block: bad arguments")
     return out
 
 

@@ -300,6 +300,79 @@ int oracle_gemm_rowcol(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const
     return 0;
 }
 
+/* ------------------------------------------------------------ block INT8 -- */
+
+int oracle_quant_act_int8(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int group,
+                          int8_t* q, float* s) {
+    if (M < 0 || K < 0 || group <= 0 || K % group) return -1;
+    if (x_dtype != ORACLE_BF16 && x_dtype != ORACLE_FP16) return -1;
+    int64_t G = K / group, Mp = pad4(M);
+    memset(s, 0, (size_t)(4 * G * Mp));
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t base = m * K + g * group;
+            float amax = 0.0f;
+            for (int64_t i = 0; i < group; ++i) {
+                float v = fabsf(load_elem(x, x_dtype, base + i));
+                if (v > amax) amax = v;
+            }
+            float mx = amax > kEps ? amax : kEps;
+            float sc = mx / kInt8Max; /* fp32 IEEE division */
+            for (int64_t i = 0; i < group; ++i)
+                q[base + i] = oracle_int8_value(load_elem(x, x_dtype, base + i), sc);
+            s[g * Mp + m] = sc;
+        }
+    }
+    return 0;
+}
+
+int oracle_quant_weight_int8(const void* w, int w_dtype, int64_t N, int64_t K, int bn, int bk,
+                             int8_t* q, float* s) {
+    if (N < 0 || K < 0 || bn <= 0 || bk <= 0 || K % bk) return -1;
+    if (w_dtype != ORACLE_FP32 && w_dtype != ORACLE_BF16 && w_dtype != ORACLE_FP16) return -1;
+    int64_t NB = (N + bn - 1) / bn, KB = K / bk;
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        int64_t n0 = nb * bn, n1 = n0 + bn < N ? n0 + bn : N;
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = kb * bk; k < (kb + 1) * bk; ++k) {
+                    float v = fabsf(load_elem(w, w_dtype, n * K + k));
+                    if (v > amax) amax = v;
+                }
+            float mx = amax > kEps ? amax : kEps;
+            float sc = mx / kInt8Max; /* fp32 IEEE division */
+            s[nb * KB + kb] = sc;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = kb * bk; k < (kb + 1) * bk; ++k)
+                    q[n * K + k] = oracle_int8_value(load_elem(w, w_dtype, n * K + k), sc);
+        }
+    }
+    return 0;
+}
+
+int oracle_gemm_int8_block(int64_t M, int64_t N, int64_t K, const int8_t* qa, const float* sa,
+                           const int8_t* qw, const float* sw, int group, int bn, int bk,
+                           int64_t row0, int64_t rows, double* out) {
+    if (!gemm_args_ok(M, N, K, group, bn, bk) || row0 < 0 || rows < 0 || row0 + rows > M)
+        return -1;
+    const int64_t G = K / bk, Mp = pad4(M);
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t m = row0 + r;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t kb = 0; kb < G; ++kb) {
+                int64_t S = 0; /* exact */
+                for (int64_t k = kb * bk; k < (kb + 1) * bk; ++k)
+                    S += (int64_t)qa[m * K + k] * (int64_t)qw[n * K + k];
+                acc += ((double)sa[kb * Mp + m] * (double)sw[(n / bn) * G + kb]) * (double)S;
+            }
+            out[r * N + n] = acc;
+        }
+    }
+    return 0;
+}
+
 /* -------------------------------------------------------------- calc_diff -- */
 
 double oracle_calc_diff(const double* x, const double* y, int64_t n) {

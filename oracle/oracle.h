@@ -127,6 +127,34 @@ int oracle_gemm_rowcol(int64_t M, int64_t N, int64_t K, const uint8_t* qa, const
                        const uint8_t* qw, const float* sw, int int8, int64_t row0, int64_t rows,
                        double* out);
 
+/* ------------------------------------------------------------------------
+ * Block INT8 ("vLLM 量化 Kernel 配置机制" §1: int8_w8a8 tables with
+ * block_shape [128,128], the block-quantised path of GPUs without FP8 tensor
+ * cores).  The page gives the layout but no formula; the reading taken is the
+ * block FP8 path's with int8 codes: per 1 x group activation group and per
+ * bn x bk weight block,
+ *   s = fp32(max(amax, 1e-10) / 127),  q = rne(clamp(fp32(x / s), -127, 127))
+ * (fp32 scales only), and the GEMM promotes every K slab's exact integer sum:
+ *   ref[m,n] = sum_kb sa[m,kb] * sw[n/bn,kb] * S_kb,
+ *   S_kb = sum_{k in slab kb} qa[m,k] * qw[n,k]     (int64, exact)
+ * accumulated in fp64 in the order kb = 0..G-1.
+ * ------------------------------------------------------------------------ */
+
+/* Activation quant with int8 codes: x [M,K] bf16/fp16 bits; q [M,K] int8;
+ * s fp32 column-major [G][Mp] (Mp = ceil(M/4)*4, padding rows 0), as the
+ * fp32 mode of oracle_quant_act. */
+int oracle_quant_act_int8(const uint16_t* x, int x_dtype, int64_t M, int64_t K, int group,
+                          int8_t* q, float* s);
+/* Weight block quant with int8 codes: w [N,K] fp32/bf16/fp16; q [N,K] int8;
+ * s fp32 [ceil(N/bn)][K/bk]. */
+int oracle_quant_weight_int8(const void* w, int w_dtype, int64_t N, int64_t K, int bn, int bk,
+                             int8_t* q, float* s);
+/* Rows [row0, row0+rows) of the block INT8 GEMM above (sa as written by
+ * oracle_quant_act_int8, sw by oracle_quant_weight_int8). */
+int oracle_gemm_int8_block(int64_t M, int64_t N, int64_t K, const int8_t* qa, const float* sa,
+                           const int8_t* qw, const float* sw, int group, int bn, int bk,
+                           int64_t row0, int64_t rows, double* out);
+
 /* calc_diff of [DG §4.4]: 1 - 2*sum(x*y) / sum(x*x + y*y), in fp64. */
 double oracle_calc_diff(const double* x, const double* y, int64_t n);
 
