@@ -484,6 +484,36 @@ bool linear_fuse_enabled() {
     return e && e[0] == '1';
 }
 
+// Block INT8 kernel shapes.
+
+fp8bq_status check_int8_block_args(int64_t M, int64_t N, int64_t K, int out_dtype) {
+    if (M < 0 || N < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (out_dtype != FP8BQ_BF16 && out_dtype != FP8BQ_FP16 && out_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_INVALID_ARG;
+    if (K == 0 || K % kGroup != 0 || N % 16 != 0) return FP8BQ_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    return FP8BQ_OK;
+}
+
+// swap-AB on the warp-level int8 MMA: the token tile covering M (8 up to 8
+// tokens), 128-token tiles above 128; split-K / stream-K as the FP8 default
+fp8bq_variant int8_block_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
+    fp8bq_variant v = default_variant(M, N, K, FP8BQ_SCALE_FP32, num_sms);
+    v.mma_scale = 0;
+    v.kind = FP8BQ_KIND_SWAP_AB;
+    v.block_n = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    const int64_t tiles = ((N + 127) / 128) * ((M + v.block_n - 1) / v.block_n);
+    const bool whole_waves = tiles % num_sms == 0 || tiles >= 4 * static_cast<int64_t>(num_sms);
+    v.split = (!whole_waves && tiles * 8 * 4 <= static_cast<int64_t>(kCounterRegion)) ? 0 : 1;
+    v.grid = 0;
+    return v;
+}
+
+int host_sms() {
+    DeviceInfo* d = nullptr;
+    return device_info(&d) == FP8BQ_OK ? d->num_sms : 152;  // GB300 without a visible GPU
+}
+
 }  // namespace
 }  // namespace fp8bq
 
@@ -1050,6 +1080,181 @@ fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M,
     if (st != FP8BQ_OK) return st;
     return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, v, base,
                        workspace_bytes, q_bytes + s_bytes, d, 1, stream);
+}
+
+// ------------------------------------------------------------ block INT8
+
+fp8bq_status fp8bq_quant_act_int8(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t K,
+                                  int group, void* q, float* s, cudaStream_t stream) {
+    if (M < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (group != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (K == 0 || K % kGroup != 0 || M > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    if ((K / kGroup + 3) / 4 > 65535) return FP8BQ_ERR_SHAPE;
+    if (M == 0) return FP8BQ_OK;
+    if (!x || !q || !s) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return FP8BQ_ERR_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    QuantActArgs a;
+    a.x = x;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.M = M;
+    a.Mp = pad_rows4(M);
+    a.K = K;
+    a.G = static_cast<int>(K / kGroup);
+    a.ue8m0 = 0;
+    a.fp16 = x_dtype == FP8BQ_FP16;
+    a.int8 = 1;
+    return from_cuda(launch_quant_act(a, stream));
+}
+
+fp8bq_status fp8bq_quant_weight_int8(const void* w, fp8bq_dtype w_dtype, int64_t N, int64_t K,
+                                     int block_n, int block_k, void* q, float* s,
+                                     cudaStream_t stream) {
+    if (N < 0 || K < 0) return FP8BQ_ERR_INVALID_ARG;
+    if (block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (w_dtype != FP8BQ_BF16 && w_dtype != FP8BQ_FP16 && w_dtype != FP8BQ_FP32)
+        return FP8BQ_ERR_INVALID_ARG;
+    if (K == 0 || K % kGroup != 0 || N > kMaxDim || K > kMaxDim) return FP8BQ_ERR_SHAPE;
+    if (N == 0) return FP8BQ_OK;
+    if (!w || !q || !s) return FP8BQ_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u))
+        return FP8BQ_ERR_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    fp8bq_status st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    QuantWeightArgs a;
+    a.w = w;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.N = N;
+    a.K = K;
+    a.NB = static_cast<int>((N + kGroup - 1) / kGroup);
+    a.KB = static_cast<int>(K / kGroup);
+    a.dtype = w_dtype;
+    a.ue8m0 = 0;
+    a.int8 = 1;
+    return from_cuda(launch_quant_weight(a, stream));
+}
+
+fp8bq_status fp8bq_select_int8_block_variant(int64_t M, int64_t N, int64_t K,
+                                             fp8bq_dtype out_dtype, fp8bq_variant* variant) {
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    fp8bq_status st = check_int8_block_args(M, N, K, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    *variant = int8_block_variant(M, N, K, host_sms());
+    return FP8BQ_OK;
+}
+
+size_t fp8bq_int8_block_variant_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                                const fp8bq_variant* v) {
+    if (!v || check_int8_block_args(M, N, K, FP8BQ_BF16) != FP8BQ_OK) return 0;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *v, host_sms(), &plan, 0, 4)) return 0;
+    return plan.ws_bytes;
+}
+
+size_t fp8bq_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_dtype out_dtype) {
+    if (check_int8_block_args(M, N, K, out_dtype) != FP8BQ_OK) return 0;
+    const fp8bq_variant v = int8_block_variant(M, N, K, host_sms());
+    return fp8bq_int8_block_variant_workspace_bytes(M, N, K, &v);
+}
+
+fp8bq_status fp8bq_gemm_int8_block_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                           const float* a_s, const void* w_q, const float* w_s,
+                                           fp8bq_dtype out_dtype, void* out,
+                                           const fp8bq_variant* variant, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream) {
+    fp8bq_status st = check_int8_block_args(M, N, K, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (!variant) return FP8BQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, *variant, d->num_sms, &plan, 0, 4)) return FP8BQ_ERR_UNSUPPORTED;
+    st = check_ws(plan, workspace, workspace_bytes);
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out,
+                    workspace, 0, d, 0, stream);
+}
+
+fp8bq_status fp8bq_gemm_int8_block(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                   const float* a_s, const void* w_q, const float* w_s,
+                                   int group, int block_n, int block_k, fp8bq_dtype out_dtype,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+    fp8bq_status st = check_int8_block_args(M, N, K, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = int8_block_variant(M, N, K, host_sms());
+    return fp8bq_gemm_int8_block_variant(M, N, K, a_q, a_s, w_q, w_s, out_dtype, out, &v,
+                                         workspace, workspace_bytes, stream);
+}
+
+size_t fp8bq_linear_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                               fp8bq_dtype out_dtype) {
+    if (check_int8_block_args(M, N, K, out_dtype) != FP8BQ_OK) return 0;
+    const size_t g = fp8bq_int8_block_workspace_bytes(M, N, K, out_dtype);
+    return kCounterRegion + align256(static_cast<size_t>(M * K)) +
+           align256(fp8bq_act_scale_bytes(M, K, kGroup, FP8BQ_SCALE_FP32)) +
+           (g ? g - kCounterRegion : 0);
+}
+
+fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N,
+                                     int64_t K, const void* w_q, const float* w_s, int group,
+                                     int block_n, int block_k, fp8bq_dtype out_dtype, void* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+    fp8bq_status st = check_int8_block_args(M, N, K, out_dtype);
+    if (st != FP8BQ_OK) return st;
+    if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
+    if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    if (!x) return FP8BQ_ERR_INVALID_ARG;
+    st = check_gemm_ptrs(x, x, w_q, w_s, out);
+    if (st != FP8BQ_OK) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8BQ_ERR_WORKSPACE;
+    if ((K / kGroup + 3) / 4 > 65535) return FP8BQ_ERR_SHAPE;
+    DeviceInfo* d = nullptr;
+    st = device_info(&d);
+    if (st != FP8BQ_OK) return st;
+    const fp8bq_variant v = int8_block_variant(M, N, K, d->num_sms);
+    GemmPlan plan;
+    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan, 0, 4)) return FP8BQ_ERR_UNSUPPORTED;
+    // workspace: [counter prefix][codes][scales][split parts]
+    const size_t q_bytes = align256(static_cast<size_t>(M * K));
+    const size_t s_bytes = align256(fp8bq_act_scale_bytes(M, K, kGroup, FP8BQ_SCALE_FP32));
+    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
+    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
+        return FP8BQ_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* a_q = base + kCounterRegion;
+    float* a_s = reinterpret_cast<float*>(base + kCounterRegion + q_bytes);
+    QuantActArgs qa;
+    qa.x = x;
+    qa.q = static_cast<uint8_t*>(a_q);
+    qa.s = a_s;
+    qa.M = M;
+    qa.Mp = pad_rows4(M);
+    qa.K = K;
+    qa.G = static_cast<int>(K / kGroup);
+    qa.ue8m0 = 0;
+    qa.fp16 = x_dtype == FP8BQ_FP16;
+    qa.int8 = 1;
+    st = from_cuda(launch_quant_act(qa, stream));
+    if (st != FP8BQ_OK) return st;
+    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out, base,
+                    q_bytes + s_bytes, d, 1, stream);
 }
 
 fp8bq_status fp8bq_device_status(int* code, cudaStream_t stream) {

@@ -1596,7 +1596,18 @@ struct I8Cfg {
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <int BN>
+// BLK (block INT8: int8_w8a8 with 1x128 activation groups and 128x128 weight
+// blocks, fp32 scales): after every K slab each thread converts its exact
+// int32 slab sums (|S| < 2^21) to fp32 exactly and promotes them by
+// sa[kb][t] * sw[nb][kb] into fp32 accumulators, as the FP8 block path does;
+// split parts are then fp32 and stores need no further scaling.
+__device__ __forceinline__ float exact_i2f(int v) {
+    // |v| < 2^22: v + 1.5 * 2^23 has the fp32 exponent of 2^23, so its low
+    // mantissa bits are v; subtracting 1.5 * 2^23 leaves exactly v
+    return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+template <int BN, bool BLK = false>
 __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
     gemm_i8_kernel(const __grid_constant__ CUtensorMap tm_w,  // weights [N, K] int8
                    const __grid_constant__ CUtensorMap tm_t,  // tokens [M, K] int8
@@ -1702,10 +1713,18 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
         wi.init(a);
         Seg sg;
         bool ok = true;
+        const int64_t Mp = (static_cast<int64_t>(a.M) + 3) / 4 * 4;  // BLK: act scale rows
         while (ok && wi.next(a, sg)) {
             int acc[BN / 8][4];
+            float accf[BLK ? BN / 8 : 1][4];
 #pragma unroll
             for (int j = 0; j < BN / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0;
+            if constexpr (BLK) {
+#pragma unroll
+                for (int j = 0; j < BN / 8; ++j)
+                    accf[j][0] = accf[j][1] = accf[j][2] = accf[j][3] = 0.0f;
+            }
+            const TileOrigin ot = tile_origin<true, BN, BM, false>(a, sg.tile);
             for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                 if (!warp_wait(&full[stage], phase, abort_flag, a.status, tmo, code)) {
                     ok = false;
@@ -1742,10 +1761,27 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
                     stage = 0;
                     phase ^= 1u;
                 }
+                if constexpr (BLK) {
+                    // promote the slab: sa of this thread's token columns,
+                    // sw of the tile's weight block
+                    const float swv = __ldg(a.w_s + static_cast<int64_t>(ot.w0 / BK) * a.G + kb);
+                    const float* sak = a.s_tok + static_cast<int64_t>(kb) * Mp;
+#pragma unroll
+                    for (int j = 0; j < BN / 8; ++j) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int t = ot.tok0 + 8 * j + 2 * t4 + c;
+                            const float f = (t < ot.tok_end ? __ldg(sak + t) : 0.0f) * swv;
+                            accf[j][c] = fmaf(exact_i2f(acc[j][c]), f, accf[j][c]);
+                            accf[j][c + 2] = fmaf(exact_i2f(acc[j][c + 2]), f, accf[j][c + 2]);
+                            acc[j][c] = acc[j][c + 2] = 0;
+                        }
+                    }
+                }
             }
             if (!ok) break;
 
-            const TileOrigin o = tile_origin<true, BN, BM, false>(a, sg.tile);
+            const TileOrigin o = ot;
             // element (j, i) of this thread: weight row w0 + 16 cw + g + 8 (i / 2),
             // token tok0 + 8 j + 2 t4 + (i % 2)
             auto store = [&](int j, int i, int v) {
@@ -1755,11 +1791,22 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
                     store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n,
                                static_cast<float>(v) * (__ldg(a.s_tok + t) * __ldg(a.w_s + n)));
             };
+            auto store_f = [&](int j, int i, float v) {  // BLK: already promoted
+                const int n = o.w0 + cw * 16 + g + 8 * (i >> 1);
+                const int t = o.tok0 + 8 * j + 2 * t4 + (i & 1);
+                if (n < o.w_end && t < o.tok_end)
+                    store_out1(a.out, a.out_dtype, static_cast<int64_t>(t) * a.N + n, v);
+            };
             if (sg.nparts == 1) {
 #pragma unroll
                 for (int j = 0; j < BN / 8; ++j)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) store(j, i, acc[j][i]);
+                    for (int i = 0; i < 4; ++i) {
+                        if constexpr (BLK)
+                            store_f(j, i, accf[j][i]);
+                        else
+                            store(j, i, acc[j][i]);
+                    }
                 continue;
             }
             // split parts: int32 [column][row] tiles in the workspace
@@ -1771,7 +1818,12 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < BN / 8; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) __stcg(mine + pidx(j, i), acc[j][i]);
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (BLK)  // fp32 parts (promoted)
+                        __stcg(reinterpret_cast<float*>(mine) + pidx(j, i), accf[j][i]);
+                    else
+                        __stcg(mine + pidx(j, i), acc[j][i]);
+                }
             __threadfence();
             __syncwarp();
             unsigned* ctr = a.counters + static_cast<int64_t>(sg.tile) * kCountersPerTile + cw;
@@ -1780,21 +1832,40 @@ __global__ void __launch_bounds__(I8Cfg<BN>::THREADS, 1)
             prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
             if (prev != static_cast<unsigned>(sg.nparts - 1)) continue;
             __threadfence();
+            if constexpr (BLK) {
+                // fp32 parts, summed in K order
+                for (int p = 0; p < sg.nparts; ++p) {
+                    const float* src = a.partials + part_slot(a, sg.tile, p) * TILE;
 #pragma unroll
-            for (int j = 0; j < BN / 8; ++j)
+                    for (int j = 0; j < BN / 8; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[j][i] = 0;
-            for (int p = 0; p < sg.nparts; ++p) {
-                const int* src = reinterpret_cast<const int*>(a.partials) + part_slot(a, sg.tile, p) * TILE;
+                        for (int i = 0; i < 4; ++i) {
+                            const float v = __ldcg(src + pidx(j, i));
+                            accf[j][i] = p == 0 ? v : accf[j][i] + v;
+                        }
+                }
 #pragma unroll
                 for (int j = 0; j < BN / 8; ++j)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[j][i] += __ldcg(src + pidx(j, i));
+                    for (int i = 0; i < 4; ++i) store_f(j, i, accf[j][i]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[j][i] = 0;
+                for (int p = 0; p < sg.nparts; ++p) {
+                    const int* src =
+                        reinterpret_cast<const int*>(a.partials) + part_slot(a, sg.tile, p) * TILE;
+#pragma unroll
+                    for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[j][i] += __ldcg(src + pidx(j, i));
+                }
+#pragma unroll
+                for (int j = 0; j < BN / 8; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) store(j, i, acc[j][i]);
             }
-#pragma unroll
-            for (int j = 0; j < BN / 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) store(j, i, acc[j][i]);
             if (lane == 0) *ctr = 0u;  // ready for the next call
         }
     }
@@ -2024,7 +2095,8 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM, false>, tm_m, tm_n, tm_sa, tm_sw, a);
 }
 
-// INT8 rowwise GEMM (plan.rowwise == 2): swap-AB tiles of 128 weight rows x BN tokens.
+// INT8 GEMM on the warp-level MMA (plan.rowwise 2: rowwise scales; 4: block
+// scales): swap-AB tiles of 128 weight rows x BN tokens.
 template <int BN>
 cudaError_t launch_i8(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
     using C = I8Cfg<BN>;
@@ -2033,9 +2105,10 @@ cudaError_t launch_i8(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        err = cudaFuncSetAttribute(gemm_i8_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::SMEM);
-        if (err != cudaSuccess) return err;
+        for (auto fn : {gemm_i8_kernel<BN, false>, gemm_i8_kernel<BN, true>}) {
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            if (err != cudaSuccess) return err;
+        }
         attr_done[dev] = 1;
     }
     const uint64_t K = static_cast<uint64_t>(g.K);
@@ -2082,7 +2155,8 @@ cudaError_t launch_i8(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_i8_kernel<BN>, tm_w, tm_t, a);
+    if (p.rowwise == 4) return cudaLaunchKernelEx(&cfg, gemm_i8_kernel<BN, true>, tm_w, tm_t, a);
+    return cudaLaunchKernelEx(&cfg, gemm_i8_kernel<BN, false>, tm_w, tm_t, a);
 }
 
 }  // namespace
@@ -2094,8 +2168,9 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if (rowwise && (experts != 0 || v.kind == FP8BQ_KIND_SWAP_AB_64)) return false;
     // e4m3 (1) and INT8 on the warp-level MMA (2, swap-AB tiles only) have no
     // block-scaled form; INT8 as FP8 planes (3) is selected by mma_scale = 1
-    if ((rowwise == 1 || rowwise == 2) && v.mma_scale != 0) return false;
-    if (rowwise == 2 && v.kind != FP8BQ_KIND_SWAP_AB) return false;
+    if ((rowwise == 1 || rowwise == 2 || rowwise == 4) && v.mma_scale != 0) return false;
+    if ((rowwise == 2 || rowwise == 4) && v.kind != FP8BQ_KIND_SWAP_AB) return false;
+    if (rowwise == 4 && K % BK != 0) return false;
     if (rowwise == 3 && (v.mma_scale != 1 || K % BK != 0)) return false;
     const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
     const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
@@ -2107,7 +2182,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     } else if (swap) {
         // (8-token tiles: the INT8 kernel on the warp-level MMA only)
         if (v.block_n != 16 && v.block_n != 32 && v.block_n != 64 && v.block_n != 128 &&
-            !(v.block_n == 8 && rowwise == 2))
+            !(v.block_n == 8 && (rowwise == 2 || rowwise == 4)))
             return false;
     } else {
         if (v.block_n != 128 && v.block_n != 256) return false;
@@ -2159,7 +2234,7 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
-    if (p.rowwise == 2) {
+    if (p.rowwise == 2 || p.rowwise == 4) {
         switch (p.bn) {
             case 8: return launch_i8<8>(p, g, stream);
             case 16: return launch_i8<16>(p, g, stream);

@@ -35,6 +35,7 @@ struct QuantActArgs {
     int G;       // groups per row
     int ue8m0;
     int fp16;    // input is fp16 (else bf16)
+    int int8 = 0;  // int8 codes, s = max(amax, eps) / 127 (fp32 scales; block INT8)
     // Grouped rows (optional): row r belongs to expert r / m_max and is
     // quantised only if r % m_max < counts[expert] (device array, clamped to
     // [0, m_max]); other rows are neither read nor written.
@@ -51,6 +52,7 @@ struct QuantWeightArgs {
     int NB, KB;
     int dtype;  // fp8bq_dtype
     int ue8m0;
+    int int8 = 0;  // int8 codes (block INT8)
 };
 cudaError_t launch_quant_weight(const QuantWeightArgs& a, cudaStream_t stream);
 
@@ -92,7 +94,8 @@ struct GemmPlan {
     int experts;   // grouped: experts (0: one plain problem)
     int rowwise;   // one scale per token and per weight row: 1 e4m3 (gemm_mx_kernel, RW 1),
                    // 2 int8 (gemm_i8_kernel), 3 int8 as two e4m3 planes (gemm_mx_kernel,
-                   // RW 2; K is then the logical K, a multiple of 128); 0 block scales
+                   // RW 2; K is then the logical K, a multiple of 128); 4 block INT8 on
+                   // the warp-level MMA (gemm_i8_kernel, BLK); 0 block FP8 scales
     size_t ws_bytes;
 };
 

@@ -69,9 +69,15 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    const float s = group_scale(amax, a.ue8m0);
+    const float s = a.int8 ? __fdiv_rn(fmaxf(amax, kEps), kInt8Max) : group_scale(amax, a.ue8m0);
 
-    if (active) {
+    if (active && a.int8) {
+        // block INT8: 16 int8 codes
+        *reinterpret_cast<uint4*>(a.q + off) =
+            make_uint4(cvt4_int8(f[0], f[1], f[2], f[3], s), cvt4_int8(f[4], f[5], f[6], f[7], s),
+                       cvt4_int8(f[8], f[9], f[10], f[11], s),
+                       cvt4_int8(f[12], f[13], f[14], f[15], s));
+    } else if (active) {
         uint32_t c[8];
         if (a.ue8m0) {
             // s = 2^e exactly, so x * (1/s) is the same correctly rounded
@@ -178,13 +184,21 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const QuantWeightArgs
     amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
-    const float s = group_scale(amax, a.ue8m0);
+    const float s = a.int8 ? __fdiv_rn(fmaxf(amax, kEps), kInt8Max) : group_scale(amax, a.ue8m0);
     if (t == 0) a.s[static_cast<int64_t>(nb) * a.KB + kb] = s;
 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t n = static_cast<int64_t>(nb) * kGroup + (t >> 3) + 32 * i;
         if (n >= a.N) continue;
+        if (a.int8) {
+            const float* v = f[i];
+            *reinterpret_cast<uint4*>(a.q + n * a.K + col) =
+                make_uint4(cvt4_int8(v[0], v[1], v[2], v[3], s), cvt4_int8(v[4], v[5], v[6], v[7], s),
+                           cvt4_int8(v[8], v[9], v[10], v[11], s),
+                           cvt4_int8(v[12], v[13], v[14], v[15], s));
+            continue;
+        }
         uint32_t c[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -214,15 +228,8 @@ __device__ __forceinline__ uint4 encode16(const float (&f)[16], float s) {
     uint32_t c[4];
     if constexpr (kInt8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t w = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float y = fminf(fmaxf(__fdiv_rn(f[4 * i + j], s), -kInt8Max), kInt8Max);
-                w |= (static_cast<uint32_t>(__float2int_rn(y)) & 0xFFu) << (8 * j);
-            }
-            c[i] = w;
-        }
+        for (int i = 0; i < 4; ++i)
+            c[i] = cvt4_int8(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], s);
     } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i)

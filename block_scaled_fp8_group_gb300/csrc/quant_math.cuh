@@ -36,6 +36,19 @@ __device__ __forceinline__ uint32_t cvt2_e4m3(float a, float b) {
                                                           __NV_E4M3));
 }
 
+// Four fp32 values -> four int8 codes (byte j = value j): round half to even
+// of clamp(v / s, -127, 127), with the IEEE division.
+__device__ __forceinline__ uint32_t cvt4_int8(float a, float b, float c, float d, float s) {
+    const float v[4] = {a, b, c, d};
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float y = fminf(fmaxf(__fdiv_rn(v[j], s), -kInt8Max), kInt8Max);
+        w |= (static_cast<uint32_t>(__float2int_rn(y)) & 0xFFu) << (8 * j);
+    }
+    return w;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float f16_lo(uint32_t w) {

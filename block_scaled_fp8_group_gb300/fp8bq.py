@@ -41,7 +41,11 @@ EXPORTS = (
     "fp8bq_grouped_linear_workspace_bytes", "fp8bq_quant_rows", "fp8bq_gemm_rowwise",
     "fp8bq_gemm_rowwise_variant", "fp8bq_select_rowwise_variant",
     "fp8bq_rowwise_workspace_bytes", "fp8bq_rowwise_variant_workspace_bytes",
-    "fp8bq_linear_rowwise", "fp8bq_linear_rowwise_workspace_bytes",
+    "fp8bq_linear_rowwise", "fp8bq_linear_rowwise_workspace_bytes", "fp8bq_quant_act_int8",
+    "fp8bq_quant_weight_int8", "fp8bq_gemm_int8_block", "fp8bq_gemm_int8_block_variant",
+    "fp8bq_select_int8_block_variant", "fp8bq_int8_block_workspace_bytes",
+    "fp8bq_int8_block_variant_workspace_bytes", "fp8bq_linear_int8_block",
+    "fp8bq_linear_int8_block_workspace_bytes",
 )
 
 
@@ -114,6 +118,19 @@ def _load():
         "fp8bq_linear_rowwise": (i32, [vp, i32, i64, i64, i64, vp, vp, i32, i32, vp, vp, sz,
                                        vp]),
         "fp8bq_linear_rowwise_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "fp8bq_quant_act_int8": (i32, [vp, i32, i64, i64, i32, vp, vp, vp]),
+        "fp8bq_quant_weight_int8": (i32, [vp, i32, i64, i64, i32, i32, vp, vp, vp]),
+        "fp8bq_gemm_int8_block": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                        vp, sz, vp]),
+        "fp8bq_gemm_int8_block_variant": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, vp,
+                                                ctypes.POINTER(Variant), vp, sz, vp]),
+        "fp8bq_select_int8_block_variant": (i32, [i64, i64, i64, i32, ctypes.POINTER(Variant)]),
+        "fp8bq_int8_block_workspace_bytes": (sz, [i64, i64, i64, i32]),
+        "fp8bq_int8_block_variant_workspace_bytes": (sz, [i64, i64, i64,
+                                                          ctypes.POINTER(Variant)]),
+        "fp8bq_linear_int8_block": (i32, [vp, i32, i64, i64, i64, vp, vp, i32, i32, i32, i32, vp,
+                                          vp, sz, vp]),
+        "fp8bq_linear_int8_block_workspace_bytes": (sz, [i64, i64, i64, i32]),
         "fp8bq_status_string": (ctypes.c_char_p, [i32]),
         "fp8bq_abi_version": (i32, []),
     }
@@ -511,6 +528,95 @@ def fp8bq_linear_rowwise(x, w_q, w_s, code="e4m3", out_dtype=torch.bfloat16, out
                                    _code(code), _dtype_code(out.dtype), _ptr(out),
                                    _ptr(workspace), wsz, _stream(stream))
     _check(st, "fp8bq_linear_rowwise")
+    return out
+
+
+# ------------------------------------------------------------------ block INT8
+
+def fp8bq_quant_act_int8(x: torch.Tensor, group: int = 128, q=None, s=None, stream=None):
+    """x [M,K] bf16/fp16 -> (q int8 [M,K], s fp32 [K/128, Mp] column-major)."""
+    _need(x, "x")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if s is None:
+        s = torch.empty(act_scale_shape(M, K, group, "fp32")[0], dtype=torch.float32,
+                        device=x.device)
+    st = _lib.fp8bq_quant_act_int8(_ptr(x), _dtype_code(x.dtype), M, K, group, _ptr(q), _ptr(s),
+                                   _stream(stream))
+    _check(st, "fp8bq_quant_act_int8")
+    return q, s
+
+
+def fp8bq_quant_weight_int8(w: torch.Tensor, block_n: int = 128, block_k: int = 128, q=None,
+                            s=None, stream=None):
+    """w [N,K] fp32/bf16/fp16 -> (q int8 [N,K], s fp32 [ceil(N/128), K/128])."""
+    _need(w, "w")
+    N, K = w.shape
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if s is None:
+        s = torch.empty(((N + block_n - 1) // block_n, K // block_k), dtype=torch.float32,
+                        device=w.device)
+    st = _lib.fp8bq_quant_weight_int8(_ptr(w), _dtype_code(w.dtype), N, K, block_n, block_k,
+                                      _ptr(q), _ptr(s), _stream(stream))
+    _check(st, "fp8bq_quant_weight_int8")
+    return q, s
+
+
+def fp8bq_select_int8_block_variant(M, N, K, out_dtype=torch.bfloat16) -> dict:
+    v = Variant()
+    st = _lib.fp8bq_select_int8_block_variant(M, N, K, _dtype_code(out_dtype), ctypes.byref(v))
+    _check(st, "fp8bq_select_int8_block_variant")
+    return v.as_dict()
+
+
+def fp8bq_gemm_int8_block(a_q, a_s, w_q, w_s, out_dtype=torch.bfloat16, out=None,
+                          workspace=None, variant: Variant | None = None, stream=None):
+    """Block INT8 GEMM: int8 codes with fp32 1x128 activation-group and 128x128
+    weight-block scales."""
+    for t, n in ((a_q, "a_q"), (a_s, "a_s"), (w_q, "w_q"), (w_s, "w_s")):
+        _need(t, n)
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    out = _out(M, N, out_dtype, a_q.device, out)
+    if variant is None:
+        nbytes = _lib.fp8bq_int8_block_workspace_bytes(M, N, K, _dtype_code(out.dtype))
+    else:
+        nbytes = _lib.fp8bq_int8_block_variant_workspace_bytes(M, N, K, ctypes.byref(variant))
+    if workspace is None:
+        workspace = _workspace(nbytes, a_q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant is None:
+        st = _lib.fp8bq_gemm_int8_block(M, N, K, _ptr(a_q), _ptr(a_s), _ptr(w_q), _ptr(w_s), 128,
+                                        128, 128, _dtype_code(out.dtype), _ptr(out),
+                                        _ptr(workspace), wsz, _stream(stream))
+    else:
+        st = _lib.fp8bq_gemm_int8_block_variant(M, N, K, _ptr(a_q), _ptr(a_s), _ptr(w_q),
+                                                _ptr(w_s), _dtype_code(out.dtype), _ptr(out),
+                                                ctypes.byref(variant), _ptr(workspace), wsz,
+                                                _stream(stream))
+    _check(st, "fp8bq_gemm_int8_block")
+    return out
+
+
+def fp8bq_linear_int8_block(x, w_q, w_s, out_dtype=torch.bfloat16, out=None, workspace=None,
+                            stream=None):
+    """Block INT8 linear layer: int8 group quant of x [M,K] (bf16/fp16), then
+    the block INT8 GEMM, in one call."""
+    for t, n in ((x, "x"), (w_q, "w_q"), (w_s, "w_s")):
+        _need(t, n)
+    M, K = x.shape
+    N = w_q.shape[0]
+    out = _out(M, N, out_dtype, x.device, out)
+    nbytes = _lib.fp8bq_linear_int8_block_workspace_bytes(M, N, K, _dtype_code(out.dtype))
+    if workspace is None:
+        workspace = _workspace(nbytes, x.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.fp8bq_linear_int8_block(_ptr(x), _dtype_code(x.dtype), M, N, K, _ptr(w_q),
+                                      _ptr(w_s), 128, 128, 128, _dtype_code(out.dtype), _ptr(out),
+                                      _ptr(workspace), wsz, _stream(stream))
+    _check(st, "fp8bq_linear_int8_block")
     return out
 
 

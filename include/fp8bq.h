@@ -346,6 +346,55 @@ fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M,
 size_t fp8bq_linear_rowwise_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_code code,
                                             fp8bq_dtype out_dtype);
 
+/* ------------------------------------------------------------ block INT8
+ *
+ * "vLLM 量化 Kernel 配置机制" §1 lists int8_w8a8 tables with block_shape
+ * [128,128]: the block-quantised path with INT8 codes.  The rule used is the
+ * block FP8 path's with int8 codes and fp32 scales:
+ *   s = fp32(max(amax, 1e-10) / 127) per 1 x 128 activation group and per
+ *       128 x 128 weight block, q = round-half-even(clamp(x / s, -127, 127));
+ *   out[m,n] = sum_kb sa[m,kb] * sw[n/128,kb] * S_kb,  S_kb the exact integer
+ *       sum of slab kb's products (int32 on the warp-level int8 MMA, promoted
+ *       per slab in fp32).
+ * Layouts as the FP8 block path with fp32 scales: activation scales fp32
+ * column-major [K/128][Mp] (Mp = ceil(M/4)*4, padding rows 0), weight scales
+ * fp32 [ceil(N/128)][K/128], codes int8 row-major.  K % 128 == 0; N % 16 == 0
+ * for the GEMM; group/block sizes 128 (FP8BQ_ERR_UNSUPPORTED otherwise). */
+fp8bq_status fp8bq_quant_act_int8(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t K,
+                                  int group, void* q, float* s, cudaStream_t stream);
+fp8bq_status fp8bq_quant_weight_int8(const void* w, fp8bq_dtype w_dtype, int64_t N, int64_t K,
+                                     int block_n, int block_k, void* q, float* s,
+                                     cudaStream_t stream);
+/* The block INT8 GEMM; workspace rules as fp8bq_gemm (counter prefix, then
+ * split parts).  The _variant form takes swap-AB shapes with block_n 8, 16,
+ * 32, 64 or 128, split >= 0, mma_scale 0. */
+fp8bq_status fp8bq_gemm_int8_block(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                   const float* a_s, const void* w_q, const float* w_s,
+                                   int group, int block_n, int block_k, fp8bq_dtype out_dtype,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+fp8bq_status fp8bq_gemm_int8_block_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
+                                           const float* a_s, const void* w_q, const float* w_s,
+                                           fp8bq_dtype out_dtype, void* out,
+                                           const fp8bq_variant* variant, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
+fp8bq_status fp8bq_select_int8_block_variant(int64_t M, int64_t N, int64_t K,
+                                             fp8bq_dtype out_dtype, fp8bq_variant* variant);
+size_t fp8bq_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_dtype out_dtype);
+size_t fp8bq_int8_block_variant_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                                const fp8bq_variant* variant);
+/* Block INT8 linear layer: fp8bq_quant_act_int8 of x [M,K] (bf16/fp16), then
+ * the GEMM, one call, two launches.  Workspace: [65536-byte counter prefix]
+ * [codes M*K][scales 4*(K/128)*Mp][split parts], each at a 256-byte aligned
+ * offset. */
+fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t N,
+                                     int64_t K, const void* w_q, const float* w_s, int group,
+                                     int block_n, int block_k, fp8bq_dtype out_dtype, void* out,
+                                     void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
+size_t fp8bq_linear_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                               fp8bq_dtype out_dtype);
+
 /* ------------------------------------------------------------ host queries */
 
 /* The variant fp8bq_gemm would run for this shape (host only, no GPU work):

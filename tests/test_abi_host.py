@@ -285,3 +285,29 @@ def test_rowwise_variant_selection_and_workspace():
     g = fp8bq.fp8bq_rowwise_workspace_bytes(8, 7168, 18432, "int8", "bf16")
     lin = fp8bq.fp8bq_linear_rowwise_workspace_bytes(8, 7168, 18432, "int8", "bf16")
     assert lin == 65536 + 8 * 18432 + 256 + (g - 65536 if g else 0)
+
+
+def test_int8_block_argument_errors_and_sizes():
+    lib = fp8bq.lib()
+    p = ctypes.c_void_p(4096)
+    g = lambda M=16, N=128, K=256, ptr=4096, grp=128, out=0: lib.fp8bq_gemm_int8_block(  # noqa
+        M, N, K, ctypes.c_void_p(ptr), ctypes.c_void_p(ptr), ctypes.c_void_p(ptr),
+        ctypes.c_void_p(ptr), grp, 128, 128, out, ctypes.c_void_p(ptr), None, 0, None)
+    assert g(K=1040) == 2          # K % 128
+    assert g(N=120) == 2           # N % 16
+    assert g(grp=64) == 4
+    assert g(out=5) == 1
+    assert g(ptr=4100) == 3
+    assert g(M=0) == 0
+    assert lib.fp8bq_quant_act_int8(p, 2, 4, 128, 128, p, p, None) == 4   # fp32 input
+    assert lib.fp8bq_quant_act_int8(p, 0, 4, 100, 128, p, p, None) == 2
+    assert lib.fp8bq_quant_weight_int8(p, 0, 4, 128, 64, 128, p, p, None) == 4
+    # swap-AB only, 8-token tiles allowed; split parts as the FP8 workspace
+    v = fp8bq.make_variant("swap", 8, 4)
+    tiles = 7168 // 128
+    assert lib.fp8bq_int8_block_variant_workspace_bytes(8, 7168, 18432, ctypes.byref(v)) == \
+        65536 + tiles * 4 * 128 * 8 * 4
+    vn = fp8bq.make_variant("normal", 256, 1)
+    assert lib.fp8bq_int8_block_variant_workspace_bytes(256, 512, 1024, ctypes.byref(vn)) == 0
+    assert fp8bq.fp8bq_select_int8_block_variant(4, 4096, 7168)["block_n"] == 8
+    assert fp8bq.fp8bq_select_int8_block_variant(2048, 4096, 7168)["kind"] == "swap"
