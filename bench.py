@@ -536,10 +536,13 @@ def moe_oracle_sample():
 
 # ----------------------------------------------- rowwise (per-token x per-channel)
 
-ROWWISE_WORKLOAD = ("rowwise {code}: decode sweep (N,K) in {{(7168,18432),(18432,7168),(4096,7168)}} "
+ROWWISE_WORKLOAD = ("{code}: decode sweep (N,K) in {{(7168,18432),(18432,7168),(4096,7168)}} "
                     "x M in {{1,2,4,8,16,24,32,48,64,96,128}}; act bf16 N(0,1), 1% channels x30 "
-                    "-> per-token quant; weights bf16 N(0,0.02) per-channel quant; bf16 out; "
-                    "fp8bq_linear_rowwise per problem")
+                    "-> {aq}; weights bf16 N(0,0.02) {wq}; bf16 out; {api} per problem")
+ROWWISE_QUANT = {"e4m3": ("per-token quant", "per-channel quant", "fp8bq_linear_rowwise"),
+                 "int8": ("per-token quant", "per-channel quant", "fp8bq_linear_rowwise"),
+                 "int8block": ("1x128 group quant", "128x128 block quant",
+                               "fp8bq_linear_int8_block")}
 ROWWISE_PREFILL_M = (2048, 4096)
 
 
@@ -553,6 +556,81 @@ def rowwise_step_bytes(M, N, K):
     return 2 * M * K + N * K + 4 * N + 2 * M * N
 
 
+def block_int8_gemm_bytes(M, N, K):
+    """Block INT8 GEMM: int8 codes, fp32 act scales [G][Mp], fp32 weight
+    block scales, bf16 out."""
+    G, Mp = K // 128, (M + 3) // 4 * 4
+    return M * K + N * K + 4 * Mp * G + 4 * ((N + 127) // 128) * G + 2 * M * N
+
+
+def block_int8_step_bytes(M, N, K):
+    G = K // 128
+    return 2 * M * K + N * K + 4 * ((N + 127) // 128) * G + 2 * M * N
+
+
+class FormatCalls:
+    """The calls one per-token x per-channel code (e4m3, int8) or block INT8
+    (int8block) makes, so one benchmark leg serves all three."""
+
+    def __init__(self, fp8bq, torch, code):
+        self.f, self.t, self.code = fp8bq, torch, code
+        self.block = code == "int8block"
+
+    def quant_w(self, wd):
+        if self.block:
+            return self.f.fp8bq_quant_weight_int8(wd)
+        return self.f.fp8bq_quant_rows(wd, self.code)
+
+    def alloc_a(self, M, K, dev):
+        t = self.t
+        qdt = t.int8 if self.code != "e4m3" else t.uint8
+        if self.block:
+            shape = self.f.act_scale_shape(M, K, 128, "fp32")[0]
+            return t.empty((M, K), dtype=qdt, device=dev), t.empty(shape, dtype=t.float32,
+                                                                     device=dev)
+        return t.empty((M, K), dtype=qdt, device=dev), t.empty(M, dtype=t.float32, device=dev)
+
+    def quant_a(self, x, q=None, s=None):
+        if self.block:
+            return self.f.fp8bq_quant_act_int8(x, q=q, s=s)
+        return self.f.fp8bq_quant_rows(x, self.code, q=q, s=s)
+
+    def gemm(self, aq, as_, wq, ws, out, workspace):
+        if self.block:
+            return self.f.fp8bq_gemm_int8_block(aq, as_, wq, ws, self.t.bfloat16, out=out,
+                                                workspace=workspace)
+        return self.f.fp8bq_gemm_rowwise(aq, as_, wq, ws, self.code, self.t.bfloat16, out=out,
+                                         workspace=workspace)
+
+    def linear(self, x, wq, ws, out, workspace):
+        if self.block:
+            return self.f.fp8bq_linear_int8_block(x, wq, ws, self.t.bfloat16, out=out,
+                                                  workspace=workspace)
+        return self.f.fp8bq_linear_rowwise(x, wq, ws, self.code, self.t.bfloat16, out=out,
+                                           workspace=workspace)
+
+    def linear_ws(self, M, N, K):
+        if self.block:
+            return self.f.lib().fp8bq_linear_int8_block_workspace_bytes(M, N, K, 0)
+        return self.f.fp8bq_linear_rowwise_workspace_bytes(M, N, K, self.code, self.t.bfloat16)
+
+    def gemm_ws(self, M, N, K):
+        if self.block:
+            return self.f.lib().fp8bq_int8_block_workspace_bytes(M, N, K, 0)
+        return self.f.fp8bq_rowwise_workspace_bytes(M, N, K, self.code, self.t.bfloat16)
+
+    def select(self, M, N, K):
+        if self.block:
+            return self.f.fp8bq_select_int8_block_variant(M, N, K, self.t.bfloat16)
+        return self.f.fp8bq_select_rowwise_variant(M, N, K, self.code, self.t.bfloat16)
+
+    def gemm_bytes(self, M, N, K):
+        return block_int8_gemm_bytes(M, N, K) if self.block else rowwise_gemm_bytes(M, N, K)
+
+    def step_bytes(self, M, N, K):
+        return block_int8_step_bytes(M, N, K) if self.block else rowwise_step_bytes(M, N, K)
+
+
 def run_gpu_rowwise(args, rank, world):
     import torch
 
@@ -561,6 +639,7 @@ def run_gpu_rowwise(args, rank, world):
     from block_scaled_fp8_group_gb300 import fp8bq
 
     code = args.code
+    fc = FormatCalls(fp8bq, torch, code)
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -568,39 +647,34 @@ def run_gpu_rowwise(args, rank, world):
     w_q, w_s = {}, {}
     for (N, K) in synth.DECODE_NK:
         wd = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
-        q, s = fp8bq.fp8bq_quant_rows(wd, code)
+        q, s = fc.quant_w(wd)
         del wd
         for M in synth.DECODE_M:
             w_q[(M, N, K)] = q.clone()  # every problem reads its own weight copy (> L2 in total)
         w_s[(N, K)] = s
         del q
     xs, aqs, ass, outs = {}, {}, {}, {}
-    qdt = torch.int8 if code == "int8" else torch.uint8
     for p in probs:
         M, N, K = p
         xs[p] = torch.from_numpy(synth.act_decode(M, K).view(np.int16)).view(torch.bfloat16).to(dev)
-        aqs[p] = torch.empty((M, K), dtype=qdt, device=dev)
-        ass[p] = torch.empty(M, dtype=torch.float32, device=dev)
+        aqs[p], ass[p] = fc.alloc_a(M, K, dev)
         outs[p] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws_bytes = max(fp8bq.fp8bq_linear_rowwise_workspace_bytes(*p, code, torch.bfloat16)
-                   for p in probs)
+    ws_bytes = max(fc.linear_ws(*p) for p in probs)
     ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
-    variants = {p: fp8bq.fp8bq_select_rowwise_variant(*p, code, torch.bfloat16) for p in probs}
+    variants = {p: fc.select(*p) for p in probs}
     mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
     ev = [(mk(), mk()) for _ in probs]
     ev_s, ev_e, ev2_s, ev2_e = mk(), mk(), mk(), mk()
 
     def step():
         for p in probs:
-            fp8bq.fp8bq_linear_rowwise(xs[p], w_q[p], w_s[(p[1], p[2])], code, torch.bfloat16,
-                                       out=outs[p], workspace=ws)
+            fc.linear(xs[p], w_q[p], w_s[(p[1], p[2])], outs[p], ws)
 
     def step_split():
         for i, p in enumerate(probs):
-            fp8bq.fp8bq_quant_rows(xs[p], code, q=aqs[p], s=ass[p])
+            fc.quant_a(xs[p], q=aqs[p], s=ass[p])
             ev[i][0].record()
-            fp8bq.fp8bq_gemm_rowwise(aqs[p], ass[p], w_q[p], w_s[(p[1], p[2])], code,
-                                     torch.bfloat16, out=outs[p], workspace=ws)
+            fc.gemm(aqs[p], ass[p], w_q[p], w_s[(p[1], p[2])], outs[p], ws)
             ev[i][1].record()
 
     step()
@@ -653,28 +727,25 @@ def run_gpu_rowwise(args, rank, world):
         for M in ROWWISE_PREFILL_M:
             xa = torch.from_numpy(synth.act_prefill(M, K).view(np.int16)).view(
                 torch.bfloat16).to(dev)
-            aq, as_ = fp8bq.fp8bq_quant_rows(xa, code)
+            aq, as_ = fc.quant_a(xa)
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            wsz = fp8bq.fp8bq_rowwise_workspace_bytes(M, N, K, code, torch.bfloat16)
+            wsz = fc.gemm_ws(M, N, K)
             wsp = ws if wsz <= ws.numel() else torch.zeros(wsz, dtype=torch.uint8, device=dev)
             for i in range(3):
-                fp8bq.fp8bq_gemm_rowwise(aq, as_, wq2[i % 2], w_s[(N, K)], code, torch.bfloat16,
-                                         out=o, workspace=wsp)
+                fc.gemm(aq, as_, wq2[i % 2], w_s[(N, K)], o, wsp)
             reps = 10
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(reps)]
             for i in range(reps):
                 evs[i][0].record()
-                fp8bq.fp8bq_gemm_rowwise(aq, as_, wq2[i % 2], w_s[(N, K)], code, torch.bfloat16,
-                                         out=o, workspace=wsp)
+                fc.gemm(aq, as_, wq2[i % 2], w_s[(N, K)], o, wsp)
                 evs[i][1].record()
             torch.cuda.synchronize()
             us = float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
             fl = 2.0 * M * N * K
             entry = {"m": M, "n": N, "k": K, "us": round(us, 2),
                      "tflops": round(fl / us / 1e6, 1),
-                     "variant": variant_name(fp8bq.fp8bq_select_rowwise_variant(
-                         M, N, K, code, torch.bfloat16))}
+                     "variant": variant_name(fc.select(M, N, K))}
             if code == "e4m3":
                 entry["frac_of_fp8_peak"] = round(fl / us / 1e6 / fp8_peak, 3)
             prefill.append(entry)
@@ -684,23 +755,27 @@ def run_gpu_rowwise(args, rank, world):
     per = []
     for i, (M, N, K) in enumerate(probs):
         t = gemm_us[i] * 1e-6
-        b = rowwise_gemm_bytes(M, N, K)
+        b = fc.gemm_bytes(M, N, K)
         per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
                     "tflops": round(2.0 * M * N * K / t / 1e12, 2),
                     "gbs_alg": round(b / t / 1e9, 1),
                     "roofline_frac": round(b / (peaks["hbm_gbs"] * 1e9) / t, 3),
                     "variant": variant_name(variants[(M, N, K)])})
-    tot = sum(rowwise_gemm_bytes(*p) for p in probs)
+    tot = sum(fc.gemm_bytes(*p) for p in probs)
     achieved = tot / (gemm_us.sum() * 1e-6) / 1e9
-    step_total = sum(rowwise_step_bytes(*p) for p in probs)
-    kern = ("gemm_mx_kernel (rowwise: plain kind::f8f6f4, scales in the epilogue)"
-            if code == "e4m3" else "gemm_i8_kernel (mma.sync m16n8k32 s8, TMA-fed)")
+    step_total = sum(fc.step_bytes(*p) for p in probs)
+    kern = {"e4m3": "gemm_mx_kernel (rowwise: plain kind::f8f6f4, scales in the epilogue)",
+            "int8": "gemm_i8_kernel (mma.sync m16n8k32 s8, TMA-fed) up to 64 tokens, "
+                    "gemm_mx_kernel on two e4m3 planes above",
+            "int8block": "gemm_i8_kernel, block promotion per K slab (mma.sync m16n8k32 s8)"}[code]
     line = {
         "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": code, "data": "synthetic",
-        "config": {"workload": ROWWISE_WORKLOAD.format(code=code),
+        "config": {"workload": ROWWISE_WORKLOAD.format(
+                       code=code, aq=ROWWISE_QUANT[code][0], wq=ROWWISE_QUANT[code][1],
+                       api=ROWWISE_QUANT[code][2]),
                    "problems_per_step": len(probs),
                    "l2": "inputs larger than L2: each GEMM reads its own weight copy",
                    "timing": "graph: step = fp8bq_linear_rowwise per problem, CUDA events on "
@@ -1003,8 +1078,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=("decode", "moe", "rowwise"), default="decode")
-    ap.add_argument("--code", choices=("e4m3", "int8"), default="e4m3",
-                    help="rowwise workload: FP8_Dynamic (e4m3) or W8A8_INT8 (int8) codes")
+    ap.add_argument("--code", choices=("e4m3", "int8", "int8block"), default="e4m3",
+                    help="rowwise workload: FP8_Dynamic (e4m3), W8A8_INT8 (int8) or block "
+                         "INT8 (int8block) codes")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -499,6 +499,13 @@ fp8bq_status check_int8_block_args(int64_t M, int64_t N, int64_t K, int out_dtyp
 // tokens), 128-token tiles above 128; split-K / stream-K as the FP8 default
 fp8bq_variant int8_block_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
     fp8bq_variant v = default_variant(M, N, K, FP8BQ_SCALE_FP32, num_sms);
+    if (M >= kInt8PlanesMinM) {
+        // two e4m3 planes on the promotion kernel, the default tile; whole
+        // tiles for the normal orientation (as the rowwise INT8 planes)
+        v.mma_scale = 1;
+        if (v.kind == FP8BQ_KIND_NORMAL) v.split = 1;
+        return v;
+    }
     v.mma_scale = 0;
     v.kind = FP8BQ_KIND_SWAP_AB;
     v.block_n = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
@@ -892,15 +899,16 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
 
 // The rowwise GEMM on a workspace region: ws_base holds [counter prefix]
 // [ws_skip bytes used by the caller][split parts][planes (INT8 on FP8)].
+//   mode: GemmPlan::rowwise (3 and 5 rewrite both operands as INT8 planes).
 fp8bq_status run_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q, const float* a_s,
-                         const void* w_q, const float* w_s, int code, int out_dtype, void* out,
+                         const void* w_q, const float* w_s, int mode, int out_dtype, void* out,
                          const fp8bq_variant& v, uint8_t* ws_base, size_t ws_bytes,
                          size_t ws_skip, DeviceInfo* d, int prefetch_w, cudaStream_t stream) {
-    const int mode = rowwise_mode(code, v);
-    const int64_t Kg = mode == 3 ? planes_k(K) : K;  // the GEMM's K
+    const bool planes = mode == 3 || mode == 5;
+    const int64_t Kg = planes ? planes_k(K) : K;  // the GEMM's K
     GemmPlan plan;
     if (!make_gemm_plan(M, N, Kg, v, d->num_sms, &plan, 0, mode)) return FP8BQ_ERR_UNSUPPORTED;
-    if (mode != 3) {
+    if (!planes) {
         if (plan.ws_bytes && (!ws_base || ws_bytes < plan.ws_bytes + ws_skip ||
                               (reinterpret_cast<uintptr_t>(ws_base) & 255u)))
             return FP8BQ_ERR_WORKSPACE;
@@ -1010,8 +1018,9 @@ fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const v
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, *variant,
-                       static_cast<uint8_t*>(workspace), workspace_bytes, 0, d, 0, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, rowwise_mode(code, *variant), out_dtype, out,
+                       *variant, static_cast<uint8_t*>(workspace), workspace_bytes, 0, d, 0,
+                       stream);
 }
 
 fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q,
@@ -1078,8 +1087,8 @@ fp8bq_status fp8bq_linear_rowwise(const void* x, fp8bq_dtype x_dtype, int64_t M,
     if (need == 0 || workspace_bytes < need) return FP8BQ_ERR_WORKSPACE;
     st = from_cuda(launch_quant_rows(qa, stream));
     if (st != FP8BQ_OK) return st;
-    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, code, out_dtype, out, v, base,
-                       workspace_bytes, q_bytes + s_bytes, d, 1, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, rowwise_mode(code, v), out_dtype, out, v,
+                       base, workspace_bytes, q_bytes + s_bytes, d, 1, stream);
 }
 
 // ------------------------------------------------------------ block INT8
@@ -1152,9 +1161,13 @@ fp8bq_status fp8bq_select_int8_block_variant(int64_t M, int64_t N, int64_t K,
 size_t fp8bq_int8_block_variant_workspace_bytes(int64_t M, int64_t N, int64_t K,
                                                 const fp8bq_variant* v) {
     if (!v || check_int8_block_args(M, N, K, FP8BQ_BF16) != FP8BQ_OK) return 0;
+    const int mode = v->mma_scale ? 5 : 4;
     GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, *v, host_sms(), &plan, 0, 4)) return 0;
-    return plan.ws_bytes;
+    if (!make_gemm_plan(M, N, K, *v, host_sms(), &plan, 0, mode)) return 0;
+    if (mode == 4) return plan.ws_bytes;
+    // [counter prefix][split parts][token planes][weight planes]
+    const size_t base = plan.ws_bytes ? plan.ws_bytes : kCounterRegion;
+    return align256(base) + planes_bytes(M, K) + planes_bytes(N, K);
 }
 
 size_t fp8bq_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_dtype out_dtype) {
@@ -1177,12 +1190,9 @@ fp8bq_status fp8bq_gemm_int8_block_variant(int64_t M, int64_t N, int64_t K, cons
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, *variant, d->num_sms, &plan, 0, 4)) return FP8BQ_ERR_UNSUPPORTED;
-    st = check_ws(plan, workspace, workspace_bytes);
-    if (st != FP8BQ_OK) return st;
-    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out,
-                    workspace, 0, d, 0, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, variant->mma_scale ? 5 : 4, out_dtype, out,
+                       *variant, static_cast<uint8_t*>(workspace), workspace_bytes, 0, d, 0,
+                       stream);
 }
 
 fp8bq_status fp8bq_gemm_int8_block(int64_t M, int64_t N, int64_t K, const void* a_q,
@@ -1229,14 +1239,11 @@ fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
     const fp8bq_variant v = int8_block_variant(M, N, K, d->num_sms);
-    GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, v, d->num_sms, &plan, 0, 4)) return FP8BQ_ERR_UNSUPPORTED;
-    // workspace: [counter prefix][codes][scales][split parts]
+    // workspace: [counter prefix][codes][scales][split parts][planes (above 64 tokens)]
     const size_t q_bytes = align256(static_cast<size_t>(M * K));
     const size_t s_bytes = align256(fp8bq_act_scale_bytes(M, K, kGroup, FP8BQ_SCALE_FP32));
-    const size_t part_bytes = plan.ws_bytes ? plan.ws_bytes - kCounterRegion : 0;
-    if (workspace_bytes < kCounterRegion + q_bytes + s_bytes + part_bytes)
-        return FP8BQ_ERR_WORKSPACE;
+    const size_t need = fp8bq_linear_int8_block_workspace_bytes(M, N, K, out_dtype);
+    if (need == 0 || workspace_bytes < need) return FP8BQ_ERR_WORKSPACE;
     uint8_t* base = static_cast<uint8_t*>(workspace);
     void* a_q = base + kCounterRegion;
     float* a_s = reinterpret_cast<float*>(base + kCounterRegion + q_bytes);
@@ -1253,8 +1260,8 @@ fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t
     qa.int8 = 1;
     st = from_cuda(launch_quant_act(qa, stream));
     if (st != FP8BQ_OK) return st;
-    return run_gemm(plan, M, N, K, a_q, a_s, w_q, w_s, FP8BQ_SCALE_FP32, out_dtype, out, base,
-                    q_bytes + s_bytes, d, 1, stream);
+    return run_rowwise(M, N, K, a_q, a_s, w_q, w_s, v.mma_scale ? 5 : 4, out_dtype, out, v, base,
+                       workspace_bytes, q_bytes + s_bytes, d, 1, stream);
 }
 
 fp8bq_status fp8bq_device_status(int* code, cudaStream_t stream) {

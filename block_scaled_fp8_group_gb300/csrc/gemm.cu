@@ -62,7 +62,10 @@ constexpr int SLOT_BYTES = 768;      // per slab: 128 act scales, 2 weight-scale
 constexpr int SLOT_SW = 512;         // weight-scale chunk c at SLOT_SW + c * SLOT_SW_STEP
 constexpr int SLOT_SW_STEP = 128;    // (TMA destinations 128-byte aligned)
 
-template <bool SWAP, int BN, int WM = BM>
+// PL = 2 (block INT8 as two e4m3 planes, 128-row tiles): a stage holds both
+// planes of both operands of one logical K slab, and the slab's MMA is the
+// four cross products per 32-wide K step into its TMEM buffer (see MxCfg).
+template <bool SWAP, int BN, int WM = BM, int PL = 1>
 struct Cfg {
     // MMA-M rows of a tile: tokens (normal, always 128) or weight rows (swap:
     // 128, or 64 with the M = 64 MMA, whose accumulator row r sits at TMEM
@@ -70,13 +73,17 @@ struct Cfg {
     static constexpr int MR = SWAP ? WM : BM;
     static_assert(MR == 128 || (SWAP && MR == 64), "tile rows");
     static constexpr int ROWS_PER_QUAD = MR / 4;
-    static constexpr int A_BYTES = MR * BK;
+    static_assert(PL == 1 || MR == 128, "planes: 128-row tiles");
+    static constexpr int A_BYTES = MR * BK;  // one plane of one slab
     static constexpr int B_BYTES = BN * BK;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int A_STAGE = PL * A_BYTES;
+    static constexpr int B_STAGE = PL * B_BYTES;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
     // 64-row weight tiles carry half the bytes per stage, so twice the stages
-    // keep the same bytes in flight
+    // keep the same bytes in flight; two planes take twice the room
     static constexpr int STAGES_128 = BN <= 16 ? 10 : BN <= 32 ? 9 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
-    static constexpr int STAGES = MR == 128 ? STAGES_128 : (BN <= 16 ? 18 : 15);
+    static constexpr int STAGES_PL = STAGES_128 / PL < 2 ? 2 : STAGES_128 / PL;
+    static constexpr int STAGES = MR == 128 ? STAGES_PL : (BN <= 16 ? 18 : 15);
     // TMEM accumulator buffers: as many as fit in the 512 columns (at most 8)
     static constexpr int NBUF = 512 / BN >= 8 ? 8 : 512 / BN;
     static constexpr int TMEM_NEED = NBUF * BN;
@@ -378,20 +385,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
 }
 
-template <bool SWAP, int BN, int WM, bool GR>
-__global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
+template <bool SWAP, int BN, int WM, bool GR, int PL = 1>
+__global__ void __launch_bounds__(Cfg<SWAP, BN, WM, PL>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_mma_m,  // MMA-M operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_mma_n,  // MMA-N operand [rows, K] e4m3
                 const __grid_constant__ CUtensorMap tm_sa,     // act scales [cols][Mp] 4-byte
                 const __grid_constant__ CUtensorMap tm_sw,     // weight scales, flat fp32
                 const KArgs a) {
-    using C = Cfg<SWAP, BN, WM>;
+    using C = Cfg<SWAP, BN, WM, PL>;
     constexpr int SR = C::SRC;  // scale ring depth of this configuration
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;                            // STAGES x [MR rows x 128 B]
-    uint8_t* sB = smem + C::STAGES * C::A_BYTES;   // STAGES x [BN rows x 128 B]
+    uint8_t* sA = smem;                            // STAGES x PL x [MR rows x 128 B]
+    uint8_t* sB = smem + C::STAGES * C::A_STAGE;   // STAGES x PL x [BN rows x 128 B]
     uint8_t* ring = smem + C::RING_OFF;            // SR x SLOT_BYTES
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + C::STAGES;
@@ -465,11 +472,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
             for (int i = 0; i < prefetched; ++i) {
                 mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
                 if (SWAP)
-                    tma_load_2d_hint(sA + i * C::A_BYTES, &tm_mma_m, &full[i], (sg.kb0 + i) * BK,
-                                     o.w0, policy_evict_first());
+                    tma_load_slab<PL>(sA + i * C::A_STAGE, &tm_mma_m, &full[i], sg.kb0 + i, o.w0,
+                                      policy_evict_first(), C::A_BYTES);
                 else
-                    tma_load_2d_hint(sB + i * C::B_BYTES, &tm_mma_n, &full[i], (sg.kb0 + i) * BK,
-                                     o.w0, policy_evict_first());
+                    tma_load_slab<PL>(sB + i * C::B_STAGE, &tm_mma_n, &full[i], sg.kb0 + i, o.w0,
+                                      policy_evict_first(), C::B_BYTES);
             }
         }
     }
@@ -505,11 +512,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                     if (fills < prefetched) {
                         // the weight tile of this stage is already on its way
                         if (SWAP)
-                            tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
-                                             kb * BK, row_n, pol_n);
+                            tma_load_slab<PL>(sB + stage * C::B_STAGE, &tm_mma_n, &full[stage], kb,
+                                              row_n, pol_n, C::B_BYTES);
                         else
-                            tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
-                                             kb * BK, row_m, pol_m);
+                            tma_load_slab<PL>(sA + stage * C::A_STAGE, &tm_mma_m, &full[stage], kb,
+                                              row_m, pol_m, C::A_BYTES);
                     } else {
                         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status,
                                                tmo, code)) {
@@ -517,10 +524,10 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                        tma_load_2d_hint(sA + stage * C::A_BYTES, &tm_mma_m, &full[stage],
-                                         kb * BK, row_m, pol_m);
-                        tma_load_2d_hint(sB + stage * C::B_BYTES, &tm_mma_n, &full[stage],
-                                         kb * BK, row_n, pol_n);
+                        tma_load_slab<PL>(sA + stage * C::A_STAGE, &tm_mma_m, &full[stage], kb,
+                                          row_m, pol_m, C::A_BYTES);
+                        tma_load_slab<PL>(sB + stage * C::B_STAGE, &tm_mma_n, &full[stage], kb,
+                                          row_n, pol_n, C::B_BYTES);
                     }
                     ++fills;
                     if (++stage == C::STAGES) {
@@ -573,13 +580,17 @@ __global__ void __launch_bounds__(Cfg<SWAP, BN, WM>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(sA + stage * C::A_BYTES);
-                    const uint32_t b_addr = smem_addr(sB + stage * C::B_BYTES);
+                    const uint32_t a_addr = smem_addr(sA + stage * C::A_STAGE);
+                    const uint32_t b_addr = smem_addr(sB + stage * C::B_STAGE);
                     const uint32_t d_addr = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk)
-                        mma_f8f6f4(d_addr, smem_desc_k128_sw128(a_addr + kk * 32),
-                                   smem_desc_k128_sw128(b_addr + kk * 32), idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int pq = 0; pq < PL * PL; ++pq)  // PL = 2: the four cross products
+                            mma_f8f6f4(d_addr,
+                                       smem_desc_k128_sw128(a_addr + (pq / PL) * C::A_BYTES + kk * 32),
+                                       smem_desc_k128_sw128(b_addr + (pq % PL) * C::B_BYTES + kk * 32),
+                                       idesc, (kk > 0 || pq > 0) ? 1u : 0u);
                     mma_commit(&empty[stage]);
                     mma_commit(&tfull[buf]);
                     if (++stage == C::STAGES) {
@@ -1921,6 +1932,26 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         attr_done[dev] = 1;
     }
     if constexpr (WM == BM) {
+        // block INT8 as two planes (rowwise 5): the PL = 2 promotion kernel
+        static int pl_attr_done[64] = {0};
+        if (p.rowwise == 5 && dev >= 0 && dev < 64 && !pl_attr_done[dev]) {
+            using C2 = Cfg<SWAP, BN, BM, 2>;
+            const auto fn = gemm_kernel<SWAP, BN, BM, false, 2>;
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C2::SMEM);
+            if (err != cudaSuccess) return err;
+            if (C2::REGSPLIT) {
+                cudaFuncAttributes fa;
+                err = cudaFuncGetAttributes(&fa, fn);
+                if (err != cudaSuccess) return err;
+                if (fa.numRegs < C2::REG_MIN_LAUNCH) {
+                    log_error("GEMM kernel compiled with too few registers for its register split");
+                    return cudaErrorInvalidConfiguration;
+                }
+            }
+            pl_attr_done[dev] = 1;
+        }
+    }
+    if constexpr (WM == BM) {
         static int mx_attr_done[64] = {0};
         if (p.mx && dev >= 0 && dev < 64 && !mx_attr_done[dev]) {
             for (auto fn : {gemm_mx_kernel<SWAP, BN, 0, false>, gemm_mx_kernel<SWAP, BN, 0, true>}) {
@@ -1956,7 +1987,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
     const bool swap = SWAP;
     // K columns of the operands: INT8 planes (rowwise 3) hold two per code
     // column (g.K is then the logical K, a multiple of 128)
-    const uint64_t K = static_cast<uint64_t>(p.rowwise == 3 ? 2 * g.K : g.K);
+    const uint64_t K = static_cast<uint64_t>((p.rowwise == 3 || p.rowwise == 5) ? 2 * g.K : g.K);
     const int G = static_cast<int>(p.rowwise ? (g.K + BK - 1) / BK : g.K / BK);
     // grouped: E stacked [N, K] weights (N % 128 == 0), E * m_max token rows
     const int64_t w_rows = g.E > 0 ? g.E * g.N : g.N;
@@ -1981,7 +2012,7 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
         ok = encode_operand(&tm_m, g.a_q, K, static_cast<uint64_t>(g.M), BM) &&
              encode_operand(&tm_n, g.w_q, K, static_cast<uint64_t>(w_rows), BN);
     }
-    if (p.rowwise) {
+    if (p.rowwise && p.rowwise != 5) {
         // rowwise scales are read by the epilogue directly: no scale maps
         tm_sa = tm_m;
         tm_sw = tm_m;
@@ -2089,6 +2120,14 @@ cudaError_t launch_bn(const GemmPlan& p, const GemmLaunch& g, cudaStream_t strea
                                       tm_sw, a);
         }
     }
+    if constexpr (WM == BM) {
+        if (p.rowwise == 5) {
+            cfg.blockDim = dim3(Cfg<SWAP, BN, BM, 2>::THREADS);
+            cfg.dynamicSmemBytes = Cfg<SWAP, BN, BM, 2>::SMEM;
+            return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, BM, false, 2>, tm_m, tm_n, tm_sa,
+                                      tm_sw, a);
+        }
+    }
     if (g.E > 0)
         return cudaLaunchKernelEx(&cfg, gemm_kernel<SWAP, BN, WM, true>, tm_m, tm_n, tm_sa, tm_sw,
                                   a);
@@ -2171,7 +2210,8 @@ bool make_gemm_plan(int64_t M, int64_t N, int64_t K, const fp8bq_variant& v, int
     if ((rowwise == 1 || rowwise == 2 || rowwise == 4) && v.mma_scale != 0) return false;
     if ((rowwise == 2 || rowwise == 4) && v.kind != FP8BQ_KIND_SWAP_AB) return false;
     if (rowwise == 4 && K % BK != 0) return false;
-    if (rowwise == 3 && (v.mma_scale != 1 || K % BK != 0)) return false;
+    // block INT8 as two planes on the promotion kernel (5): mma_scale = 1, as 3
+    if ((rowwise == 3 || rowwise == 5) && (v.mma_scale != 1 || K % BK != 0)) return false;
     const bool swap = v.kind == FP8BQ_KIND_SWAP_AB || v.kind == FP8BQ_KIND_SWAP_AB_64;
     const int wm = v.kind == FP8BQ_KIND_SWAP_AB_64 ? 64 : BM;  // weight rows per swap tile
     if (v.kind != FP8BQ_KIND_SWAP_AB && v.kind != FP8BQ_KIND_NORMAL &&

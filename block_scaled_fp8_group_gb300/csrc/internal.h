@@ -95,7 +95,9 @@ struct GemmPlan {
     int rowwise;   // one scale per token and per weight row: 1 e4m3 (gemm_mx_kernel, RW 1),
                    // 2 int8 (gemm_i8_kernel), 3 int8 as two e4m3 planes (gemm_mx_kernel,
                    // RW 2; K is then the logical K, a multiple of 128); 4 block INT8 on
-                   // the warp-level MMA (gemm_i8_kernel, BLK); 0 block FP8 scales
+                   // the warp-level MMA (gemm_i8_kernel, BLK), 5 block INT8 as two e4m3
+                   // planes on the promotion kernel (gemm_kernel, PL 2; K logical); 0 block
+                   // FP8 scales
     size_t ws_bytes;
 };
 

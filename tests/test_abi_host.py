@@ -310,4 +310,9 @@ def test_int8_block_argument_errors_and_sizes():
     vn = fp8bq.make_variant("normal", 256, 1)
     assert lib.fp8bq_int8_block_variant_workspace_bytes(256, 512, 1024, ctypes.byref(vn)) == 0
     assert fp8bq.fp8bq_select_int8_block_variant(4, 4096, 7168)["block_n"] == 8
-    assert fp8bq.fp8bq_select_int8_block_variant(2048, 4096, 7168)["kind"] == "swap"
+    # above 64 tokens: two e4m3 planes on the promotion kernel (mma_scale = 1)
+    v = fp8bq.fp8bq_select_int8_block_variant(2048, 4096, 7168)
+    assert v["kind"] == "normal" and v["mma_scale"] == 1
+    vp = fp8bq.make_variant("normal", 256, 1, 0, 1)
+    assert lib.fp8bq_int8_block_variant_workspace_bytes(256, 512, 1024, ctypes.byref(vp)) == \
+        65536 + 256 * 2 * 1024 + 512 * 2 * 1024

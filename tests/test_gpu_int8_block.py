@@ -1,7 +1,8 @@
 """GPU parity of block INT8 (int8_w8a8, 1x128 activation groups, 128x128
 weight blocks, fp32 scales; "vLLM 量化 Kernel 配置机制" §1) against the oracle:
-quant codes and scales bit-exact; every GEMM kernel shape (swap-AB token
-tiles 8..128, split-K, stream-K) on ragged shapes; DeepSeek-V3 shapes at full
+quant codes and scales bit-exact; every GEMM kernel shape (warp-level int8
+MMA: swap-AB token tiles 8..128; two e4m3 planes on the promotion kernel:
+swap-AB and normal tiles; split-K, stream-K) on ragged shapes; DeepSeek-V3 shapes at full
 size on sampled rows; the linear layer (quant + GEMM in one call)."""
 import numpy as np
 import pytest
@@ -71,15 +72,24 @@ def run(fp8bq, qa, sa, qw, sw, out, variant=None):
     return o.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("bn", [8, 16, 32, 64, 128])
+VARIANTS = ([("swap", bn, 0) for bn in (8, 16, 32, 64, 128)] +
+            [("swap", bn, 1) for bn in (16, 32, 64, 128)] +
+            [("normal", bn, 1) for bn in (128, 256)])
+
+
+@pytest.mark.parametrize("kind,bn,planes", VARIANTS)
 @pytest.mark.parametrize("split", [1, 3, 0])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
-def test_gemm_int8_block_variants(fp8bq, bn, split, out):
-    # ragged: tokens past whole tiles, weight rows past a 128-row block
+def test_gemm_int8_block_variants(fp8bq, kind, bn, planes, split, out):
+    """planes=0: the warp-level int8 MMA with per-slab promotion; planes=1:
+    the codes as two e4m3 planes on the tcgen05 FP8 MMA, promoted per slab
+    on the CUDA cores.  Ragged: tokens past whole tiles, weight rows past a
+    128-row block."""
     M, N, K = 150, 400, 1024
     _, qa, sa, qw, sw = problem(M, N, K, seed=bn + split)
-    got = run(fp8bq, qa, sa, qw, sw, out, fp8bq.make_variant("swap", bn, split))
-    check_gemm(got, oracle.gemm_int8_block(qa, sa, qw, sw), out, f"int8 block swap/{bn}/s{split}")
+    got = run(fp8bq, qa, sa, qw, sw, out, fp8bq.make_variant(kind, bn, split, 0, planes))
+    check_gemm(got, oracle.gemm_int8_block(qa, sa, qw, sw), out,
+               f"int8 block {kind}/{bn}/s{split}/planes={planes}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1536, 1536), (8, 18432, 7168), (128, 7168, 18432),
