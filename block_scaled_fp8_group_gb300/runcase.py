@@ -5,6 +5,8 @@ command the profiler captures.
         --fmt ue8m0 --iters 3 [--variant swap/16/0[/grid/mma_scale]] [--op gemm|linear|quant]
     python -m block_scaled_fp8_group_gb300.runcase --m 8 --n 18432 --k 7168 \
         --op rowwise --code int8 --iters 3 [--variant swap/16/1]
+    python -m block_scaled_fp8_group_gb300.runcase --m 2048 --n 7168 --k 18432 \
+        --op int8block --iters 2
 
 Inputs are the decode-sweep distributions from ``synth`` (bf16 N(0,1) with 1%
 outlier channels, bf16 N(0,0.02) weights), quantised on the GPU.
@@ -26,7 +28,8 @@ def main():
     ap.add_argument("--k", type=int, required=True)
     ap.add_argument("--fmt", default="ue8m0", choices=("fp32", "ue8m0"))
     ap.add_argument("--out", default="bf16", choices=("bf16", "fp16", "fp32"))
-    ap.add_argument("--op", default="gemm", choices=("gemm", "linear", "quant", "rowwise"))
+    ap.add_argument("--op", default="gemm",
+                    choices=("gemm", "linear", "quant", "rowwise", "int8block"))
     ap.add_argument("--code", default="e4m3", choices=("e4m3", "int8"),
                     help="--op rowwise: per-token x per-channel codes")
     ap.add_argument("--variant", default=None,
@@ -50,6 +53,18 @@ def main():
         v = fp8bq.make_variant(parts[0], int(parts[1]), int(parts[2]),
                                int(parts[3]) if len(parts) > 3 else 0,
                                int(parts[4]) if len(parts) > 4 else 0)
+    if args.op == "int8block":
+        # block INT8: 1x128 activation groups, 128x128 weight blocks
+        xa = torch.from_numpy(synth.act_prefill(args.m, args.k).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        aq, as_ = fp8bq.fp8bq_quant_act_int8(xa)
+        wq, ws = fp8bq.fp8bq_quant_weight_int8(w)
+        for _ in range(args.iters):
+            fp8bq.fp8bq_gemm_int8_block(aq, as_, wq, ws, out_dt, variant=v)
+        torch.cuda.synchronize()
+        if fp8bq.fp8bq_device_status() != 0:
+            raise SystemExit("device wait timed out")
+        return
     if args.op == "rowwise":
         wq, ws = fp8bq.fp8bq_quant_rows(w, args.code)
         aq, as_ = fp8bq.fp8bq_quant_rows(x, args.code)
