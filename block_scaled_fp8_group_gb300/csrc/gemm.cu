@@ -8,6 +8,19 @@
 // accumulator); "用 Helion 为 vLLM 构建高性能可移植线性后端", 内核实现, the
 // Split-K and Swap-AB variants.
 //
+// Kernels in this file (the host picks one per plan, GemmPlan::rowwise/mx):
+//   gemm_kernel     promotion on the CUDA cores (fp32 or UE8M0 scales);
+//                   GR: grouped (MoE) tiles; PL = 2: block INT8 as two e4m3
+//                   planes (four cross products per K step)
+//   gemm_mx_kernel  block-scaled MMA for UE8M0 scales; FQ: activation quant
+//                   fused into the producer; RW = 1: rowwise (FP8_Dynamic)
+//                   scales applied in the epilogue; RW = 2: rowwise INT8 as
+//                   two e4m3 planes
+//   gemm_i8_kernel  warp-level int8 MMA (mma.sync), rowwise INT8 or (BLK)
+//                   block INT8 with per-slab promotion
+// All share the work schedule (WorkIter: split-K items or stream-K shares),
+// the tile origins, the bounded waits and the split-part ticket protocol.
+//
 // Design (one CTA per SM, persistent over its work):
 //   warp 0     TMA producer: per K slab, one 128x128 tile of the MMA-M operand
 //              and one BNx128 tile of the MMA-N operand into a STAGES-deep
