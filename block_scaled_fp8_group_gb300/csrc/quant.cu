@@ -292,8 +292,24 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const QuantRows
 // ------------------------------------------------------------ int8 planes
 //
 // One CTA per row; a thread turns 16 int8 codes (one 16-byte load) into 16
-// codes of 16 h and 16 codes of l (two 16-byte stores).  Every value is an
-// integer of at most 4 significant bits, so the e4m3 conversion is exact.
+// codes of 16 h and 16 codes of l (two 16-byte stores).  Each nibble indexes
+// a 16-entry table of e4m3 codes, four bytes at a time with byte permutes:
+//   l = q & 15        -> e4m3(l):          0, 1, 2, ..., 15
+//   h = q >> 4 (signed) -> e4m3(16 h) for the nibble 0..7 (h = 0..7) and
+//                        8..15 (h = -8..-1)
+// (the entries are the OCP e4m3 encodings of those exact integers: bias 7,
+// three mantissa bits).
+__device__ __forceinline__ uint32_t nibble_lut(uint32_t n, uint32_t t0, uint32_t t1, uint32_t t2,
+                                               uint32_t t3) {
+    // n: four nibbles, one in the low half of each byte
+    const uint32_t sel = (n & 0x7u) | ((n >> 4) & 0x70u) | ((n >> 8) & 0x700u) |
+                         ((n >> 12) & 0x7000u);  // low three index bits, a nibble per byte
+    const uint32_t lo = __byte_perm(t0, t1, sel);  // entries 0..7
+    const uint32_t hi = __byte_perm(t2, t3, sel);  // entries 8..15
+    const uint32_t m = ((n >> 3) & 0x01010101u) * 0xFFu;  // bytes whose index is >= 8
+    return (lo & ~m) | (hi & m);
+}
+
 __global__ void __launch_bounds__(kRowThreads) int8_planes_kernel(const Int8PlanesArgs a) {
     pdl_wait_prior_grid();
     pdl_launch_dependents();
@@ -309,15 +325,10 @@ __global__ void __launch_bounds__(kRowThreads) int8_planes_kernel(const Int8Plan
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float h[4], l[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int b = static_cast<int>(static_cast<int8_t>((w[i] >> (8 * j)) & 0xFFu));
-                h[j] = static_cast<float>(16 * (b >> 4));  // arithmetic shift: floor(b / 16)
-                l[j] = static_cast<float>(b & 15);
-            }
-            hi[i] = cvt2_e4m3(h[0], h[1]) | (cvt2_e4m3(h[2], h[3]) << 16);
-            lo[i] = cvt2_e4m3(l[0], l[1]) | (cvt2_e4m3(l[2], l[3]) << 16);
+            lo[i] = nibble_lut(w[i] & 0x0F0F0F0Fu, 0x44403800u, 0x4E4C4A48u, 0x53525150u,
+                               0x57565554u);
+            hi[i] = nibble_lut((w[i] >> 4) & 0x0F0F0F0Fu, 0x64605800u, 0x6E6C6A68u, 0xEAECEEF0u,
+                               0xD8E0E4E8u);
         }
         // slab kb = c / 8 starts at 256 kb; the chunk sits at 16 (c % 8) inside
         const int64_t o = static_cast<int64_t>(c >> 3) * 256 + (c & 7) * 16;
