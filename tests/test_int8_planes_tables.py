@@ -17,8 +17,8 @@ def kernel_tables():
     tabs = []
     for c in calls:
         words = re.findall(r"0x([0-9A-Fa-f]{8})u", c)
-        if len(words) == 4:
-            tabs.append([int(w, 16) for w in words])
+        if len(words) >= 4:  # the nibble mask, then the table's four words
+            tabs.append([int(w, 16) for w in words[-4:]])
     assert len(tabs) == 2, "expected the l table and the 16h table"
     return tabs  # [l table, 16h table], in the order of the kernel's calls
 
