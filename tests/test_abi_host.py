@@ -316,3 +316,37 @@ def test_int8_block_argument_errors_and_sizes():
     vp = fp8bq.make_variant("normal", 256, 1, 0, 1)
     assert lib.fp8bq_int8_block_variant_workspace_bytes(256, 512, 1024, ctypes.byref(vp)) == \
         65536 + 256 * 2 * 1024 + 512 * 2 * 1024
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/fp8bq.h compiles as C11 and a C program links against the
+    library and calls it (no C++ or torch types at the boundary)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "t.c"
+    src.write_text(
+        '#include "fp8bq.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "    fp8bq_variant v;\n"
+        "    if (fp8bq_abi_version() != 1) return 1;\n"
+        "    /* a host-side argument error, no GPU needed */\n"
+        "    if (fp8bq_select_variant(16, 100, 256, FP8BQ_SCALE_FP32, FP8BQ_BF16, &v)\n"
+        "        != FP8BQ_ERR_SHAPE) return 2;\n"
+        "    printf(\"%s\\n\", fp8bq_status_string(FP8BQ_ERR_SHAPE));\n"
+        "    return 0;\n"
+        "}\n")
+    exe = tmp_path / "t"
+    libdir = os.path.dirname(fp8bq.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror=implicit-function-declaration",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src),
+                        "-L", libdir, "-lfp8bq", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip()
