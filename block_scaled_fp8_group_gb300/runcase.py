@@ -7,6 +7,8 @@ command the profiler captures.
         --op rowwise --code int8 --iters 3 [--variant swap/16/1]
     python -m block_scaled_fp8_group_gb300.runcase --m 2048 --n 7168 --k 18432 \
         --op int8block --iters 2
+    python -m block_scaled_fp8_group_gb300.runcase --m 0 --n 4096 --k 7168 \
+        --op grouped --tokens 128 --iters 2
 
 Inputs are the decode-sweep distributions from ``synth`` (bf16 N(0,1) with 1%
 outlier channels, bf16 N(0,0.02) weights), quantised on the GPU.
@@ -29,7 +31,10 @@ def main():
     ap.add_argument("--fmt", default="ue8m0", choices=("fp32", "ue8m0"))
     ap.add_argument("--out", default="bf16", choices=("bf16", "fp16", "fp32"))
     ap.add_argument("--op", default="gemm",
-                    choices=("gemm", "linear", "quant", "rowwise", "int8block"))
+                    choices=("gemm", "linear", "quant", "rowwise", "int8block", "grouped"))
+    ap.add_argument("--tokens", type=int, default=128,
+                    help="--op grouped: tokens routed top-8 over 32 local experts of 256 "
+                         "(--n/--k: one expert's projection)")
     ap.add_argument("--code", default="e4m3", choices=("e4m3", "int8"),
                     help="--op rowwise: per-token x per-channel codes")
     ap.add_argument("--variant", default=None,
@@ -44,6 +49,27 @@ def main():
         for _ in range(args.iters):
             fp8bq.fp8bq_quant_act(x, args.fmt)
         torch.cuda.synchronize()
+        return
+    if args.op == "grouped":
+        # the MoE workload's grouped GEMM: E experts, counts from seeded routing
+        E = synth.MOE_E_LOCAL
+        counts = synth.moe_counts(E, args.tokens)
+        M_max = int((counts.max() + 3) // 4 * 4)
+        xg = torch.from_numpy(synth.moe_act(E, M_max, args.k).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        wb = synth.moe_weight_bf16(E, args.n, args.k)
+        wq = torch.empty((E, args.n, args.k), dtype=torch.uint8, device=dev)
+        ws = torch.empty((E, args.n // 128, args.k // 128), dtype=torch.float32, device=dev)
+        for e in range(E):
+            wd = torch.from_numpy(wb[e].view(np.int16)).view(torch.bfloat16).to(dev)
+            fp8bq.fp8bq_quant_weight(wd, args.fmt, q=wq[e], s=ws[e])
+        aq, as_ = fp8bq.fp8bq_quant_act(xg, args.fmt)
+        cnt = torch.from_numpy(counts).to(dev)
+        for _ in range(args.iters):
+            fp8bq.fp8bq_grouped_gemm(aq, as_, wq, ws, cnt, fmt=args.fmt, out_dtype=out_dt)
+        torch.cuda.synchronize()
+        if fp8bq.fp8bq_device_status() != 0:
+            raise SystemExit("device wait timed out")
         return
     w = torch.from_numpy(synth.weight_bf16(args.n, args.k).view(np.int16)).view(
         torch.bfloat16).to(dev)
