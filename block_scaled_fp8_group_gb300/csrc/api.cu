@@ -126,9 +126,14 @@ std::string table_path(const std::string& device_name) {
     return library_dir() + "/../tables/" + device_name + ".tbl";
 }
 
+// Table-only format code of the rowwise e4m3 GEMM (FP8_Dynamic): its own
+// measured shapes, "rw8" in the table file.
+constexpr int kTableRowwiseE4m3 = 2;
+
 int parse_fmt(const char* s) {
     if (!std::strcmp(s, "fp32")) return FP8BQ_SCALE_FP32;
     if (!std::strcmp(s, "ue8m0")) return FP8BQ_SCALE_UE8M0;
+    if (!std::strcmp(s, "rw8")) return kTableRowwiseE4m3;
     return -1;
 }
 int parse_out(const char* s) {
@@ -208,24 +213,39 @@ fp8bq_variant default_variant(int64_t M, int64_t N, int64_t K, int fmt, int num_
     return v;
 }
 
+// Nearest-M entry of (N, K, fmt, out) in the table; caller holds the lock.
+bool table_lookup_locked(int64_t M, int64_t N, int64_t K, int fmt, int out, fp8bq_variant* v) {
+    const TableKey key(N, K, fmt, out);
+    auto it = g_table.rows.find(key);
+    if (it == g_table.rows.end() || it->second.empty()) return false;
+    const fp8bq_variant* best = nullptr;
+    int64_t best_d = 0;
+    for (const auto& kv : it->second) {  // ascending M: strict '<' keeps the smaller on ties
+        const int64_t d = kv.first > M ? kv.first - M : M - kv.first;
+        if (!best || d < best_d) {
+            best = &kv.second;
+            best_d = d;
+        }
+    }
+    *v = *best;
+    return true;
+}
+
+// The table's entry for the rowwise e4m3 GEMM, if it has the shape.
+bool rowwise_table_lookup(int64_t M, int64_t N, int64_t K, int out,
+                          const std::string& device_name, fp8bq_variant* v) {
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    if (!g_table.loaded) load_table_locked(device_name);
+    return table_lookup_locked(M, N, K, kTableRowwiseE4m3, out, v);
+}
+
 fp8bq_variant select_variant(int64_t M, int64_t N, int64_t K, int fmt, int out,
                              const std::string& device_name, int num_sms) {
     std::lock_guard<std::mutex> lock(g_table_mutex);
     if (!g_table.loaded) load_table_locked(device_name);
     const TableKey key(N, K, fmt, out);
-    auto it = g_table.rows.find(key);
-    if (it != g_table.rows.end() && !it->second.empty()) {
-        const fp8bq_variant* best = nullptr;
-        int64_t best_d = 0;
-        for (const auto& kv : it->second) {  // ascending M: strict '<' keeps the smaller on ties
-            const int64_t d = kv.first > M ? kv.first - M : M - kv.first;
-            if (!best || d < best_d) {
-                best = &kv.second;
-                best_d = d;
-            }
-        }
-        return *best;
-    }
+    fp8bq_variant hit;
+    if (table_lookup_locked(M, N, K, fmt, out, &hit)) return hit;
     if (g_table.logged.insert(key).second) {
         const char* e = std::getenv("FP8BQ_LOG");
         if (e && std::atoi(e) == 1)
@@ -349,6 +369,12 @@ constexpr int64_t kInt8PlanesMinM = 65;
 // (the FP8-plane kernel); smaller M: swap-AB with the token tile covering M.
 fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out_dtype,
                               const std::string& device_name, int num_sms) {
+    fp8bq_variant measured;
+    if (code == FP8BQ_CODE_E4M3 &&
+        rowwise_table_lookup(M, N, K, out_dtype, device_name, &measured) &&
+        measured.mma_scale == 0 && measured.kind != FP8BQ_KIND_SWAP_AB_64 &&
+        measured.split <= (K + kGroup - 1) / kGroup)
+        return measured;  // shapes measured for the rowwise kernel itself
     fp8bq_variant v = code == FP8BQ_CODE_E4M3
                           ? select_variant(M, N, K, FP8BQ_SCALE_UE8M0, out_dtype, device_name,
                                            num_sms)

@@ -2,7 +2,7 @@
 §3: per (N, K, device, dtype) and per point of the M grid, time every candidate
 kernel configuration and keep the fastest).
 
-    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small \
+    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small,rowwise \
         [--out block_scaled_fp8_group_gb300/tables/<device>.tbl]
 
 Candidates per M: swap-AB with token tiles 16..128 (and 64 weight rows per
@@ -37,6 +37,9 @@ SETS = {
     "prefill": [(n, k, "fp32", o, synth.PREFILL_M) for n, k in synth.PREFILL_NK
                 for o in ("bf16", "fp32")],
     "full": [(n, k, "ue8m0", o, synth.M_GRID) for n, k in synth.FULL_NK for o in ("fp16", "bf16")],
+    # the rowwise e4m3 GEMM (FP8_Dynamic: one scale per token and per weight
+    # row), table format "rw8": the decode sweep's shapes plus two large M
+    "rowwise": [(n, k, "rw8", "bf16", synth.DECODE_M + (2048, 4096)) for n, k in synth.DECODE_NK],
 }
 
 
@@ -46,9 +49,11 @@ def device_table_path() -> str:
 
 
 def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
-    """(kind, block_n, split, mma_scale) tuples."""
+    """(kind, block_n, split, mma_scale) tuples (rw8: the rowwise kernel has
+    neither the block-scaled MMA nor 64-row tiles)."""
     G = K // 128
     mx = fmt == "ue8m0" and K % 512 == 0
+    rw = fmt == "rw8"
     out = []
     if M <= 128:
         tok = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
@@ -57,7 +62,7 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
             for split in (0, 1, 2, 3, 4, 6, 8):
                 if split <= G:
                     out += [("swap", bn, split, m) for m in ((0, 1) if mx else (0,))]
-                    if bn <= 32:
+                    if bn <= 32 and not rw:
                         out.append(("swap64", bn, split, 0))
     else:
         for bn in (128, 256):
@@ -68,10 +73,18 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
     return out
 
 
+def run_variant(aq, as_, wq, ws, v, fmt, out_dt, out, ws_buf):
+    if fmt == "rw8":
+        fp8bq.fp8bq_gemm_rowwise(aq, as_, wq, ws, "e4m3", out_dt, out=out, workspace=ws_buf,
+                                 variant=v)
+    else:
+        fp8bq.fp8bq_gemm_variant(aq, as_, wq, ws, v, fmt=fmt, out_dtype=out_dt, out=out,
+                                 workspace=ws_buf)
+
+
 def time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf, batch=24, reps=3):
     for c in copies[:2]:
-        fp8bq.fp8bq_gemm_variant(aq, as_, c, ws, v, fmt=fmt, out_dtype=out_dt, out=out,
-                                 workspace=ws_buf)
+        run_variant(aq, as_, c, ws, v, fmt, out_dt, out, ws_buf)
     torch.cuda.synchronize()
     best = None
     for _ in range(reps):
@@ -80,8 +93,7 @@ def time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf, batch=24, rep
         torch.cuda._sleep(1_000_000)
         a.record()
         for i in range(batch):
-            fp8bq.fp8bq_gemm_variant(aq, as_, copies[i % len(copies)], ws, v, fmt=fmt,
-                                     out_dtype=out_dt, out=out, workspace=ws_buf)
+            run_variant(aq, as_, copies[i % len(copies)], ws, v, fmt, out_dt, out, ws_buf)
         b.record()
         b.synchronize()
         t = a.elapsed_time(b) * 1e3 / batch
@@ -93,19 +105,21 @@ def tune_shape(N, K, fmt, out_name, Ms, log):
     dev = torch.device("cuda")
     out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_name]
     w = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
-    wq, ws = fp8bq.fp8bq_quant_weight(w, fmt)
+    rw = fmt == "rw8"
+    wq, ws = fp8bq.fp8bq_quant_rows(w, "e4m3") if rw else fp8bq.fp8bq_quant_weight(w, fmt)
     del w
     n_copies = max(2, int(np.ceil(L2_BYTES / (N * K))) + 1)
     copies = [wq] + [wq.clone() for _ in range(n_copies - 1)]
     rows = []
     for M in Ms:
         x = torch.from_numpy(synth.act_decode(M, K).view(np.int16)).view(torch.bfloat16).to(dev)
-        aq, as_ = fp8bq.fp8bq_quant_act(x, fmt)
+        aq, as_ = fp8bq.fp8bq_quant_rows(x, "e4m3") if rw else fp8bq.fp8bq_quant_act(x, fmt)
         out = torch.empty((M, N), dtype=out_dt, device=dev)
         results = []
         for kind, bn, split, mx in candidates(M, N, K, fmt):
             v = fp8bq.make_variant(kind, bn, split, 0, mx)
-            need = fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v)
+            need = (fp8bq.fp8bq_rowwise_variant_workspace_bytes(M, N, K, "e4m3", v) if rw
+                    else fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v))
             if need == 0 and split != 1:
                 continue  # not supported for this shape (e.g. too many tiles for tickets)
             ws_buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
