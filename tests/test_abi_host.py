@@ -350,3 +350,30 @@ def test_header_is_plain_c_and_links(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.strip()
+
+
+def test_rowwise_table_entries(tmp_path, monkeypatch):
+    """rw8 lines of the table give the rowwise e4m3 GEMM its own measured
+    shapes (nearest M); int8 and block-path lookups ignore them."""
+    t = tmp_path / "rw.tbl"
+    t.write_text("7168 18432 rw8 bf16 1 swap 16 2 0 0\n"
+                 "7168 18432 rw8 bf16 64 swap 64 2 0 0\n"
+                 "7168 18432 ue8m0 bf16 1 swap 16 8 0 1\n")
+    monkeypatch.setenv("FP8BQ_TABLE", str(t))
+    fp8bq.fp8bq_reload_table()
+    try:
+        v = fp8bq.fp8bq_select_rowwise_variant(4, 7168, 18432, "e4m3", "bf16")
+        assert (v["kind"], v["block_n"], v["split"], v["from_table"]) == ("swap", 16, 2, True)
+        v = fp8bq.fp8bq_select_rowwise_variant(50, 7168, 18432, "e4m3", "bf16")
+        assert (v["block_n"], v["split"]) == (64, 2)
+        # other (N, K) or output dtype: no rw8 entry, the block path's shape / default
+        v = fp8bq.fp8bq_select_rowwise_variant(4, 7168, 18432, "e4m3", "fp16")
+        assert v["mma_scale"] == 0 and v["from_table"] is False
+        # the block path keeps its own entry
+        v = fp8bq.fp8bq_select_variant(1, 7168, 18432, "ue8m0", "bf16")
+        assert (v["split"], v["mma_scale"]) == (8, 1)
+        # int8 never takes e4m3 shapes
+        assert fp8bq.fp8bq_select_rowwise_variant(4, 7168, 18432, "int8", "bf16")["block_n"] == 8
+    finally:
+        monkeypatch.delenv("FP8BQ_TABLE")
+        fp8bq.fp8bq_reload_table()
