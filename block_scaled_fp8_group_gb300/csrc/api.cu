@@ -126,14 +126,19 @@ std::string table_path(const std::string& device_name) {
     return library_dir() + "/../tables/" + device_name + ".tbl";
 }
 
-// Table-only format code of the rowwise e4m3 GEMM (FP8_Dynamic): its own
-// measured shapes, "rw8" in the table file.
+// Table-only format codes of the other GEMMs, each with its own measured
+// shapes: rowwise e4m3 (FP8_Dynamic) "rw8", rowwise INT8 "ri8", block INT8
+// "bi8" (for INT8, mma_scale 1 = the two-plane kernel).
 constexpr int kTableRowwiseE4m3 = 2;
+constexpr int kTableRowwiseInt8 = 3;
+constexpr int kTableBlockInt8 = 4;
 
 int parse_fmt(const char* s) {
     if (!std::strcmp(s, "fp32")) return FP8BQ_SCALE_FP32;
     if (!std::strcmp(s, "ue8m0")) return FP8BQ_SCALE_UE8M0;
     if (!std::strcmp(s, "rw8")) return kTableRowwiseE4m3;
+    if (!std::strcmp(s, "ri8")) return kTableRowwiseInt8;
+    if (!std::strcmp(s, "bi8")) return kTableBlockInt8;
     return -1;
 }
 int parse_out(const char* s) {
@@ -231,12 +236,12 @@ bool table_lookup_locked(int64_t M, int64_t N, int64_t K, int fmt, int out, fp8b
     return true;
 }
 
-// The table's entry for the rowwise e4m3 GEMM, if it has the shape.
-bool rowwise_table_lookup(int64_t M, int64_t N, int64_t K, int out,
-                          const std::string& device_name, fp8bq_variant* v) {
+// The table's entry for one of the table-only formats, if it has the shape.
+bool format_table_lookup(int table_fmt, int64_t M, int64_t N, int64_t K, int out,
+                         const std::string& device_name, fp8bq_variant* v) {
     std::lock_guard<std::mutex> lock(g_table_mutex);
     if (!g_table.loaded) load_table_locked(device_name);
-    return table_lookup_locked(M, N, K, kTableRowwiseE4m3, out, v);
+    return table_lookup_locked(M, N, K, table_fmt, out, v);
 }
 
 fp8bq_variant select_variant(int64_t M, int64_t N, int64_t K, int fmt, int out,
@@ -369,12 +374,16 @@ constexpr int64_t kInt8PlanesMinM = 65;
 // (the FP8-plane kernel); smaller M: swap-AB with the token tile covering M.
 fp8bq_variant rowwise_variant(int64_t M, int64_t N, int64_t K, int code, int out_dtype,
                               const std::string& device_name, int num_sms) {
+    // shapes measured for the rowwise kernels themselves (checked as the
+    // planner would: a stale or hand-edited entry falls through)
     fp8bq_variant measured;
-    if (code == FP8BQ_CODE_E4M3 &&
-        rowwise_table_lookup(M, N, K, out_dtype, device_name, &measured) &&
-        measured.mma_scale == 0 && measured.kind != FP8BQ_KIND_SWAP_AB_64 &&
-        measured.split <= (K + kGroup - 1) / kGroup)
-        return measured;  // shapes measured for the rowwise kernel itself
+    const int tfmt = code == FP8BQ_CODE_E4M3 ? kTableRowwiseE4m3 : kTableRowwiseInt8;
+    if (format_table_lookup(tfmt, M, N, K, out_dtype, device_name, &measured)) {
+        GemmPlan probe;
+        const int mode = code == FP8BQ_CODE_E4M3 ? 1 : (measured.mma_scale ? 3 : 2);
+        const int64_t Kg = mode == 3 ? (K + kGroup - 1) / kGroup * kGroup : K;
+        if (make_gemm_plan(M, N, Kg, measured, num_sms, &probe, 0, mode)) return measured;
+    }
     fp8bq_variant v = code == FP8BQ_CODE_E4M3
                           ? select_variant(M, N, K, FP8BQ_SCALE_UE8M0, out_dtype, device_name,
                                            num_sms)
@@ -523,7 +532,14 @@ fp8bq_status check_int8_block_args(int64_t M, int64_t N, int64_t K, int out_dtyp
 
 // swap-AB on the warp-level int8 MMA: the token tile covering M (8 up to 8
 // tokens), 128-token tiles above 128; split-K / stream-K as the FP8 default
-fp8bq_variant int8_block_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
+fp8bq_variant int8_block_variant(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
+                                 const std::string& device_name) {
+    fp8bq_variant measured;
+    if (format_table_lookup(kTableBlockInt8, M, N, K, out_dtype, device_name, &measured)) {
+        GemmPlan probe;
+        if (make_gemm_plan(M, N, K, measured, num_sms, &probe, 0, measured.mma_scale ? 5 : 4))
+            return measured;
+    }
     fp8bq_variant v = default_variant(M, N, K, FP8BQ_SCALE_FP32, num_sms);
     if (M >= kInt8PlanesMinM) {
         // two e4m3 planes on the promotion kernel, the default tile; whole
@@ -545,6 +561,11 @@ fp8bq_variant int8_block_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
 int host_sms() {
     DeviceInfo* d = nullptr;
     return device_info(&d) == FP8BQ_OK ? d->num_sms : 152;  // GB300 without a visible GPU
+}
+
+std::string host_device_name() {
+    DeviceInfo* d = nullptr;
+    return device_info(&d) == FP8BQ_OK ? d->name : std::string();
 }
 
 }  // namespace
@@ -1180,7 +1201,7 @@ fp8bq_status fp8bq_select_int8_block_variant(int64_t M, int64_t N, int64_t K,
     if (!variant) return FP8BQ_ERR_INVALID_ARG;
     fp8bq_status st = check_int8_block_args(M, N, K, out_dtype);
     if (st != FP8BQ_OK) return st;
-    *variant = int8_block_variant(M, N, K, host_sms());
+    *variant = int8_block_variant(M, N, K, out_dtype, host_sms(), host_device_name());
     return FP8BQ_OK;
 }
 
@@ -1198,7 +1219,7 @@ size_t fp8bq_int8_block_variant_workspace_bytes(int64_t M, int64_t N, int64_t K,
 
 size_t fp8bq_int8_block_workspace_bytes(int64_t M, int64_t N, int64_t K, fp8bq_dtype out_dtype) {
     if (check_int8_block_args(M, N, K, out_dtype) != FP8BQ_OK) return 0;
-    const fp8bq_variant v = int8_block_variant(M, N, K, host_sms());
+    const fp8bq_variant v = int8_block_variant(M, N, K, out_dtype, host_sms(), host_device_name());
     return fp8bq_int8_block_variant_workspace_bytes(M, N, K, &v);
 }
 
@@ -1232,7 +1253,7 @@ fp8bq_status fp8bq_gemm_int8_block(int64_t M, int64_t N, int64_t K, const void* 
     if (M == 0 || N == 0) return FP8BQ_OK;
     st = check_gemm_ptrs(a_q, a_s, w_q, w_s, out);
     if (st != FP8BQ_OK) return st;
-    const fp8bq_variant v = int8_block_variant(M, N, K, host_sms());
+    const fp8bq_variant v = int8_block_variant(M, N, K, out_dtype, host_sms(), host_device_name());
     return fp8bq_gemm_int8_block_variant(M, N, K, a_q, a_s, w_q, w_s, out_dtype, out, &v,
                                          workspace, workspace_bytes, stream);
 }
@@ -1264,7 +1285,7 @@ fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    const fp8bq_variant v = int8_block_variant(M, N, K, d->num_sms);
+    const fp8bq_variant v = int8_block_variant(M, N, K, out_dtype, d->num_sms, d->name);
     // workspace: [counter prefix][codes][scales][split parts][planes (above 64 tokens)]
     const size_t q_bytes = align256(static_cast<size_t>(M * K));
     const size_t s_bytes = align256(fp8bq_act_scale_bytes(M, K, kGroup, FP8BQ_SCALE_FP32));

@@ -19,6 +19,7 @@ mma_scale.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import os
 import time
 
@@ -40,7 +41,15 @@ SETS = {
     # the rowwise e4m3 GEMM (FP8_Dynamic: one scale per token and per weight
     # row), table format "rw8": the decode sweep's shapes plus two large M
     "rowwise": [(n, k, "rw8", "bf16", synth.DECODE_M + (2048, 4096)) for n, k in synth.DECODE_NK],
+    # rowwise INT8 ("ri8") and block INT8 ("bi8"): both INT8 kernels compete
+    # (warp-level int8 MMA, mma_scale 0; two e4m3 planes, mma_scale 1)
+    "rowwise_int8": [(n, k, "ri8", "bf16", synth.DECODE_M + (2048, 4096))
+                     for n, k in synth.DECODE_NK],
+    "block_int8": [(n, k, "bi8", "bf16", synth.DECODE_M + (2048, 4096))
+                   for n, k in synth.DECODE_NK],
 }
+
+INT8_FMTS = ("ri8", "bi8")
 
 
 def device_table_path() -> str:
@@ -52,6 +61,8 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
     """(kind, block_n, split, mma_scale) tuples (rw8: the rowwise kernel has
     neither the block-scaled MMA nor 64-row tiles)."""
     G = K // 128
+    if fmt in INT8_FMTS:
+        return int8_candidates(M, G)
     mx = fmt == "ue8m0" and K % 512 == 0
     rw = fmt == "rw8"
     out = []
@@ -73,8 +84,34 @@ def candidates(M: int, N: int, K: int, fmt: str = "fp32"):
     return out
 
 
+def int8_candidates(M: int, G: int):
+    """INT8: the warp-level kernel (swap-AB, token tiles from 8) up to 128
+    tokens, the two-plane kernel from 32 tokens (swap-AB, and normal tiles
+    above 128 tokens)."""
+    out = []
+    splits = [sp for sp in (0, 1, 2, 3, 4, 6, 8) if sp <= G]
+    if M <= 128:
+        tok = 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+        for bn in sorted({tok, max(8, tok // 2)}):
+            out += [("swap", bn, sp, 0) for sp in splits]
+        if M >= 32:
+            for bn in sorted({max(16, tok), max(16, tok // 2)}):
+                out += [("swap", bn, sp, 1) for sp in (0, 1, 2) if sp <= G]
+    else:
+        for bn in (128, 256):
+            out += [("normal", bn, sp, 1) for sp in (0, 1, 2) if sp <= G]
+        out += [("swap", 128, sp, 1) for sp in (0, 1) if sp <= G]
+    return out
+
+
 def run_variant(aq, as_, wq, ws, v, fmt, out_dt, out, ws_buf):
-    if fmt == "rw8":
+    if fmt == "ri8":
+        fp8bq.fp8bq_gemm_rowwise(aq, as_, wq, ws, "int8", out_dt, out=out, workspace=ws_buf,
+                                 variant=v)
+    elif fmt == "bi8":
+        fp8bq.fp8bq_gemm_int8_block(aq, as_, wq, ws, out_dt, out=out, workspace=ws_buf,
+                                    variant=v)
+    elif fmt == "rw8":
         fp8bq.fp8bq_gemm_rowwise(aq, as_, wq, ws, "e4m3", out_dt, out=out, workspace=ws_buf,
                                  variant=v)
     else:
@@ -106,20 +143,41 @@ def tune_shape(N, K, fmt, out_name, Ms, log):
     out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_name]
     w = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
     rw = fmt == "rw8"
-    wq, ws = fp8bq.fp8bq_quant_rows(w, "e4m3") if rw else fp8bq.fp8bq_quant_weight(w, fmt)
+    if fmt == "ri8":
+        wq, ws = fp8bq.fp8bq_quant_rows(w, "int8")
+    elif fmt == "bi8":
+        wq, ws = fp8bq.fp8bq_quant_weight_int8(w)
+    elif rw:
+        wq, ws = fp8bq.fp8bq_quant_rows(w, "e4m3")
+    else:
+        wq, ws = fp8bq.fp8bq_quant_weight(w, fmt)
     del w
     n_copies = max(2, int(np.ceil(L2_BYTES / (N * K))) + 1)
     copies = [wq] + [wq.clone() for _ in range(n_copies - 1)]
     rows = []
     for M in Ms:
         x = torch.from_numpy(synth.act_decode(M, K).view(np.int16)).view(torch.bfloat16).to(dev)
-        aq, as_ = fp8bq.fp8bq_quant_rows(x, "e4m3") if rw else fp8bq.fp8bq_quant_act(x, fmt)
+        if fmt == "ri8":
+            aq, as_ = fp8bq.fp8bq_quant_rows(x, "int8")
+        elif fmt == "bi8":
+            aq, as_ = fp8bq.fp8bq_quant_act_int8(x)
+        elif rw:
+            aq, as_ = fp8bq.fp8bq_quant_rows(x, "e4m3")
+        else:
+            aq, as_ = fp8bq.fp8bq_quant_act(x, fmt)
         out = torch.empty((M, N), dtype=out_dt, device=dev)
         results = []
         for kind, bn, split, mx in candidates(M, N, K, fmt):
             v = fp8bq.make_variant(kind, bn, split, 0, mx)
-            need = (fp8bq.fp8bq_rowwise_variant_workspace_bytes(M, N, K, "e4m3", v) if rw
-                    else fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v))
+            if fmt == "ri8":
+                need = fp8bq.fp8bq_rowwise_variant_workspace_bytes(M, N, K, "int8", v)
+            elif fmt == "bi8":
+                need = fp8bq.lib().fp8bq_int8_block_variant_workspace_bytes(M, N, K,
+                                                                            ctypes.byref(v))
+            elif rw:
+                need = fp8bq.fp8bq_rowwise_variant_workspace_bytes(M, N, K, "e4m3", v)
+            else:
+                need = fp8bq.fp8bq_variant_workspace_bytes(M, N, K, v)
             if need == 0 and split != 1:
                 continue  # not supported for this shape (e.g. too many tiles for tickets)
             ws_buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)

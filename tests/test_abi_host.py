@@ -377,3 +377,48 @@ def test_rowwise_table_entries(tmp_path, monkeypatch):
     finally:
         monkeypatch.delenv("FP8BQ_TABLE")
         fp8bq.fp8bq_reload_table()
+
+
+def test_int8_table_entries(tmp_path, monkeypatch):
+    """ri8 / bi8 lines give the rowwise INT8 and block INT8 GEMMs measured
+    shapes, including the choice between the warp-level kernel (mma_scale 0)
+    and the two e4m3 planes (mma_scale 1); an entry the planner rejects falls
+    through to the fixed rule."""
+    t = tmp_path / "i8.tbl"
+    t.write_text("7168 18432 ri8 bf16 32 swap 32 3 0 1\n"
+                 "7168 18432 ri8 bf16 96 swap 64 4 0 0\n"
+                 "7168 18432 bi8 bf16 16 swap 16 6 0 0\n"
+                 "7168 18432 bi8 bf16 2048 swap 128 1 0 1\n"
+                 # block_n 8 only exists on the warp-level kernel
+                 "2112 7168 bi8 bf16 4 swap 8 1 0 1\n")
+    monkeypatch.setenv("FP8BQ_TABLE", str(t))
+    fp8bq.fp8bq_reload_table()
+    try:
+        v = fp8bq.fp8bq_select_rowwise_variant(32, 7168, 18432, "int8", "bf16")
+        assert (v["kind"], v["block_n"], v["split"], v["mma_scale"], v["from_table"]) == \
+            ("swap", 32, 3, 1, True)
+        # nearest M: 100 tokens take the 96-token line (warp-level kernel above
+        # the fixed 65-token planes threshold)
+        v = fp8bq.fp8bq_select_rowwise_variant(100, 7168, 18432, "int8", "bf16")
+        assert (v["block_n"], v["split"], v["mma_scale"]) == (64, 4, 0)
+        # e4m3 ignores INT8 lines
+        assert fp8bq.fp8bq_select_rowwise_variant(32, 7168, 18432, "e4m3", "bf16")[
+            "from_table"] is False
+        v = fp8bq.fp8bq_select_int8_block_variant(16, 7168, 18432, "bf16")
+        assert (v["block_n"], v["split"], v["mma_scale"], v["from_table"]) == (16, 6, 0, True)
+        v = fp8bq.fp8bq_select_int8_block_variant(3000, 7168, 18432, "bf16")
+        assert (v["kind"], v["block_n"], v["mma_scale"]) == ("swap", 128, 1)
+        # the workspace query follows the table's choice: planes need room
+        # for both operands' planes, the warp-level kernel none
+        ws_planes = fp8bq.lib().fp8bq_int8_block_workspace_bytes(3000, 7168, 18432,
+                                                                 fp8bq._dtype_code("bf16"))
+        assert ws_planes >= 2 * 18432 * (3000 + 7168)
+        # rejected entry (8-token tile on the planes kernel): the fixed rule
+        v = fp8bq.fp8bq_select_int8_block_variant(4, 2112, 7168, "bf16")
+        assert (v["block_n"], v["mma_scale"], v["from_table"]) == (8, 0, False)
+        # fp16 output: no entry
+        assert fp8bq.fp8bq_select_int8_block_variant(16, 7168, 18432, "fp16")[
+            "from_table"] is False
+    finally:
+        monkeypatch.delenv("FP8BQ_TABLE")
+        fp8bq.fp8bq_reload_table()
