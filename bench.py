@@ -765,9 +765,10 @@ def run_gpu_rowwise(args, rank, world):
     achieved = tot / (gemm_us.sum() * 1e-6) / 1e9
     step_total = sum(fc.step_bytes(*p) for p in probs)
     kern = {"e4m3": "gemm_mx_kernel (rowwise: plain kind::f8f6f4, scales in the epilogue)",
-            "int8": "gemm_i8_kernel (mma.sync m16n8k32 s8, TMA-fed) up to 64 tokens, "
-                    "gemm_mx_kernel on two e4m3 planes above",
-            "int8block": "gemm_i8_kernel, block promotion per K slab (mma.sync m16n8k32 s8)"}[code]
+            "int8": "gemm_i8_kernel (mma.sync m16n8k32 s8, TMA-fed) or gemm_mx_kernel on two "
+                    "e4m3 planes, per shape from the measured table",
+            "int8block": "gemm_i8_kernel (block promotion per K slab, mma.sync m16n8k32 s8) or "
+                         "gemm_mx_kernel on two e4m3 planes, per shape from the measured table"}[code]
     line = {
         "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -321,8 +321,10 @@ fp8bq_status fp8bq_gemm_rowwise(int64_t M, int64_t N, int64_t K, const void* a_q
  *        swap-AB or normal tiles as for e4m3.  Both operands are rewritten into
  *        the workspace first (2 bytes per code, K rounded up to 128), so this
  *        form needs a workspace even without split-K.
- * fp8bq_gemm_rowwise picks the warp-level kernel up to 64 tokens and the
- * planes above.  Other shapes: FP8BQ_ERR_UNSUPPORTED. */
+ * fp8bq_gemm_rowwise takes the kernel and shape from the measured table's
+ * "ri8" entry for the problem (nearest M) when there is one, else the
+ * warp-level kernel up to 64 tokens and the planes above.  Other shapes:
+ * FP8BQ_ERR_UNSUPPORTED. */
 fp8bq_status fp8bq_gemm_rowwise_variant(int64_t M, int64_t N, int64_t K, const void* a_q,
                                         const float* a_s, const void* w_q, const float* w_s,
                                         fp8bq_code code, fp8bq_dtype out_dtype, void* out,
@@ -366,8 +368,14 @@ fp8bq_status fp8bq_quant_weight_int8(const void* w, fp8bq_dtype w_dtype, int64_t
                                      int block_n, int block_k, void* q, float* s,
                                      cudaStream_t stream);
 /* The block INT8 GEMM; workspace rules as fp8bq_gemm (counter prefix, then
- * split parts).  The _variant form takes swap-AB shapes with block_n 8, 16,
- * 32, 64 or 128, split >= 0, mma_scale 0. */
+ * split parts, then, for the planes kernel, both operands' e4m3 planes).  The
+ * _variant form chooses the kernel by mma_scale, as fp8bq_gemm_rowwise_variant
+ * does for int8: 0 -- the warp-level int8 MMA with per-slab promotion, swap-AB
+ * tiles with block_n 8, 16, 32, 64 or 128; 1 -- two e4m3 planes on the
+ * promotion kernel, swap-AB (16..128) or normal (128, 256) tiles.  split >= 0
+ * (0 = stream-K).  fp8bq_gemm_int8_block takes the measured table's "bi8"
+ * entry when there is one, else the warp-level kernel up to 64 tokens and the
+ * planes above. */
 fp8bq_status fp8bq_gemm_int8_block(int64_t M, int64_t N, int64_t K, const void* a_q,
                                    const float* a_s, const void* w_q, const float* w_s,
                                    int group, int block_n, int block_k, fp8bq_dtype out_dtype,
