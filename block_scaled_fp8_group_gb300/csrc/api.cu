@@ -91,8 +91,8 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 // ------------------------------------------------------- variant table
 //
 // Text file, one entry per line:  N K fmt out M kind block_n split grid [mma_scale]
-// (fmt: fp32|ue8m0, out: bf16|fp16|fp32, kind: normal|swap|swap64; mma_scale 0
-// when absent).  Per
+// (fmt: fp32|ue8m0, or a table-only format below; out: bf16|fp16|fp32; kind:
+// normal|swap|swap64; mma_scale 0 when absent).  Per
 // (N, K, fmt, out) the entries form an M grid; a lookup takes the grid point
 // nearest to M, the smaller one on a tie ("vLLM 量化 Kernel 配置机制" §4.2:
 // configs[min(keys, key=|x - M|)], e.g. M=37 -> 32, M=2050 -> 2048).
@@ -128,10 +128,13 @@ std::string table_path(const std::string& device_name) {
 
 // Table-only format codes of the other GEMMs, each with its own measured
 // shapes: rowwise e4m3 (FP8_Dynamic) "rw8", rowwise INT8 "ri8", block INT8
-// "bi8" (for INT8, mma_scale 1 = the two-plane kernel).
+// "bi8" (for INT8, mma_scale 1 = the two-plane kernel), and the grouped (MoE)
+// GEMM with fp32 or UE8M0 scales, "gfp32" / "gue8m0" (M = rows per expert).
 constexpr int kTableRowwiseE4m3 = 2;
 constexpr int kTableRowwiseInt8 = 3;
 constexpr int kTableBlockInt8 = 4;
+constexpr int kTableGroupedFp32 = 5;
+constexpr int kTableGroupedUe8m0 = 6;
 
 int parse_fmt(const char* s) {
     if (!std::strcmp(s, "fp32")) return FP8BQ_SCALE_FP32;
@@ -139,6 +142,8 @@ int parse_fmt(const char* s) {
     if (!std::strcmp(s, "rw8")) return kTableRowwiseE4m3;
     if (!std::strcmp(s, "ri8")) return kTableRowwiseInt8;
     if (!std::strcmp(s, "bi8")) return kTableBlockInt8;
+    if (!std::strcmp(s, "gfp32")) return kTableGroupedFp32;
+    if (!std::strcmp(s, "gue8m0")) return kTableGroupedUe8m0;
     return -1;
 }
 int parse_out(const char* s) {
@@ -568,6 +573,23 @@ std::string host_device_name() {
     return device_info(&d) == FP8BQ_OK ? d->name : std::string();
 }
 
+// Kernel shape of a grouped problem: the table's grouped entry for (N, K,
+// out) at the nearest rows-per-expert M_max when it has one and the planner
+// (and, for the block-scaled MMA, the scale format) accepts it for these E;
+// else the default rule.  The entries are measured at one expert count.
+fp8bq_variant grouped_variant(int64_t E, int64_t M_max, int64_t N, int64_t K, int fmt, int out,
+                              const std::string& device_name, int num_sms) {
+    fp8bq_variant measured;
+    const int tfmt = fmt == FP8BQ_SCALE_UE8M0 ? kTableGroupedUe8m0 : kTableGroupedFp32;
+    if (format_table_lookup(tfmt, M_max, N, K, out, device_name, &measured)) {
+        GemmPlan probe;
+        const bool mx_ok =
+            !measured.mma_scale || (fmt == FP8BQ_SCALE_UE8M0 && K % (4 * kGroup) == 0);
+        if (mx_ok && make_gemm_plan(M_max, N, K, measured, num_sms, &probe, E)) return measured;
+    }
+    return default_grouped_variant(E, M_max, N, K, fmt, num_sms);
+}
+
 }  // namespace
 }  // namespace fp8bq
 
@@ -769,10 +791,7 @@ fp8bq_status fp8bq_select_grouped_variant(int64_t E, int64_t M_max, int64_t N, i
     if (!variant) return FP8BQ_ERR_INVALID_ARG;
     fp8bq_status st = check_grouped_args(E, M_max, N, K, fmt, out_dtype);
     if (st != FP8BQ_OK) return st;
-    DeviceInfo* d = nullptr;
-    int sms = 152;  // GB300 when no GPU is visible (host-only queries)
-    if (device_info(&d) == FP8BQ_OK) sms = d->num_sms;
-    *variant = default_grouped_variant(E, M_max, N, K, fmt, sms);
+    *variant = grouped_variant(E, M_max, N, K, fmt, out_dtype, host_device_name(), host_sms());
     return FP8BQ_OK;
 }
 
@@ -850,7 +869,7 @@ fp8bq_status fp8bq_grouped_linear(const void* x, fp8bq_dtype x_dtype, int64_t E,
     DeviceInfo* d = nullptr;
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
-    const fp8bq_variant v = default_grouped_variant(E, M_max, N, K, fmt, d->num_sms);
+    const fp8bq_variant v = grouped_variant(E, M_max, N, K, fmt, out_dtype, d->name, d->num_sms);
     GemmPlan plan;
     if (!make_gemm_plan(M_max, N, K, v, d->num_sms, &plan, E)) return FP8BQ_ERR_UNSUPPORTED;
     // workspace: [counter prefix][codes][scales][split-K partials], as fp8bq_linear

@@ -2,7 +2,7 @@
 §3: per (N, K, device, dtype) and per point of the M grid, time every candidate
 kernel configuration and keep the fastest).
 
-    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small,rowwise \
+    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small,rowwise,moe \
         [--out block_scaled_fp8_group_gb300/tables/<device>.tbl]
 
 Candidates per M: swap-AB with token tiles 16..128 (and 64 weight rows per
@@ -50,6 +50,14 @@ SETS = {
 }
 
 INT8_FMTS = ("ri8", "bi8")
+
+# grouped (MoE) GEMM, table formats "gue8m0" / "gfp32" keyed by the rows per
+# expert M_max: (N, K, scale fmt, out dtype, token counts routed over E local
+# experts as the MoE workload routes them)
+GROUPED_SETS = {
+    "moe": [(n, k, "ue8m0", "bf16", (32, 128, 512, 1024, 2048, 4096, 8192))
+            for n, k in synth.MOE_NK],
+}
 
 
 def device_table_path() -> str:
@@ -200,6 +208,78 @@ def tune_shape(N, K, fmt, out_name, Ms, log):
     return rows
 
 
+def tune_grouped(N, K, fmt, out_name, token_counts, log):
+    """Grouped entries: E = the MoE workload's local experts, counts from its
+    routing; weights and activations random on the device (timing only).  One
+    weight copy: every launch reads the occupied experts' weights, far more
+    than the L2 holds."""
+    dev = torch.device("cuda")
+    E = synth.MOE_E_LOCAL
+    out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.SEED_WEIGHT)
+    w = torch.randn((E * N, K), device=dev, generator=g, dtype=torch.bfloat16) * 0.02
+    wq, ws = fp8bq.fp8bq_quant_weight(w, fmt)
+    del w
+    copies = [wq, wq]
+    rows, seen = [], set()
+    for T in token_counts:
+        counts = synth.moe_counts(E, T)
+        M_max = int((counts.max() + 3) // 4 * 4)
+        if M_max in seen:
+            continue
+        seen.add(M_max)
+        cnt = torch.from_numpy(counts).to(dev)
+        x = torch.randn((E * M_max, K), device=dev, generator=g, dtype=torch.bfloat16)
+        aq, as_ = fp8bq.fp8bq_quant_act(x, fmt)
+        del x
+        out = torch.empty((E * M_max, N), dtype=out_dt, device=dev)
+        results = []
+        for kind, bn, split, mx in candidates(M_max, N, K, fmt):
+            v = fp8bq.make_variant(kind, bn, split, 0, mx)
+            need = fp8bq.fp8bq_grouped_variant_workspace_bytes(E, M_max, N, K, v)
+            ws_buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
+
+            def run(c, v=v, ws_buf=ws_buf):
+                fp8bq.fp8bq_grouped_gemm(aq, as_, c, ws, cnt, fmt=fmt, out_dtype=out_dt, out=out,
+                                         workspace=ws_buf, variant=v)
+            try:
+                run(wq)  # the planner rejects shapes the kernels lack, on the host
+            except fp8bq.Fp8bqError:
+                continue
+            results.append((time_calls(run, copies), kind, bn, split, mx))
+        results.sort()
+        t, kind, bn, split, mx = results[0]
+        rows.append(f"{N} {K} g{fmt} {out_name} {M_max} {kind} {bn} {split} 0 {mx}")
+        dflt = fp8bq.fp8bq_select_grouped_variant(E, M_max, N, K, fmt, out_dt)
+        log(f"  N={N} K={K} g{fmt}/{out_name} T={T} M_max={M_max}: best "
+            f"{kind}/{bn}/s{split}{'/mx' if mx else ''} {t:.2f} us; "
+            f"{len(results)} candidates; default {dflt['kind']}/{dflt['block_n']}/"
+            f"s{dflt['split']}{'/mx' if dflt['mma_scale'] else ''}")
+    del copies, wq
+    torch.cuda.empty_cache()
+    return rows
+
+
+def time_calls(run, copies, batch=24, reps=3):
+    for c in copies[:2]:
+        run(c)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(1_000_000)
+        a.record()
+        for i in range(batch):
+            run(copies[i % len(copies)])
+        b.record()
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e3 / batch
+        best = t if best is None else min(best, t)
+    return best
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--sets", default="small,decode,prefill,full")
@@ -218,6 +298,13 @@ def main():
     t0 = time.time()
     done = set()
     for name in args.sets.split(","):
+        if name in GROUPED_SETS:
+            for (N, K, fmt, out_name, toks) in GROUPED_SETS[name]:
+                print(f"tuning grouped N={N} K={K} {fmt}/{out_name} over tokens={list(toks)}",
+                      flush=True)
+                for row in tune_grouped(N, K, fmt, out_name, toks, lambda s: print(s, flush=True)):
+                    keep[tuple(row.split()[:5])] = row
+            continue
         for (N, K, fmt, out_name, Ms) in SETS[name]:
             key = (N, K, fmt, out_name)
             Ms = tuple(m for m in Ms if (key, m) not in done)

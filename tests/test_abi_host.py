@@ -422,3 +422,37 @@ def test_int8_table_entries(tmp_path, monkeypatch):
     finally:
         monkeypatch.delenv("FP8BQ_TABLE")
         fp8bq.fp8bq_reload_table()
+
+
+def test_grouped_table_entries(tmp_path, monkeypatch):
+    """gue8m0 / gfp32 lines give the grouped (MoE) GEMM measured shapes at the
+    nearest rows per expert; the block-scaled MMA is never taken for fp32
+    scales, and the plain GEMM ignores grouped lines."""
+    t = tmp_path / "g.tbl"
+    t.write_text("4096 7168 gue8m0 bf16 16 swap 16 3 0 1\n"
+                 "4096 7168 gue8m0 bf16 788 normal 128 1 0 0\n"
+                 # stream-K over 32 experts' tiles: more tiles than ticket
+                 # counters, so the planner rejects it
+                 "4096 7168 gue8m0 bf16 4096 normal 128 0 0 0\n"
+                 "4096 7168 gfp32 bf16 16 swap 16 2 0 1\n")
+    monkeypatch.setenv("FP8BQ_TABLE", str(t))
+    fp8bq.fp8bq_reload_table()
+    try:
+        v = fp8bq.fp8bq_select_grouped_variant(32, 20, 4096, 7168, "ue8m0", "bf16")
+        assert (v["kind"], v["block_n"], v["split"], v["mma_scale"], v["from_table"]) == \
+            ("swap", 16, 3, 1, True)
+        # the workspace query follows the entry: split parts of 32 experts
+        assert fp8bq.fp8bq_grouped_gemm_workspace_bytes(32, 20, 4096, 7168, "ue8m0",
+                                                        "bf16") >= 3 * 32 * 20 * 4096 * 4
+        v = fp8bq.fp8bq_select_grouped_variant(32, 700, 4096, 7168, "ue8m0", "bf16")
+        assert (v["kind"], v["block_n"], v["split"], v["mma_scale"]) == ("normal", 128, 1, 0)
+        v = fp8bq.fp8bq_select_grouped_variant(32, 4000, 4096, 7168, "ue8m0", "bf16")
+        assert v["from_table"] is False
+        # fp32 scales cannot take the block-scaled MMA: the entry falls through
+        v = fp8bq.fp8bq_select_grouped_variant(32, 20, 4096, 7168, "fp32", "bf16")
+        assert v["from_table"] is False and v["mma_scale"] == 0
+        # the plain (non-grouped) GEMM has no entry for this shape
+        assert fp8bq.fp8bq_select_variant(16, 4096, 7168, "ue8m0", "bf16")["from_table"] is False
+    finally:
+        monkeypatch.delenv("FP8BQ_TABLE")
+        fp8bq.fp8bq_reload_table()
