@@ -147,3 +147,51 @@ def test_bounded_wait_times_out_and_reports(fp8bq):
     x = to_dev_bits(synth.act_small(4, 256))
     fp8bq.fp8bq_quant_act(x, "fp32")
     torch.cuda.synchronize()
+
+
+def test_fp32_converter_every_pattern(fp8bq):
+    """Every fp32 bit pattern in [-448, 448] (both signs, zeros and
+    subnormals included) through the GPU's e4m3 conversion.  In fp32 weight
+    blocks whose first element is 448 the scale is 448/448 = 1 exactly, so
+    each of the other 16383 elements reaches the conversion unchanged; its
+    code must be the oracle's encoding of the same value."""
+    per = 128 * 128 - 1
+    top = 0x43E00000  # 448.0
+    n_pos = top + 1   # patterns 0 .. 448.0 of one sign
+    blocks = 2048
+    chunk = blocks * per
+    dev_w = torch.empty((blocks * 128, 128), dtype=torch.float32, device="cuda")
+    dev_q = torch.empty((blocks * 128, 128), dtype=torch.uint8, device="cuda")
+    dev_s = torch.empty((blocks, 1), dtype=torch.float32, device="cuda")
+    host = np.empty((blocks, 128 * 128), dtype=np.uint32)
+    host[:, 0] = top
+    checked = 0
+
+    def oracle_codes(w, nb):
+        bounds = np.linspace(0, nb, 17).astype(int) * 128
+        with ThreadPoolExecutor(max_workers=16) as ex:
+            parts = list(ex.map(lambda r: oracle.quant_weight(w[r[0]:r[1]], oracle.FP32)[0],
+                                [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]))
+        return np.concatenate(parts, axis=0)
+
+    for sign in (0, 0x80000000):
+        for start in range(0, n_pos, chunk):
+            cnt = min(chunk, n_pos - start)
+            nb = (cnt + per - 1) // per
+            body = np.full(nb * per, top, dtype=np.uint32)  # padding repeats 448
+            body[:cnt] = np.arange(start, start + cnt, dtype=np.uint32) | np.uint32(sign)
+            host[:nb, 1:] = body.reshape(nb, per)
+            w = host[:nb].view(np.float32).reshape(nb * 128, 128)
+            dev_w[:nb * 128].copy_(torch.from_numpy(w))
+            fp8bq.fp8bq_quant_weight(dev_w[:nb * 128], "fp32", q=dev_q[:nb * 128], s=dev_s[:nb])
+            q = dev_q[:nb * 128].cpu().numpy()
+            s = dev_s[:nb].cpu().numpy()
+            assert np.all(s == 1.0)
+            rq = oracle_codes(w, nb)
+            if not np.array_equal(q, rq):
+                bad = np.flatnonzero(q.reshape(-1) != rq.reshape(-1))[:5]
+                vals = w.reshape(-1)[bad]
+                raise AssertionError(f"codes differ at {vals!r}: gpu {q.reshape(-1)[bad]}, "
+                                     f"oracle {rq.reshape(-1)[bad]}")
+            checked += cnt
+    assert checked == 2 * n_pos
