@@ -2,7 +2,8 @@
 §3: per (N, K, device, dtype) and per point of the M grid, time every candidate
 kernel configuration and keep the fastest).
 
-    python -m block_scaled_fp8_group_gb300.tune --sets decode,prefill,full,small,rowwise,moe \
+    python -m block_scaled_fp8_group_gb300.tune \
+        --sets small,decode,prefill,full,rowwise,rowwise_int8,block_int8,moe \
         [--out block_scaled_fp8_group_gb300/tables/<device>.tbl]
 
 Candidates per M: swap-AB with token tiles 16..128 (and 64 weight rows per
@@ -10,7 +11,11 @@ tile for token tiles up to 32) and the normal
 orientation with 128/256-wide weight tiles, each with stream-K (split 0),
 no split, and a few fixed K splits; with UE8M0 scales and K % 512 == 0 every
 candidate with 128-row tiles also runs with the scales applied by the
-block-scaled MMA (mma_scale 1).  Each candidate is timed on cold weights
+block-scaled MMA (mma_scale 1).  The INT8 sets ("ri8", "bi8") time both
+INT8 kernels: the warp-level int8 MMA (mma_scale 0, token tiles from 8) and
+the two e4m3 planes on the FP8 MMA (mma_scale 1).  The grouped set ("moe")
+times the grouped GEMM over the MoE workload's 32 local experts and keys its
+entries ("gue8m0") by the rows per expert.  Each candidate is timed on cold weights
 (a rotation of weight copies larger than L2) as the mean of a batch of
 back-to-back launches queued behind a GPU sleep, so launch gaps do not count
 host time.  Lines of the table file: N K fmt out M kind block_n split grid
