@@ -95,7 +95,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 // normal|swap|swap64; mma_scale 0 when absent).  Per
 // (N, K, fmt, out) the entries form an M grid; a lookup takes the grid point
 // nearest to M, the smaller one on a tie ("vLLM 量化 Kernel 配置机制" §4.2:
-// configs[min(keys, key=|x - M|)], e.g. M=37 -> 32, M=2050 -> 2048).
+// the key with the least |key - M|, e.g. M=37 -> 32, M=2050 -> 2048).
 
 using TableKey = std::tuple<int64_t, int64_t, int, int>;  // N, K, fmt, out
 
