@@ -85,6 +85,12 @@ def step_bytes(M, N, K):
     return 2 * M * K + N * K + 4 * ((N + 127) // 128) * G + 2 * M * N
 
 
+def gemm_flops(M, N, K):
+    """The pages' TFLOPS numerator: 2*m*n*k ("vLLM DeepGEMM FP8 Block GEMM 基准测试"
+    §4.3)."""
+    return 2.0 * M * N * K
+
+
 def pages_gbs_bytes(M, N, K):
     """The pages' GB/s numerator: m*k + k*n + 2*m*n ("vLLM DeepGEMM FP8 Block GEMM
     基准测试" §4.3)."""
@@ -742,7 +748,7 @@ def run_gpu_rowwise(args, rank, world):
                 evs[i][1].record()
             torch.cuda.synchronize()
             us = float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
-            fl = 2.0 * M * N * K
+            fl = gemm_flops(M, N, K)
             entry = {"m": M, "n": N, "k": K, "us": round(us, 2),
                      "tflops": round(fl / us / 1e6, 1),
                      "variant": variant_name(fc.select(M, N, K))}
@@ -757,7 +763,7 @@ def run_gpu_rowwise(args, rank, world):
         t = gemm_us[i] * 1e-6
         b = fc.gemm_bytes(M, N, K)
         per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
-                    "tflops": round(2.0 * M * N * K / t / 1e12, 2),
+                    "tflops": round(gemm_flops(M, N, K) / t / 1e12, 2),
                     "gbs_alg": round(b / t / 1e9, 1),
                     "roofline_frac": round(b / (peaks["hbm_gbs"] * 1e9) / t, 3),
                     "variant": variant_name(variants[(M, N, K)])})
@@ -1071,7 +1077,7 @@ def run_gpu(args, rank, world):
     for i, (M, N, K) in enumerate(probs):
         t = gemm_us[i] * 1e-6
         b = gemm_bytes(M, N, K)
-        fl = 2.0 * M * N * K
+        fl = gemm_flops(M, N, K)
         t_roof = max(b / (peaks["hbm_gbs"] * 1e9), fl / (fp8_peak * 1e12))
         per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
                     "tflops": round(fl / t / 1e12, 2),
