@@ -40,6 +40,9 @@ def main():
     ap.add_argument("--variant", default=None,
                     help="kind/block_n/split[/grid[/mma_scale]] (default: the table's)")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--time", action="store_true",
+                    help="--op quant: also print the mean time of 50 back-to-back launches "
+                         "over input copies larger than the L2 (CUDA events)")
     args = ap.parse_args()
     dev = torch.device("cuda")
     out_dt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[args.out]
@@ -49,6 +52,8 @@ def main():
         for _ in range(args.iters):
             fp8bq.fp8bq_quant_act(x, args.fmt)
         torch.cuda.synchronize()
+        if args.time:
+            time_quant(x, args.fmt)
         return
     if args.op == "grouped":
         # the MoE workload's grouped GEMM: E experts, counts from seeded routing
@@ -112,6 +117,44 @@ def main():
     torch.cuda.synchronize()
     if fp8bq.fp8bq_device_status() != 0:
         raise SystemExit("device wait timed out")
+
+
+def time_quant(x, fmt, launches=50):
+    """Mean device time of the activation quant: `launches` back-to-back
+    launches captured in a CUDA graph (no host time between them) over
+    rotated input copies that together exceed the 129 MB L2 (inputs smaller
+    than 2 MB rotate through 64 copies and stay in L2: launch-bound sizes).
+    Algorithmic bandwidth: 2 B in + 1 B out per element, plus the scales."""
+    M, K = x.shape
+    n = min(64, max(2, 1 + -(-(256 << 20) // (2 * M * K))))
+    copies = [x] + [x.clone() for _ in range(n - 1)]
+    qs = [fp8bq.fp8bq_quant_act(c, fmt) for c in copies]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(launches):
+                j = i % len(copies)
+                fp8bq.fp8bq_quant_act(copies[j], fmt, q=qs[j][0], s=qs[j][1])
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    best = None
+    for _ in range(3):
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / launches
+        best = us if best is None else min(best, us)
+    scale_bytes = qs[0][1].numel() * qs[0][1].element_size()
+    byt = 3 * M * K + scale_bytes
+    print(f"quant {fmt} M={M} K={K}: {best:.2f} us, {byt / best / 1e3:.1f} GB/s algorithmic "
+          f"({len(copies)} input copies, {launches} launches in a graph, best of 3)")
 
 
 if __name__ == "__main__":
