@@ -133,22 +133,8 @@ def run_variant(aq, as_, wq, ws, v, fmt, out_dt, out, ws_buf):
 
 
 def time_variant(aq, as_, copies, ws, v, fmt, out_dt, out, ws_buf, batch=24, reps=3):
-    for c in copies[:2]:
-        run_variant(aq, as_, c, ws, v, fmt, out_dt, out, ws_buf)
-    torch.cuda.synchronize()
-    best = None
-    for _ in range(reps):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(1_000_000)
-        a.record()
-        for i in range(batch):
-            run_variant(aq, as_, copies[i % len(copies)], ws, v, fmt, out_dt, out, ws_buf)
-        b.record()
-        b.synchronize()
-        t = a.elapsed_time(b) * 1e3 / batch
-        best = t if best is None else min(best, t)
-    return best
+    return time_calls(lambda c: run_variant(aq, as_, c, ws, v, fmt, out_dt, out, ws_buf),
+                      copies, batch, reps)
 
 
 def tune_shape(N, K, fmt, out_name, Ms, log):
@@ -267,6 +253,8 @@ def tune_grouped(N, K, fmt, out_name, token_counts, log):
 
 
 def time_calls(run, copies, batch=24, reps=3):
+    """Best of `reps` mean launch times (us) of `batch` calls of run(copy),
+    copies rotated, queued behind a GPU sleep so host time does not count."""
     for c in copies[:2]:
         run(c)
     torch.cuda.synchronize()
