@@ -637,6 +637,18 @@ size_t fp8bq_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, const fp8b
     return plan.ws_bytes;
 }
 
+fp8bq_status fp8bq_variant_supported(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                     const fp8bq_variant* v) {
+    if (!v) return FP8BQ_ERR_INVALID_ARG;
+    fp8bq_status st = check_gemm_args(M, N, K, fmt, FP8BQ_BF16);
+    if (st != FP8BQ_OK) return st;
+    if (v->mma_scale && (fmt != FP8BQ_SCALE_UE8M0 || K % (4 * kGroup) != 0))
+        return FP8BQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP8BQ_OK;
+    GemmPlan plan;
+    return make_gemm_plan(M, N, K, *v, host_sms(), &plan) ? FP8BQ_OK : FP8BQ_ERR_UNSUPPORTED;
+}
+
 fp8bq_status fp8bq_select_variant(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
                                   fp8bq_dtype out_dtype, fp8bq_variant* variant) {
     if (!variant) return FP8BQ_ERR_INVALID_ARG;

@@ -45,7 +45,7 @@ EXPORTS = (
     "fp8bq_quant_weight_int8", "fp8bq_gemm_int8_block", "fp8bq_gemm_int8_block_variant",
     "fp8bq_select_int8_block_variant", "fp8bq_int8_block_workspace_bytes",
     "fp8bq_int8_block_variant_workspace_bytes", "fp8bq_linear_int8_block",
-    "fp8bq_linear_int8_block_workspace_bytes",
+    "fp8bq_linear_int8_block_workspace_bytes", "fp8bq_variant_supported",
 )
 
 
@@ -79,6 +79,7 @@ def _load():
         "fp8bq_weight_scale_bytes": (sz, [i64, i64, i32, i32]),
         "fp8bq_gemm_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "fp8bq_variant_workspace_bytes": (sz, [i64, i64, i64, ctypes.POINTER(Variant)]),
+        "fp8bq_variant_supported": (i32, [i64, i64, i64, i32, ctypes.POINTER(Variant)]),
         "fp8bq_linear_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "fp8bq_quant_act": (i32, [vp, i32, i64, i64, i32, i32, vp, vp, vp]),
         "fp8bq_quant_weight": (i32, [vp, i32, i64, i64, i32, i32, i32, vp, vp, vp]),
@@ -271,6 +272,12 @@ def make_variant(kind, block_n: int, split: int = 1, grid: int = 0,
 
 def fp8bq_gemm_workspace_bytes(M, N, K, fmt="fp32", out_dtype=torch.bfloat16) -> int:
     return _lib.fp8bq_gemm_workspace_bytes(M, N, K, _fmt(fmt), _dtype_code(out_dtype))
+
+
+def fp8bq_variant_supported(M, N, K, fmt, variant: Variant) -> bool:
+    """Whether the kernels have this explicit shape for (M, N, K) and the scale
+    format (host-only; launches nothing)."""
+    return _lib.fp8bq_variant_supported(M, N, K, _fmt(fmt), ctypes.byref(variant)) == FP8BQ_OK
 
 
 def fp8bq_variant_workspace_bytes(M, N, K, variant: Variant) -> int:

@@ -175,6 +175,13 @@ fp8bq_status fp8bq_gemm_variant(int64_t M, int64_t N, int64_t K, const void* a_q
                                 fp8bq_scale_fmt fmt, fp8bq_dtype out_dtype, void* out,
                                 const fp8bq_variant* variant, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
+/* Host-only check of an explicit kernel shape before fp8bq_gemm_variant:
+ * FP8BQ_OK when the kernels have this tile/split/schedule for (M, N, K) and
+ * the scale format (the block-scaled MMA, mma_scale 1, needs UE8M0 scales and
+ * K % 512 == 0) on this GPU (152 SMs when none is visible); the argument
+ * errors of fp8bq_gemm, or FP8BQ_ERR_UNSUPPORTED.  Launches nothing. */
+fp8bq_status fp8bq_variant_supported(int64_t M, int64_t N, int64_t K, fp8bq_scale_fmt fmt,
+                                     const fp8bq_variant* variant);
 
 /* ---------------------------------------------------------- grouped GEMM */
 
