@@ -365,11 +365,12 @@ fp8bq_status check_rowwise_ptrs(const void* a_q, const float* a_s, const void* w
     return FP8BQ_OK;
 }
 
-// INT8 problems with at least this many tokens run as two e4m3 planes on the
-// tcgen05 FP8 MMA (four cross products per K step); smaller ones on the
-// warp-level int8 MMA, which streams the int8 weights once.  On GB300 the
-// warp-level kernel is faster up to 64 tokens (one 64-token tile) and the
-// planes from 96 on (7168 x 18432: 129 vs 157 us at 64, 245 vs 174 us at 96).
+// INT8 shapes without a measured table entry: at least this many tokens run
+// as two e4m3 planes on the tcgen05 FP8 MMA (four cross products per K step),
+// fewer on the warp-level int8 MMA, which streams the int8 weights once.  The
+// warp-level kernel wins while one token tile covers M and the int8 MMA rate
+// is not yet the bound; where the two are close (48-64 tokens on GB300) the
+// table's measured entries decide.
 constexpr int64_t kInt8PlanesMinM = 65;
 
 // Kernel shape of a rowwise problem.  e4m3: the tile and split the block path
@@ -1317,7 +1318,7 @@ fp8bq_status fp8bq_linear_int8_block(const void* x, fp8bq_dtype x_dtype, int64_t
     st = device_info(&d);
     if (st != FP8BQ_OK) return st;
     const fp8bq_variant v = int8_block_variant(M, N, K, out_dtype, d->num_sms, d->name);
-    // workspace: [counter prefix][codes][scales][split parts][planes (above 64 tokens)]
+    // workspace: [counter prefix][codes][scales][split parts][planes (two-plane kernel)]
     const size_t q_bytes = align256(static_cast<size_t>(M * K));
     const size_t s_bytes = align256(fp8bq_act_scale_bytes(M, K, kGroup, FP8BQ_SCALE_FP32));
     const size_t need = fp8bq_linear_int8_block_workspace_bytes(M, N, K, out_dtype);
