@@ -195,3 +195,33 @@ def test_fp32_converter_every_pattern(fp8bq):
                                      f"oracle {rq.reshape(-1)[bad]}")
             checked += cnt
     assert checked == 2 * n_pos
+
+
+@pytest.mark.parametrize("ue", [False, True])
+@pytest.mark.parametrize("amax", [1.0, 3.0, 0.3, 1000.0, 7.0e-3, 250.0, 1.0e-6])
+def test_act_quant_every_bf16_value_per_scale(fp8bq, amax, ue):
+    """Groups whose first element is A (a bf16 value) have s = fp32(A/448)
+    (UE8M0: the next power of two), which is not a power of two in fp32 mode,
+    so each of the other 127 elements goes through the IEEE division x/s and
+    the e4m3 conversion: every finite bf16 value with |x| <= A is checked
+    against the oracle for each A."""
+    a_bits = synth.f32_to_bf16_bits(np.array([amax], dtype=np.float32))[0]
+    a_val = synth.bf16_bits_to_f32(np.array([a_bits], dtype=np.uint16))[0]
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = synth.bf16_bits_to_f32(bits)
+    keep = bits[np.isfinite(vals) & (np.abs(vals) <= a_val)]
+    per = 127
+    G = (keep.size + per - 1) // per
+    groups = np.zeros((G, 128), dtype=np.uint16)
+    flat = np.concatenate([keep, np.zeros(G * per - keep.size, dtype=np.uint16)])
+    groups[:, 1:] = flat.reshape(G, per)
+    groups[:, 0] = a_bits
+    rows = (G + 7) // 8
+    xb = np.zeros((rows * 8, 128), dtype=np.uint16)
+    xb[:G] = groups
+    xb[G:, 0] = a_bits
+    xb = xb.reshape(rows, 1024)
+    q, s = run_act(fp8bq, xb, False, ue)
+    rq, rs = oracle.quant_act(xb, oracle.BF16, 128, ue)
+    np.testing.assert_array_equal(q, rq)
+    np.testing.assert_array_equal(s, rs.view(np.uint32))
