@@ -1,42 +1,54 @@
 """Benchmark of the W8A8 block-FP8 linear hot path on GB300.
 
-Workload (one "step"): the decode sweep -- (N, K) in {(7168, 18432),
-(18432, 7168), (4096, 7168)} x M in {1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128},
-33 problems; per problem the activation quant (bf16 -> e4m3 + packed UE8M0
-scales) and the block-scaled GEMM (UE8M0, bf16 out) in the variant the
-per-shape table selects.  Activations: bf16 N(0,1) with 1% of the K channels
-x30; weights bf16 N(0,0.02) quantised 128x128 (UE8M0) once, outside the timed
-region (as the pages' benchmark does).  Every GEMM of a step reads its own
-copy of the weights (3.2 GB per step), so no GEMM finds its operands in L2.
+Workloads (`--workload`; the default is the largest configuration, `grid`):
 
-Reported: value = algorithmic bytes of the whole step / step time (GB/s),
-per-problem GEMM us / TFLOPS / GB/s / roofline fraction, the roofline of the
-dominant kernel (the GEMM) against the measured HBM copy bandwidth, an
-end-to-end number through fp8bq_linear with pinned host buffers, and the CPU
-oracle timed on a bounded sample.  `--impl reference` times the oracle alone.
+  grid     the full grid: M in {1,2,4,8,16,24,32,48,64,96,128,256,512,1024,
+           1536,2048,3072,4096} x (N,K) in {(1536,7168),(7168,1536),
+           (4096,7168),(7168,18432),(18432,7168),(24576,7168)}, fp16 and
+           bf16 out: 216 fp8bq_linear calls (activation quant + block-scaled
+           GEMM, UE8M0) per pass.  Activations bf16 N(0,1) with 0.5% of the K
+           channels x50, weights bf16 N(0,0.02) quantised 128x128 once,
+           outside the timed region.
+  decode   the decode sweep: (N,K) in {(7168,18432),(18432,7168),(4096,7168)}
+           x M in {1..128} (11 points), UE8M0, bf16 out, act 1% channels x30.
+  prefill  the prefill sweep: (N,K) in {(24576,7168),(4096,7168),(7168,18432)}
+           x M in {256..4096} (7 points), fp32 scales, bf16 and fp32 out,
+           act Student-t(3) scaled to unit RMS.
+  small    M=16, N=K=1536, fp32 scales, bf16 out, fp32 N(0,0.02) weights: 100
+           back-to-back calls per pass, each on its own weight copy (cold),
+           and the same 100 calls on one copy (hot L2).
+  quant    the standalone per-token-group quant: M in {1,64,1024,4096,16384}
+           x K in {1536,7168,18432}, fp32 and UE8M0 scales; every 8th row
+           holds one +-1000 spike per group.
+  moe      the grouped (mixture-of-experts) linear layer (32 local experts).
+  rowwise  the per-token x per-channel formats (`--code e4m3|int8|int8block`).
 
-`--workload moe` times the grouped (mixture-of-experts) path instead: 32 local
-experts of DeepSeek-V3's routed-expert projections (gate+up N=4096 K=7168,
-down N=7168 K=2048), tokens routed top-8 of 256 experts with a seeded skewed
-popularity, a decode batch (128 tokens) and a prefill chunk (4096 tokens);
-per problem one fp8bq_grouped_linear call (quant of the occupied rows +
-grouped GEMM).
+A step is `passes` passes over the workload's problems, replayed from one
+CUDA graph; `passes` is the smallest count for which the K timed steps last
+at least `--min-timed-s` seconds, so the clock samples cover a loaded GPU
+whatever K is.  Every problem reads its own weight copy (and activation
+copy), so the inputs of a pass are far larger than L2.
 
-`--workload rowwise --code e4m3|int8` times the per-token x per-channel
-formats (FP8_Dynamic, W8A8_INT8) on the decode sweep's problems, one
-fp8bq_linear_rowwise per problem, and the rowwise GEMM alone at M = 2048 and
-4096 on the same (N,K).
+Reported beside `value`: per (M,N,K) the GEMM's time (isolated, cold; and
+hot, directly after the same GEMM), TFLOPS, the pages' GB/s and the
+algorithmic GB/s and the fraction of the roofline min(FP8 peak, HBM); the
+two target regimes (M <= 64 against HBM, M >= 2048 against the FP8 peak);
+the roofline of the dominant kernel; an end-to-end number through the same
+public call with pinned host buffers; and the CPU oracle timed on a bounded
+sample.  `--impl reference` times the oracle alone on the same workload.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import numpy as np
@@ -47,43 +59,21 @@ sys.path.insert(0, ROOT)
 from block_scaled_fp8_group_gb300 import synth  # noqa: E402
 
 METRIC = "block-FP8 GEMM µs, TFLOPS and GB/s per (M,N,K) on 1 GB300; % of roofline"
-WORKLOAD = ("decode sweep: (N,K) in {(7168,18432),(18432,7168),(4096,7168)} x "
-            "M in {1,2,4,8,16,24,32,48,64,96,128}; act bf16 N(0,1), 1% channels x30 -> "
-            "per-token-group quant (UE8M0 packed); weights bf16 N(0,0.02) 128x128 UE8M0; "
-            "bf16 out")
-# The pages' DeepGEMM numbers on H100 80GB HBM3 for shapes of this sweep
-# ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §3.2, DeepGEMM table) -- context only.
-H100_DEEPGEMM_US = {(8, 7168, 18432): 70.8, (8, 18432, 7168): 69.3, (8, 4096, 7168): 102.9,
-                    (64, 7168, 18432): 69.4, (64, 18432, 7168): 70.4, (64, 4096, 7168): 69.1,
-                    (128, 7168, 18432): 71.9, (128, 18432, 7168): 69.3,
-                    (128, 4096, 7168): 141.1}
 FP8_TO_BF16_NOMINAL = 2.0  # 4.5 / 2.25 PFLOP/s dense, nominal ratio
+# The pages' DeepGEMM numbers on H100 80GB HBM3 ("vLLM DeepGEMM FP8 Block GEMM
+# 基准测试" §3.2, DeepGEMM table), µs per (m, n, k) -- context only.
+H100_DEEPGEMM_US = {
+    (8, 4096, 7168): 102.9, (8, 7168, 18432): 70.8, (8, 18432, 7168): 69.3,
+    (64, 4096, 7168): 69.1, (64, 7168, 18432): 69.4, (64, 18432, 7168): 70.4,
+    (64, 24576, 1536): 70.1, (64, 32768, 512): 68.4, (64, 7168, 16384): 69.5,
+    (128, 4096, 7168): 141.1, (128, 7168, 18432): 71.9, (128, 18432, 7168): 69.3,
+    (1024, 4096, 7168): 89.7, (1024, 18432, 7168): 279.0, (2048, 4096, 7168): 175.1,
+    (4096, 4096, 7168): 335.4}
+
+OUT_SIZE = {"bf16": 2, "fp16": 2, "fp32": 4}
 
 
-def problems():
-    return [(M, N, K) for M in synth.DECODE_M for (N, K) in synth.DECODE_NK]
-
-
-def gemm_bytes(M, N, K):
-    """Algorithmic bytes of one GEMM launch: e4m3 A and W, packed UE8M0 act
-    scales, fp32 weight scales, bf16 output."""
-    G = K // 128
-    Mp = (M + 3) // 4 * 4
-    return M * K + N * K + 4 * Mp * ((G + 3) // 4) + 4 * ((N + 127) // 128) * G + 2 * M * N
-
-
-def quant_bytes(M, K):
-    G = K // 128
-    Mp = (M + 3) // 4 * 4
-    return 2 * M * K + M * K + 4 * Mp * ((G + 3) // 4)
-
-
-def step_bytes(M, N, K):
-    """Algorithmic bytes of one problem of the step (linear layer): bf16 A in,
-    W, weight scales, bf16 out (the intermediate codes are not counted)."""
-    G = K // 128
-    return 2 * M * K + N * K + 4 * ((N + 127) // 128) * G + 2 * M * N
-
+# ------------------------------------------------------------- formulas
 
 def gemm_flops(M, N, K):
     """The pages' TFLOPS numerator: 2*m*n*k ("vLLM DeepGEMM FP8 Block GEMM 基准测试"
@@ -97,13 +87,51 @@ def pages_gbs_bytes(M, N, K):
     return M * K + K * N + 2 * M * N
 
 
+def act_scale_bytes(M, K, fmt):
+    """Activation scale buffer: [G][Mp] fp32, or [ceil(G/4)][Mp] packed UE8M0."""
+    G, Mp = K // 128, (M + 3) // 4 * 4
+    return 4 * Mp * ((G + 3) // 4 if fmt == "ue8m0" else G)
+
+
+def weight_scale_bytes(N, K):
+    return 4 * ((N + 127) // 128) * (K // 128)
+
+
+def gemm_bytes(M, N, K, fmt="ue8m0", odt="bf16"):
+    """Algorithmic bytes of one GEMM launch: e4m3 A and W, activation and
+    weight scales, the output."""
+    return M * K + N * K + act_scale_bytes(M, K, fmt) + weight_scale_bytes(N, K) + \
+        OUT_SIZE[odt] * M * N
+
+
+def linear_bytes(M, N, K, odt="bf16"):
+    """Algorithmic bytes of one linear layer (quant + GEMM): bf16 A in, W,
+    weight scales, the output (the intermediate codes are not counted)."""
+    return 2 * M * K + N * K + weight_scale_bytes(N, K) + OUT_SIZE[odt] * M * N
+
+
+def quant_bytes(M, K, fmt):
+    """Activation quant: bf16 in, e4m3 codes and the scales out."""
+    return 2 * M * K + M * K + act_scale_bytes(M, K, fmt)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+        burst = float(d["bf16_tflops"])
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": burst,
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", burst)),
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def roof_time(byt, flops, peaks):
+    """The roofline time max(bytes / HBM, flops / FP8 peak) and its bound."""
+    fp8 = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
+    th, tt = byt / (peaks["hbm_gbs"] * 1e9), flops / (fp8 * 1e12)
+    return (th, "hbm") if th >= tt else (tt, "tensor")
 
 
 def variant_name(v: dict) -> str:
@@ -111,23 +139,32 @@ def variant_name(v: dict) -> str:
     return "{kind}/{block_n}/s{split}".format(**v) + ("/mx" if v.get("mma_scale") else "")
 
 
-def gemm_source_hash():
+def source_hash(files):
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "internal.h"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "block_scaled_fp8_group_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profile_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "gemm_decode_sweep_traffic.txt")
+def gemm_source_hash():
+    return source_hash(("gemm_impl.cuh", "gemm.cu", "ptx.cuh", "internal.h"))
+
+
+def quant_source_hash():
+    return source_hash(("quant.cu", "quant_math.cuh", "internal.h"))
+
+
+def profile_traffic(name, src_hash):
+    """DRAM traffic per algorithmic byte of the dominant kernel, from a
+    committed ncu summary `profiles/<name>` taken on the current kernel
+    source (sha256 prefix); None otherwise."""
+    p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
-    t = re.search(r"traffic_bytes_per_launch_avg:\s*([0-9.eE+]+)", txt)
-    if not m or not t or m.group(1) != gemm_source_hash():
+    t = re.search(r"traffic_per_algorithmic_byte:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != src_hash:
         return None
     return float(t.group(1))
 
@@ -135,6 +172,8 @@ def profile_traffic():
 # ------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi samples (100 ms) from start() to stop(); start it before
+    the warm-up so the samples that count are taken under load."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -154,12 +193,10 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -171,85 +208,25 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm_max = max(r[1] for r in rows)
-        loaded = [r for r in rows if r[0] > 0.5 * sm_max] or rows
+        p_max = max(r[2] for r in rows)
+        # under load: drawing well above idle power (the SM clock stays at its
+        # maximum at idle on these parts, so it cannot tell load apart)
+        loaded = [r for r in rows if r[2] > 0.4 * p_max] or rows
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({n for r in rows for n, v in zip(names, r[2]) if v.lower() == "active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([r[0] for r in loaded])), "sm_max_mhz": sm_max,
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": p_max}
 
 
-# ------------------------------------------------------------- oracle legs
-
-_ORACLE_W = {}
-
-
-def oracle_time_sample(rows_per_shape=1, reps=1):
-    """Times the CPU oracle (quant of the sampled rows + their GEMM rows) on
-    one thread; returns (extrapolated whole-step seconds, sample seconds,
-    description).  Weights are quantised by the oracle outside the timing."""
-    import oracle
-    total_rows = sum(synth.DECODE_M)
-    est = 0.0
-    sample_s = 0.0
-    for (N, K) in synth.DECODE_NK:
-        if (N, K) not in _ORACLE_W:
-            _ORACLE_W[(N, K)] = oracle.quant_weight(synth.weight_bf16(N, K), oracle.BF16, 128,
-                                                    128, True)
-        qw, sw = _ORACLE_W[(N, K)]
-        xb = synth.act_decode(rows_per_shape, K)
-        best = None
-        for _ in range(reps):
-            t0 = time.perf_counter()
-            qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
-            oracle.gemm(qa, sa, qw, sw, True)
-            dt = time.perf_counter() - t0
-            best = dt if best is None else min(best, dt)
-        sample_s += best
-        est += best / rows_per_shape * total_rows
-    desc = (f"{rows_per_shape} activation row(s) per (N,K) through oracle quant + fp64 GEMM "
-            f"(all N columns), single thread; whole-step time extrapolated linearly in M "
-            f"({total_rows} rows per (N,K))")
-    return est, sample_s, desc
-
-
-def oracle_time_all_cores(threads=None):
-    """The same oracle routine over row partitions on all host cores: one row
-    per thread per (N,K), quant + fp64 GEMM row, threads around the unchanged
-    single-thread C calls (ctypes releases the GIL).  Returns (extrapolated
-    whole-step seconds, threads, description)."""
-    from concurrent.futures import ThreadPoolExecutor
-
-    import oracle
-    n = threads or os.cpu_count() or 1
-    total_rows = sum(synth.DECODE_M)
-    est = 0.0
-    for (N, K) in synth.DECODE_NK:
-        if (N, K) not in _ORACLE_W:
-            _ORACLE_W[(N, K)] = oracle.quant_weight(synth.weight_bf16(N, K), oracle.BF16, 128,
-                                                    128, True)
-        qw, sw = _ORACLE_W[(N, K)]
-        xb = synth.act_decode(n, K)
-
-        def one(r):
-            qa, sa = oracle.quant_act(np.ascontiguousarray(xb[r:r + 1]), oracle.BF16, 128, True)
-            oracle.gemm(qa, sa, qw, sw, True)
-
-        with ThreadPoolExecutor(max_workers=n) as ex:
-            t0 = time.perf_counter()
-            list(ex.map(one, range(n)))
-            dt = time.perf_counter() - t0
-        est += dt / n * total_rows
-    desc = (f"{n} activation rows per (N,K), one per thread on {n} threads (row partitions of "
-            "the same single-thread oracle routine); extrapolated linearly in M")
-    return est, n, desc
-
+# ------------------------------------------------------------- replicas
 
 def max_over_ranks(seconds: float, device) -> float:
     """The slowest rank's time: replicas report the whole job's throughput as
@@ -261,42 +238,847 @@ def max_over_ranks(seconds: float, device) -> float:
     return float(t.item())
 
 
-def job_value(bytes_per_rank: float, world: int, seconds: float) -> float:
-    """Whole-job GB/s of `world` replicas that each moved bytes_per_rank in
-    `seconds` (the max over ranks): weak scaling."""
-    return world * bytes_per_rank / seconds / 1e9
+def max_int_over_ranks(v: int, device) -> int:
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return int(t.item())
 
 
-def total_step_bytes():
-    return sum(step_bytes(M, N, K) for (M, N, K) in problems())
+def job_value(units_per_rank: float, world: int, seconds: float, scale: float = 1e9) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    units_per_rank in `seconds` (the max over ranks): weak scaling."""
+    return world * units_per_rank / seconds / scale
 
 
-def run_reference(args, rank, world):
+# ------------------------------------------------------------- workloads
+
+class Problem:
+    """One call of a linear sweep: (M, N, K), the output dtype and, for
+    repeated shapes, the copy index (its own weight and activation copy)."""
+
+    def __init__(self, M, N, K, odt, copy=0):
+        self.M, self.N, self.K, self.odt, self.copy = M, N, K, odt, copy
+
+    @property
+    def key(self):  # the tensors a problem reads (shared by its output dtypes)
+        return (self.M, self.N, self.K, self.copy)
+
+    @property
+    def shape(self):
+        return (self.M, self.N, self.K, self.odt)
+
+
+class Sweep:
+    """A linear-layer workload: problems, scale format, input recipes."""
+
+    def __init__(self, name, text, problems, fmt, act, weight, unit, act_oracle):
+        self.name, self.text, self.problems, self.fmt = name, text, problems, fmt
+        self.act, self.weight, self.unit, self.act_oracle = act, weight, unit, act_oracle
+
+    def config(self, world):
+        odts = sorted({p.odt for p in self.problems})
+        return {"workload": self.text, "problems_per_pass": len(self.problems),
+                "scale_fmt": self.fmt, "out_dtypes": odts,
+                "api": "fp8bq_linear (activation quant + GEMM, two launches with PDL)",
+                "l2": "inputs larger than L2: every problem reads its own weight and "
+                      "activation copy",
+                "parallelism": "replicas" if world > 1 else "single GPU"}
+
+    def units(self, p):
+        """Units of `value` one problem contributes."""
+        if self.unit == "TFLOPS":
+            return gemm_flops(p.M, p.N, p.K)
+        return linear_bytes(p.M, p.N, p.K, p.odt)
+
+    @property
+    def unit_scale(self):
+        return 1e12 if self.unit == "TFLOPS" else 1e9
+
+
+def _weight_bf16(N, K):
+    return synth.weight_bf16_blocked(N, K), "bf16"
+
+
+def _weight_f32(N, K):
+    return synth.normal_blocked((N, K), synth.SEED_WEIGHT, std=0.02), "fp32"
+
+
+def _act_small(M, K):
+    return synth.f32_to_bf16_bits_par(synth.normal_blocked((M, K), synth.SEED_ACT))
+
+
+def make_sweep(name):
+    if name == "grid":
+        probs = [Problem(M, N, K, odt) for odt in ("bf16", "fp16") for M in synth.M_GRID
+                 for (N, K) in synth.FULL_NK]
+        text = ("full grid: M in {1,2,4,8,16,24,32,48,64,96,128,256,512,1024,1536,2048,3072,"
+                "4096} x (N,K) in {(1536,7168),(7168,1536),(4096,7168),(7168,18432),"
+                "(18432,7168),(24576,7168)}, fp16 and bf16 out; fused quant+GEMM per call; "
+                "act bf16 N(0,1) 0.5% channels x50; weights bf16 N(0,0.02) 128x128; UE8M0")
+        return Sweep(name, text, probs, "ue8m0", synth.act_full_grid_blocked, _weight_bf16,
+                     "TFLOPS", synth.act_full_grid_blocked)
+    if name == "decode":
+        probs = [Problem(M, N, K, "bf16") for M in synth.DECODE_M for (N, K) in synth.DECODE_NK]
+        text = ("decode sweep: (N,K) in {(7168,18432),(18432,7168),(4096,7168)} x "
+                "M in {1,2,4,8,16,24,32,48,64,96,128}; act bf16 N(0,1), 1% channels x30 -> "
+                "per-token-group quant (UE8M0 packed); weights bf16 N(0,0.02) 128x128 UE8M0; "
+                "bf16 out")
+        return Sweep(name, text, probs, "ue8m0", synth.act_decode_blocked, _weight_bf16,
+                     "GB/s", synth.act_decode_blocked)
+    if name == "prefill":
+        probs = [Problem(M, N, K, odt) for odt in ("bf16", "fp32") for M in synth.PREFILL_M
+                 for (N, K) in synth.PREFILL_NK]
+        text = ("prefill sweep: (N,K) in {(24576,7168),(4096,7168),(7168,18432)} x "
+                "M in {256,512,1024,1536,2048,3072,4096}; act bf16 Student-t(3) unit RMS; "
+                "weights bf16 N(0,0.02) 128x128; fp32 scales; bf16 and fp32 out")
+        return Sweep(name, text, probs, "fp32", synth.act_prefill_blocked, _weight_bf16,
+                     "TFLOPS", synth.act_prefill_blocked)
+    if name == "small":
+        probs = [Problem(16, 1536, 1536, "bf16", c) for c in range(100)]
+        text = ("small: M=16, N=K=1536; act bf16 N(0,1); weights fp32 N(0,0.02) 128x128; "
+                "fp32 scales; bf16 out; 100 back-to-back calls per pass, each on its own "
+                "weight copy")
+        return Sweep(name, text, probs, "fp32", _act_small, _weight_f32, "GB/s", _act_small)
+    raise ValueError(name)
+
+
+# ------------------------------------------------------------- oracle legs
+
+def oracle_weights(sweep, host_w):
+    """The oracle's own quantisation of each (N,K) weight, in parallel
+    threads (the C calls release the GIL); outside every timing."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    ue = sweep.fmt == "ue8m0"
+    nks = sorted(host_w)
+
+    def one(nk):
+        w, kind = host_w[nk]
+        return nk, oracle.quant_weight(w, oracle.BF16 if kind == "bf16" else oracle.FP32, 128,
+                                       128, ue)
+
+    with ThreadPoolExecutor(max_workers=len(nks)) as ex:
+        return dict(ex.map(one, nks))
+
+
+def oracle_sample(sweep, qws, rows=1):
+    """Times the oracle on one thread: per (N,K), `rows` activation rows
+    through oracle quant + fp64 GEMM (all N columns).  Returns (whole-pass
+    seconds extrapolated linearly in M over the pass's problems, sample
+    seconds, description)."""
+    import oracle
+    ue = sweep.fmt == "ue8m0"
+    per_row, sample_s = {}, 0.0
+    for (N, K) in sorted(qws):
+        qw, sw = qws[(N, K)]
+        xb = np.ascontiguousarray(sweep.act_oracle(rows, K))
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(xb, oracle.BF16, 128, ue)
+        oracle.gemm(qa, sa, qw, sw, ue)
+        dt = time.perf_counter() - t0
+        sample_s += dt
+        per_row[(N, K)] = dt / rows
+    est = sum(per_row[(p.N, p.K)] * p.M for p in sweep.problems)
+    desc = (f"{rows} activation row(s) per (N,K) through oracle quant + fp64 GEMM (all N "
+            f"columns), single thread; the pass's time extrapolated linearly in M over its "
+            f"{len(sweep.problems)} problems")
+    return est, sample_s, desc
+
+
+def oracle_all_cores(sweep, qws, threads=None):
+    """The same routine over row partitions on all host cores (one row per
+    thread per (N,K)); returns (extrapolated pass seconds, threads, desc)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    ue = sweep.fmt == "ue8m0"
+    n = threads or os.cpu_count() or 1
+    per_row = {}
+    for (N, K) in sorted(qws):
+        qw, sw = qws[(N, K)]
+        xb = np.ascontiguousarray(sweep.act_oracle(n, K))
+
+        def one(r):
+            qa, sa = oracle.quant_act(np.ascontiguousarray(xb[r:r + 1]), oracle.BF16, 128, ue)
+            oracle.gemm(qa, sa, qw, sw, ue)
+
+        with ThreadPoolExecutor(max_workers=n) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(one, range(n)))
+            per_row[(N, K)] = (time.perf_counter() - t0) / n
+    est = sum(per_row[(p.N, p.K)] * p.M for p in sweep.problems)
+    return est, n, (f"{n} activation rows per (N,K), one per thread on {n} threads (row "
+                    "partitions of the same single-thread oracle routine); extrapolated "
+                    "linearly in M")
+
+
+QUANT_TEXT = ("standalone per-token-group quant: bf16 M x K, M in {1,64,1024,4096,16384} x "
+              "K in {1536,7168,18432}, group 128, N(0,1) with one +-1000 spike per group in "
+              "every 8th row; fp32 scales and UE8M0 scales packed 4 per int32 (column-major, "
+              "rows padded to a multiple of 4)")
+
+
+def quant_problems():
+    return [(M, K, fmt) for fmt in ("fp32", "ue8m0") for M in synth.QUANT_M
+            for K in synth.QUANT_K]
+
+
+def quant_config(world):
+    return {"workload": QUANT_TEXT, "problems_per_pass": len(quant_problems()),
+            "api": "fp8bq_quant_act",
+            "l2": "inputs larger than L2: every (M,K) reads its own input copy",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def quant_oracle_sample(rows=64):
+    import oracle
+    per_row, sample_s = {}, 0.0
+    for K in synth.QUANT_K:
+        xb = np.ascontiguousarray(synth.act_quant_blocked(rows, K))
+        for fmt in ("fp32", "ue8m0"):
+            t0 = time.perf_counter()
+            oracle.quant_act(xb, oracle.BF16, 128, fmt == "ue8m0")
+            dt = time.perf_counter() - t0
+            sample_s += dt
+            per_row[(K, fmt)] = dt / rows
+    est = sum(per_row[(K, fmt)] * M for (M, K, fmt) in quant_problems())
+    return est, sample_s, (f"{rows} rows per (K, scale format) through the oracle quant, single "
+                           "thread; extrapolated linearly in M")
+
+
+# ------------------------------------------------------------- GPU helpers
+
+def _events(torch, n, external):
+    mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if external else \
+        (lambda: torch.cuda.Event(enable_timing=True))
+    return [(mk(), mk()) for _ in range(n)]
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed_steps(torch, graph, args, world, dev, local, rank):
+    """W warm-up steps and K timed steps of `passes` replays each, CUDA events
+    on the launching stream around every step, clocks sampled from before the
+    warm-up to the end of the timed region.  Returns (mean step seconds --
+    the max over ranks --, passes, clocks, wall seconds of the timed region)."""
+    import torch.distributed as dist
+    cal = []
+    for _ in range(3):  # calibration (untimed): one pass at a time
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        cal.append(a.elapsed_time(b) / 1e3)
+    pass_s = min(cal)
+    passes = max(1, math.ceil(args.min_timed_s / (max(1, args.steps) * pass_s)))
+    if world > 1:
+        passes = max_int_over_ranks(passes, dev)
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    for _ in range(args.warmup):
+        for _ in range(passes):
+            graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = _events(torch, args.steps, False)
+    t0 = time.perf_counter()
+    for a, b in evs:
+        a.record()
+        for _ in range(passes):
+            graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop() if rank == 0 else None
+    step_s = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+    if world > 1:
+        step_s = max_over_ranks(step_s, dev)
+    return step_s, passes, clk, wall
+
+
+def _ext_events_ok(torch):
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+class Background:
+    """Runs fn() in a thread (the oracle legs, whose C calls release the GIL)
+    while the GPU is kept busy."""
+
+    def __init__(self, fn):
+        self.out, self.err = None, None
+
+        def run():
+            try:
+                self.out = fn()
+            except BaseException as e:  # reported by result()
+                self.err = e
+
+        self.t = threading.Thread(target=run, daemon=True)
+        self.t.start()
+
+    def done(self):
+        return not self.t.is_alive()
+
+    def result(self):
+        self.t.join()
+        if self.err is not None:
+            raise self.err
+        return self.out
+
+
+# ------------------------------------------------------------- linear sweeps
+
+def run_sweep(args, rank, world, sweep):
+    import torch
+
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ext = _ext_events_ok(torch)
+    if not ext:
+        raise RuntimeError("timing needs torch.cuda.Event(external=True) (events in a graph)")
+    fmt, probs = sweep.fmt, sweep.problems
+    keys = sorted({p.key for p in probs})
+    nks = sorted({(p.N, p.K) for p in probs})
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+
+    # ---- setup (untimed): weights quantised once, one copy per problem key
+    host_w, w_q, w_s = {}, {}, {}
+    for (N, K) in nks:
+        wh, kind = sweep.weight(N, K)
+        if want_cpu:
+            host_w[(N, K)] = (wh, kind)
+        if kind == "bf16":
+            wd = torch.from_numpy(wh.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            wd = torch.from_numpy(wh).to(dev)
+        q, s = fp8bq.fp8bq_quant_weight(wd, fmt)
+        del wd
+        w_s[(N, K)] = s
+        first = True
+        for k in keys:
+            if (k[1], k[2]) == (N, K):
+                w_q[k] = q if first else q.clone()
+                first = False
+    prep = Background(lambda: oracle_weights(sweep, host_w)) if want_cpu else None
+    max_m = {}
+    for p in probs:
+        max_m[p.K] = max(max_m.get(p.K, 0), p.M)
+    host_x = {K: sweep.act(Mx, K) for K, Mx in max_m.items()}
+    xs = {}
+    for k in keys:
+        M, N, K, _ = k
+        xs[k] = torch.from_numpy(host_x[K][:M].view(np.int16)).view(torch.bfloat16).to(dev)
+    outs = {p.shape + (p.copy,): torch.empty((p.M, p.N), dtype=fp8bq._CODE_TO_TORCH[
+        fp8bq._dtype_code(p.odt)], device=dev) for p in probs}
+    aqs, ass = {}, {}
+    for k in keys:
+        M, N, K, _ = k
+        shape, dt = fp8bq.act_scale_shape(M, K, 128, fmt)
+        aqs[k] = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        ass[k] = torch.empty(shape, dtype=dt, device=dev)
+    ws_bytes = max(fp8bq.fp8bq_linear_workspace_bytes(p.M, p.N, p.K, fmt, p.odt) for p in probs)
+    ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
+    variants = {p.shape: fp8bq.fp8bq_select_variant(p.M, p.N, p.K, fmt, p.odt) for p in probs}
+    torch.cuda.synchronize()
+
+    def out_of(p):
+        return outs[p.shape + (p.copy,)]
+
+    def step():
+        for p in probs:
+            fp8bq.fp8bq_linear(xs[p.key], w_q[p.key], w_s[(p.N, p.K)], fmt=fmt,
+                               out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
+
+    ev_i = _events(torch, len(probs), True)
+    ev_h = _events(torch, len(probs), True)
+
+    def step_instr():
+        # quant and GEMM as separate calls, events around every GEMM launch
+        for i, p in enumerate(probs):
+            fp8bq.fp8bq_quant_act(xs[p.key], fmt, q=aqs[p.key], s=ass[p.key])
+            ev_i[i][0].record()
+            fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w_q[p.key], w_s[(p.N, p.K)], fmt=fmt,
+                             out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
+            ev_i[i][1].record()
+
+    def step_hot():
+        # every GEMM twice in a row; the second one is timed (operands in L2
+        # as far as they fit)
+        for i, p in enumerate(probs):
+            g = lambda: fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w_q[p.key],  # noqa: E731
+                                         w_s[(p.N, p.K)], fmt=fmt, out_dtype=out_of(p).dtype,
+                                         out=out_of(p), workspace=ws)
+            g()
+            ev_h[i][0].record()
+            g()
+            ev_h[i][1].record()
+
+    chain_sets = {"all": list(range(len(probs)))}
+    low = [i for i, p in enumerate(probs) if p.M <= 64]
+    if low and len(low) < len(probs):
+        chain_sets["m_le_64"] = low
+
+    def chain_fn(idx):
+        def f():
+            for i in idx:
+                p = probs[i]
+                fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w_q[p.key], w_s[(p.N, p.K)], fmt=fmt,
+                                 out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
+        return f
+
+    # first launches: load the table, set kernel attributes
+    step()
+    step_instr()
+    torch.cuda.synchronize()
+    g_step = capture(torch, step)
+    g_instr = capture(torch, step_instr)
+    g_hot = capture(torch, step_hot)
+    g_chain = {name: capture(torch, chain_fn(idx)) for name, idx in chain_sets.items()}
+
+    step_s, passes, clk, wall = timed_steps(torch, g_step, args, world, dev, local, rank)
+    launches = args.steps * passes * 2 * len(probs)
+
+    # ---- per-GEMM durations (instrumented pass), the oracle timed meanwhile
+    qws = prep.result() if prep is not None else None
+    cpu_job = None
+    if want_cpu:
+        def cpu_legs():
+            est, sample_s, desc = oracle_sample(sweep, qws, rows=args.oracle_rows)
+            est_all, nthr, desc_all = oracle_all_cores(sweep, qws)
+            return est, sample_s, desc, est_all, nthr, desc_all
+        cpu_job = Background(cpu_legs)
+    gemm_ms = np.zeros(len(probs))
+    n_instr = 0
+    while n_instr < args.instr_passes or (cpu_job is not None and not cpu_job.done()):
+        g_instr.replay()
+        torch.cuda.synchronize()
+        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_i])
+        n_instr += 1
+    gemm_us = gemm_ms / n_instr * 1e3
+    hot_ms = np.zeros(len(probs))
+    for _ in range(args.instr_passes):
+        g_hot.replay()
+        torch.cuda.synchronize()
+        hot_ms += np.array([a.elapsed_time(b) for a, b in ev_h])
+    hot_us = hot_ms / args.instr_passes * 1e3
+    chain_s = {}
+    for name, g in g_chain.items():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.instr_passes):
+            g.replay()
+        b.record()
+        b.synchronize()
+        chain_s[name] = a.elapsed_time(b) / 1e3 / args.instr_passes
+    assert fp8bq.fp8bq_device_status() == 0
+
+    # ---- end to end through fp8bq_linear with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = sweep_e2e(torch, fp8bq, args, world, dev, sweep, host_x, w_q, w_s, ws, out_of)
+
     if rank != 0:
         return 0
-    steps, warm = args.steps_ref, max(0, args.warmup)
-    for _ in range(warm):
-        oracle_time_sample(1)
-    ests = []
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        est, _, desc = oracle_time_sample(1)
-        ests.append(est)
-    wall = time.perf_counter() - t0
-    est = float(np.mean(ests))
-    value = total_step_bytes() / est / 1e9
+    peaks = load_peaks()
+    fp8 = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
+    fp8_sus = peaks["bf16_tflops_sustained"] * FP8_TO_BF16_NOMINAL
+    per = []
+    for i, p in enumerate(probs):
+        t = gemm_us[i] * 1e-6
+        byt = gemm_bytes(p.M, p.N, p.K, fmt, p.odt)
+        fl = gemm_flops(p.M, p.N, p.K)
+        tr, bound = roof_time(byt, fl, peaks)
+        per.append({"m": p.M, "n": p.N, "k": p.K, "out": p.odt, "copy": p.copy,
+                    "us": gemm_us[i], "us_hot": hot_us[i], "tflops": fl / t / 1e12,
+                    "gbs_pages": pages_gbs_bytes(p.M, p.N, p.K) / t / 1e9,
+                    "gbs_alg": byt / t / 1e9, "roofline_frac": tr / t, "bound": bound,
+                    "variant": variant_name(variants[p.shape]),
+                    "h100_deepgemm_us": H100_DEEPGEMM_US.get((p.M, p.N, p.K))})
+    per = merge_copies(per)
+
+    def regime(sel, kind):
+        rows = [(i, p) for i, p in enumerate(probs) if sel(p)]
+        if not rows:
+            return None
+        t = sum(gemm_us[i] for i, _ in rows) * 1e-6
+        if kind == "hbm":
+            byt = sum(gemm_bytes(p.M, p.N, p.K, fmt, p.odt) for _, p in rows)
+            fr = [gemm_bytes(p.M, p.N, p.K, fmt, p.odt) / (peaks["hbm_gbs"] * 1e9) /
+                  (gemm_us[i] * 1e-6) for i, p in rows]
+            out = {"gemms": len(rows), "gbs_alg": byt / t / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                   "frac": byt / t / 1e9 / peaks["hbm_gbs"], "frac_min": min(fr),
+                   "frac_max": max(fr), "peak_source": "measured copy bandwidth"}
+            if "m_le_64" in chain_s and sel is _m_le_64:
+                out["frac_chained"] = byt / chain_s["m_le_64"] / 1e9 / peaks["hbm_gbs"]
+                out["chain_us"] = chain_s["m_le_64"] * 1e6
+            return out
+        fl = sum(gemm_flops(p.M, p.N, p.K) for _, p in rows)
+        fr = [gemm_flops(p.M, p.N, p.K) / (fp8 * 1e12) / (gemm_us[i] * 1e-6) for i, p in rows]
+        return {"gemms": len(rows), "tflops": fl / t / 1e12, "peak_tflops": fp8,
+                "frac": fl / t / 1e12 / fp8, "frac_min": min(fr), "frac_max": max(fr),
+                "frac_of_sustained": fl / t / 1e12 / fp8_sus,
+                "peak_source": "2 x measured bf16 cuBLAS burst (nominal fp8/bf16 ratio); "
+                               "frac_of_sustained against 2 x the sustained bf16 figure"}
+
+    targets = {"m_le_64_vs_hbm": regime(_m_le_64, "hbm"),
+               "m_ge_2048_vs_fp8": regime(lambda p: p.M >= 2048, "tensor")}
+
+    # the dominant kernel class: the GEMM launches of the bound that holds
+    # most of the instrumented time
+    cls = {"hbm": [], "tensor": []}
+    for i, p in enumerate(probs):
+        byt = gemm_bytes(p.M, p.N, p.K, fmt, p.odt)
+        cls[roof_time(byt, gemm_flops(p.M, p.N, p.K), peaks)[1]].append(i)
+    dom = max(cls, key=lambda c: sum(gemm_us[i] for i in cls[c]))
+    idx = cls[dom]
+    t_dom = sum(gemm_us[i] for i in idx) * 1e-6
+    names = sorted({variant_name(variants[probs[i].shape]) for i in idx})
+    n_mx = sum(1 for i in idx if variants[probs[i].shape]["mma_scale"])
+    kern = (f"block-scaled FP8 GEMM, {len(idx)} {dom}-bound launches of the pass "
+            f"({n_mx} gemm_mx_kernel, {len(idx) - n_mx} gemm_kernel; variants "
+            f"{', '.join(names[:12])}{' ...' if len(names) > 12 else ''})")
+    alg_bytes_dom = sum(gemm_bytes(probs[i].M, probs[i].N, probs[i].K, fmt, probs[i].odt)
+                        for i in idx)
+    ratio = profile_traffic(f"gemm_{sweep.name}_traffic.txt", gemm_source_hash())
+    traffic = None if ratio is None else ratio * alg_bytes_dom / len(idx)
+    if dom == "tensor":
+        fl = sum(gemm_flops(probs[i].M, probs[i].N, probs[i].K) for i in idx)
+        ach = fl / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_sus, "unit": "TFLOP/s",
+                "frac": ach / fp8_sus, "traffic": traffic,
+                "frac_of_burst_peak": ach / fp8,
+                "peak_source": f"{peaks['source']}: 2 x bf16_tflops_sustained (the kernel is "
+                               "timed inside a seconds-long loop; nominal fp8/bf16 ratio 2)"}
+    else:
+        ach = alg_bytes_dom / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
+        if len(chain_sets["all"]) == len(idx):
+            roof["achieved_chained"] = alg_bytes_dom / chain_s["all"] / 1e9
+            roof["frac_chained"] = roof["achieved_chained"] / peaks["hbm_gbs"]
+    roof.update({"kernel": kern, "launches_per_pass": len(idx),
+                 "algorithmic_bytes_per_launch": alg_bytes_dom / len(idx),
+                 "method": "achieved = the class's algorithmic flops (or bytes) over the sum "
+                           "of its launches' durations, each GEMM timed alone between CUDA "
+                           "events in a graph replay of the pass (cold: every GEMM reads its "
+                           "own weight copy); traffic = the ncu DRAM bytes per algorithmic "
+                           "byte of the committed summary x the class's bytes per launch"})
+
+    cpu = None
+    if cpu_job is not None:
+        est, sample_s, desc, est_all, nthr, desc_all = cpu_job.result()
+        units = sum(sweep.units(p) for p in probs)
+        cpu = {"value": units / est / sweep.unit_scale, "unit": sweep.unit, "cores": 1,
+               "kind": "oracle", "extrapolated": True,
+               "sample": desc + f" (sample took {sample_s:.1f} s; run while the GPU's "
+                                "per-GEMM passes ran)",
+               "all_cores": {"value": units / est_all / sweep.unit_scale, "unit": sweep.unit,
+                             "cores": nthr, "sample": desc_all}}
+    units_pass = sum(sweep.units(p) for p in probs)
+    value = job_value(units_pass * passes, world, step_s, sweep.unit_scale)
+    t_roof_pass = sum(roof_time(linear_bytes(p.M, p.N, p.K, p.odt), gemm_flops(p.M, p.N, p.K),
+                                peaks)[0] for p in probs)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
-        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": est * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-        "wall_s": wall,
+        "metric": METRIC, "value": value, "unit": sweep.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic", "config": sweep.config(world),
+        "passes_per_step": passes,
+        "timing": "graph replays; a step = passes_per_step passes over the problems (the "
+                  "smallest count that makes the timed region >= --min-timed-s); CUDA events "
+                  "on the launching stream around every step; 3 untimed calibration passes "
+                  "before the warm-up; per_shape from an instrumented graph (quant and GEMM "
+                  "as separate calls, events around every GEMM launch)",
+        "step_roofline_frac": t_roof_pass * passes / step_s,
+        "roofline": roof, "targets": targets, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk,
+        "gemm_chain_us": {k: v * 1e6 for k, v in chain_s.items()},
+        "instrumented_passes": n_instr, "per_shape": per, "wall_timed_s": wall,
+        "gemm_source_sha256_16": gemm_source_hash(),
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(_round(line)), flush=True)
+    return 0
+
+
+def _m_le_64(p):
+    return p.M <= 64
+
+
+def merge_copies(per):
+    """One entry per (m, n, k, out): the mean over the problem's copies."""
+    groups = {}
+    for e in per:
+        groups.setdefault((e["m"], e["n"], e["k"], e["out"]), []).append(e)
+    out = []
+    for key, es in groups.items():
+        e = dict(es[0])
+        e.pop("copy")
+        for f in ("us", "us_hot", "tflops", "gbs_pages", "gbs_alg", "roofline_frac"):
+            e[f] = float(np.mean([x[f] for x in es]))
+        if len(es) > 1:
+            e["copies"] = len(es)
+        out.append(e)
+    return out
+
+
+def _round(o):
+    if isinstance(o, float):
+        return float(f"{o:.6g}")
+    if isinstance(o, dict):
+        return {k: _round(v) for k, v in o.items()}
+    if isinstance(o, list):
+        return [_round(v) for v in o]
+    return o
+
+
+def sweep_e2e(torch, fp8bq, args, world, dev, sweep, host_x, w_q, w_s, ws, out_of):
+    """fp8bq_linear per problem with every input copied in from pinned host
+    memory and every output copied back, each step.  The copies overlap the
+    compute: inputs go up on one side stream, the compute stream waits once
+    per 6 problems (each cross-stream wait cuts the chain of programmatic
+    launches), outputs go back on another side stream as each layer ends."""
+    probs, fmt = sweep.problems, sweep.fmt
+    hx = {K: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+          for K, v in host_x.items()}
+    xd = {i: torch.empty((p.M, p.K), dtype=torch.bfloat16, device=dev)
+          for i, p in enumerate(probs)}
+    ho = {i: torch.empty(out_of(p).shape, dtype=out_of(p).dtype).pin_memory()
+          for i, p in enumerate(probs)}
+    h2d = sum(2 * p.M * p.K for p in probs)
+    d2h = sum(OUT_SIZE[p.odt] * p.M * p.N for p in probs)
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    wait_every = 6
+
+    def e2e_step():
+        cur = torch.cuda.current_stream()
+        h2d_s.wait_stream(cur)
+        d2h_s.wait_stream(cur)
+        ready = []
+        with torch.cuda.stream(h2d_s):
+            for i, p in enumerate(probs):
+                xd[i].copy_(hx[p.K][:p.M], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(h2d_s)
+                ready.append(e)
+        for i, p in enumerate(probs):
+            if i % wait_every == 0:
+                cur.wait_event(ready[min(i + wait_every, len(probs)) - 1])
+            o = out_of(p)
+            fp8bq.fp8bq_linear(xd[i], w_q[p.key], w_s[(p.N, p.K)], fmt=fmt, out_dtype=o.dtype,
+                               out=o, workspace=ws)
+            done = torch.cuda.Event()
+            done.record(cur)
+            d2h_s.wait_event(done)
+            with torch.cuda.stream(d2h_s):
+                ho[i].copy_(o, non_blocking=True)
+        cur.wait_stream(h2d_s)
+        cur.wait_stream(d2h_s)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    g = capture(torch, e2e_step)
+    for _ in range(max(1, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, args.e2e_steps))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    b.synchronize()
+    s = a.elapsed_time(b) / 1e3 / n
+    if world > 1:
+        s = max_over_ranks(s, dev)
+    units = sum(sweep.units(p) for p in probs)
+    return {"value": job_value(units, world, s, sweep.unit_scale), "unit": sweep.unit,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": s * 1e3,
+            "steps": n, "passes_per_step": 1,
+            "api": "fp8bq_linear per problem (graph); every step copies each problem's input "
+                   "from pinned host memory on a side stream ahead of its layer (the compute "
+                   "waits once per 6 problems) and its output back on another side stream"}
+
+
+# ------------------------------------------------------------- quant workload
+
+def run_quant(args, rank, world):
+    import torch
+
+    from block_scaled_fp8_group_gb300 import build
+    build.build()
+    from block_scaled_fp8_group_gb300 import fp8bq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    probs = quant_problems()
+    base = {K: synth.act_quant_blocked(max(synth.QUANT_M), K) for K in synth.QUANT_K}
+    xs = {(M, K): torch.from_numpy(base[K][:M].view(np.int16)).view(torch.bfloat16).to(dev)
+          for (M, K, _) in probs}
+    qs, ss = {}, {}
+    for (M, K, fmt) in probs:
+        shape, dt = fp8bq.act_scale_shape(M, K, 128, fmt)
+        qs[(M, K, fmt)] = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        ss[(M, K, fmt)] = torch.empty(shape, dtype=dt, device=dev)
+
+    def call(p):
+        M, K, fmt = p
+        fp8bq.fp8bq_quant_act(xs[(M, K)], fmt, q=qs[p], s=ss[p])
+
+    def step():
+        for p in probs:
+            call(p)
+
+    ev_i = _events(torch, len(probs), True)
+    ev_h = _events(torch, len(probs), True)
+
+    def step_instr():
+        for i, p in enumerate(probs):
+            ev_i[i][0].record()
+            call(p)
+            ev_i[i][1].record()
+
+    def step_hot():
+        for i, p in enumerate(probs):
+            call(p)
+            ev_h[i][0].record()
+            call(p)
+            ev_h[i][1].record()
+
+    step()
+    torch.cuda.synchronize()
+    g_step, g_instr, g_hot = capture(torch, step), capture(torch, step_instr), capture(torch,
+                                                                                       step_hot)
+    step_s, passes, clk, wall = timed_steps(torch, g_step, args, world, dev, local, rank)
+    cpu_job = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_job = Background(lambda: quant_oracle_sample(args.oracle_rows * 16))
+    us = np.zeros(len(probs))
+    n_instr = 0
+    while n_instr < args.instr_passes or (cpu_job is not None and not cpu_job.done()):
+        g_instr.replay()
+        torch.cuda.synchronize()
+        us += np.array([a.elapsed_time(b) for a, b in ev_i]) * 1e3
+        n_instr += 1
+    us /= n_instr
+    hot = np.zeros(len(probs))
+    for _ in range(args.instr_passes):
+        g_hot.replay()
+        torch.cuda.synchronize()
+        hot += np.array([a.elapsed_time(b) for a, b in ev_h]) * 1e3
+    hot /= args.instr_passes
+    assert fp8bq.fp8bq_device_status() == 0
+
+    e2e = None
+    if not args.no_e2e:
+        hx = {K: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+              for K, v in base.items()}
+        xd = {p: torch.empty((p[0], p[1]), dtype=torch.bfloat16, device=dev) for p in probs}
+        hq = {p: torch.empty(qs[p].shape, dtype=torch.uint8).pin_memory() for p in probs}
+        hs = {p: torch.empty(ss[p].shape, dtype=ss[p].dtype).pin_memory() for p in probs}
+        h2d = sum(2 * M * K for (M, K, _) in probs)
+        d2h = sum(M * K + act_scale_bytes(M, K, f) for (M, K, f) in probs)
+
+        def e2e_step():
+            for p in probs:
+                M, K, fmt = p
+                xd[p].copy_(hx[K][:M], non_blocking=True)
+                fp8bq.fp8bq_quant_act(xd[p], fmt, q=qs[p], s=ss[p])
+                hq[p].copy_(qs[p], non_blocking=True)
+                hs[p].copy_(ss[p], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        g = capture(torch, e2e_step)
+        for _ in range(max(1, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        n = max(1, min(args.steps, args.e2e_steps))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            g.replay()
+        b.record()
+        b.synchronize()
+        s = a.elapsed_time(b) / 1e3 / n
+        if world > 1:
+            s = max_over_ranks(s, dev)
+        e2e = {"value": job_value(sum(quant_bytes(*p) for p in probs), world, s), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": s * 1e3,
+               "steps": n, "api": "fp8bq_quant_act per problem (graph), input copied in from "
+                                  "pinned host memory, codes and scales copied back, serially"}
+    if rank != 0:
+        return 0
+    peaks = load_peaks()
+    per = []
+    for i, (M, K, fmt) in enumerate(probs):
+        b = quant_bytes(M, K, fmt)
+        per.append({"m": M, "k": K, "scale_fmt": fmt, "us": us[i], "us_hot": hot[i],
+                    "gbs_alg": b / (us[i] * 1e-6) / 1e9,
+                    "roofline_frac": b / (peaks["hbm_gbs"] * 1e9) / (us[i] * 1e-6)})
+    tot = sum(quant_bytes(*p) for p in probs)
+    ach = tot / (us.sum() * 1e-6) / 1e9
+    ratio = profile_traffic("quant_act_traffic.txt", quant_source_hash())
+    roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"],
+            "traffic": None if ratio is None else ratio * tot / len(probs),
+            "kernel": f"quant_act_kernel, {len(probs)} launches per pass",
+            "algorithmic_bytes_per_launch": tot / len(probs),
+            "method": "achieved = the pass's algorithmic bytes over the sum of the launches' "
+                      "durations, each timed alone between CUDA events in a graph replay",
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
+    by_fmt = {}
+    for fmt in ("fp32", "ue8m0"):
+        sel = [i for i, p in enumerate(probs) if p[2] == fmt and p[0] >= 4096]
+        b = sum(quant_bytes(*probs[i]) for i in sel)
+        by_fmt[fmt] = {"m_ge_4096_frac": b / (sum(us[i] for i in sel) * 1e-6) / 1e9 /
+                       peaks["hbm_gbs"]}
+    cpu = None
+    if cpu_job is not None:
+        est, sample_s, desc = cpu_job.result()
+        cpu = {"value": tot / est / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "extrapolated": True, "sample": desc + f" (sample took {sample_s:.2f} s)"}
+    line = {
+        "metric": METRIC, "value": job_value(tot * passes, world, step_s), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": quant_config(world),
+        "passes_per_step": passes,
+        "timing": "graph replays; a step = passes_per_step passes over the 30 quant calls; "
+                  "CUDA events on the launching stream around every step",
+        "roofline": roof, "targets": by_fmt, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * passes * len(probs), "clocks": clk, "per_shape": per,
+        "wall_timed_s": wall, "quant_source_sha256_16": quant_source_hash(),
+    }
+    print(json.dumps(_round(line)), flush=True)
     return 0
 
 
@@ -332,9 +1114,30 @@ def moe_bytes(N, K, counts, linear):
     return w + a + 2 * toks * N
 
 
+def moe_oracle_sample():
+    """The oracle on one thread over one token row of each MoE problem (quant
+    of the row + its GEMM row against its expert's weights), extrapolated
+    linearly to the problem's token rows."""
+    import oracle
+    est, sample_s = 0.0, 0.0
+    for (T, N, K, counts, M_max) in moe_problems():
+        e = int(np.argmax(counts > 0))
+        wb = synth.moe_weight_bf16(1, N, K, seed=synth.SEED_WEIGHT + 1000 * e)[0]
+        qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+        xb = synth.act_decode(1, K)
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
+        oracle.gemm(qa, sa, qw, sw, True)
+        dt = time.perf_counter() - t0
+        sample_s += dt
+        est += dt * int(counts.sum())
+    return est, sample_s, ("one token row per MoE problem through oracle quant + fp64 GEMM "
+                           "(all N columns of its expert), single thread; extrapolated "
+                           "linearly to each problem's token rows")
+
+
 def run_gpu_moe(args, rank, world):
     import torch
-    import torch.distributed as dist
 
     from block_scaled_fp8_group_gb300 import build
     build.build()
@@ -380,9 +1183,7 @@ def run_gpu_moe(args, rank, world):
             fp8bq.fp8bq_grouped_linear(xs[i], wq[i], ws[i], cnts[i], fmt="ue8m0", out=outs[i],
                                        workspace=wspace)
 
-    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-    ev = [(mk(), mk()) for _ in probs]
-    ev_s, ev_e, ev2_s, ev2_e = mk(), mk(), mk(), mk()
+    ev = _events(torch, len(probs), True)
 
     def step_split():
         for i in range(len(probs)):
@@ -395,42 +1196,14 @@ def run_gpu_moe(args, rank, world):
     step()
     step_split()
     torch.cuda.synchronize()
-    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g1, stream=side):
-            ev_s.record()
-            step()
-            ev_e.record()
-        with torch.cuda.graph(g2, stream=side):
-            ev2_s.record()
-            step_split()
-            ev2_e.record()
-    torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        g1.replay()
-        g2.replay()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    step_ms = []
-    t_wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        g1.replay()
-        ev_e.synchronize()
-        step_ms.append(ev_s.elapsed_time(ev_e))
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
-    step_s = float(np.mean(step_ms)) / 1e3
-    n_instr = max(1, min(args.steps, args.instr_steps))
+    g1, g2 = capture(torch, step), capture(torch, step_split)
+    step_s, passes, clk, wall = timed_steps(torch, g1, args, 1, dev, local, rank)
     gemm_ms = np.zeros(len(probs))
-    for _ in range(n_instr):
+    for _ in range(args.instr_passes):
         g2.replay()
-        ev2_e.synchronize()
+        torch.cuda.synchronize()
         gemm_ms += np.array([a.elapsed_time(b) for a, b in ev])
-    gemm_us = gemm_ms / n_instr * 1e3
+    gemm_us = gemm_ms / args.instr_passes * 1e3
     assert fp8bq.fp8bq_device_status() == 0
 
     # end to end: activations and counts from pinned host memory, outputs back
@@ -450,12 +1223,8 @@ def run_gpu_moe(args, rank, world):
 
     e2e_step()
     torch.cuda.synchronize()
-    g3 = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g3, stream=side):
-            e2e_step()
-    torch.cuda.synchronize()
-    for _ in range(args.warmup):
+    g3 = capture(torch, e2e_step)
+    for _ in range(max(1, args.warmup)):
         g3.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -468,18 +1237,17 @@ def run_gpu_moe(args, rank, world):
     e2e_s = a.elapsed_time(b) / 1e3 / n_e2e
     step_total = sum(moe_bytes(p[1], p[2], p[3], True) for p in probs)
     peaks = load_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
     per = []
     for i, (T, N, K, counts, M_max) in enumerate(probs):
         t = gemm_us[i] * 1e-6
         byt = moe_bytes(N, K, counts, False)
         fl = 2.0 * int(counts.sum()) * N * K
-        t_roof = max(byt / (peaks["hbm_gbs"] * 1e9), fl / (fp8_peak * 1e12))
+        tr, bound = roof_time(byt, fl, peaks)
         per.append({"tokens": T, "n": N, "k": K, "experts": E, "m_max": M_max,
                     "experts_with_tokens": int((counts > 0).sum()),
-                    "token_rows": int(counts.sum()), "us": round(gemm_us[i], 3),
-                    "tflops": round(fl / t / 1e12, 2), "gbs_alg": round(byt / t / 1e9, 1),
-                    "roofline_frac": round(t_roof / t, 3),
+                    "token_rows": int(counts.sum()), "us": gemm_us[i],
+                    "tflops": fl / t / 1e12, "gbs_alg": byt / t / 1e9,
+                    "roofline_frac": tr / t, "bound": bound,
                     "variant": variant_name(variants[i])})
     tot_gemm = sum(moe_bytes(p[1], p[2], p[3], False) for p in probs)
     achieved = tot_gemm / (gemm_us.sum() * 1e-6) / 1e9
@@ -487,57 +1255,34 @@ def run_gpu_moe(args, rank, world):
     if not args.no_cpu_baseline:
         est, sample_s, desc = moe_oracle_sample()
         cpu = {"value": step_total / est / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f" (sample took {sample_s:.1f} s)"}
+               "extrapolated": True, "sample": desc + f" (sample took {sample_s:.1f} s)"}
     line = {
-        "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
+        "metric": METRIC, "value": step_total * passes / step_s / 1e9, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": MOE_WORKLOAD, "problems_per_step": len(probs),
+        "config": {"workload": MOE_WORKLOAD, "problems_per_pass": len(probs),
                    "l2": "inputs larger than L2: every problem reads its own weight copy "
                          "(0.47-0.94 GB each)",
-                   "timing": "graph: step = fp8bq_grouped_linear per problem, CUDA events on "
-                             "the launching stream; per-GEMM durations from an instrumented "
-                             "pass (quant and grouped GEMM as separate calls)",
                    "parallelism": "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": None,
+        "passes_per_step": passes,
+        "timing": "graph: a pass = fp8bq_grouped_linear per problem; a step = passes_per_step "
+                  "passes; per-GEMM durations from an instrumented pass",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "grouped block-FP8 GEMM (gemm_kernel / gemm_mx_kernel, grouped "
-                               "tiles), 4 launches per step",
+                               "tiles), 4 launches per pass",
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"},
         "cpu_baseline": cpu,
         "e2e": {"value": step_total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
                 "api": "fp8bq_grouped_linear per problem (graph), activations and counts "
                        "copied in from pinned host memory and outputs copied back each step"},
-        "gpu_launches": args.steps * 2 * len(probs), "clocks": clk, "per_shape": per,
-        "wall_timed_s": round(t_wall, 3), "gemm_source_sha256_16": gemm_source_hash(),
+        "gpu_launches": args.steps * passes * 2 * len(probs), "clocks": clk, "per_shape": per,
+        "wall_timed_s": wall, "gemm_source_sha256_16": gemm_source_hash(),
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(_round(line)), flush=True)
     return 0
-
-
-def moe_oracle_sample():
-    """The oracle on one thread over one token row of each MoE problem (quant
-    of the row + its GEMM row against its expert's weights), extrapolated
-    linearly to the problem's token rows."""
-    import oracle
-    est, sample_s = 0.0, 0.0
-    for (T, N, K, counts, M_max) in moe_problems():
-        e = int(np.argmax(counts > 0))
-        wb = synth.moe_weight_bf16(1, N, K, seed=synth.SEED_WEIGHT + 1000 * e)[0]
-        qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
-        xb = synth.act_decode(1, K)
-        t0 = time.perf_counter()
-        qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
-        oracle.gemm(qa, sa, qw, sw, True)
-        dt = time.perf_counter() - t0
-        sample_s += dt
-        est += dt * int(counts.sum())
-    return est, sample_s, ("one token row per MoE problem through oracle quant + fp64 GEMM "
-                           "(all N columns of its expert), single thread; extrapolated "
-                           "linearly to each problem's token rows")
 
 
 # ----------------------------------------------- rowwise (per-token x per-channel)
@@ -637,6 +1382,36 @@ class FormatCalls:
         return block_int8_step_bytes(M, N, K) if self.block else rowwise_step_bytes(M, N, K)
 
 
+def rowwise_problems():
+    return [(M, N, K) for M in synth.DECODE_M for (N, K) in synth.DECODE_NK]
+
+
+def rowwise_oracle_sample(code):
+    """The oracle on one thread over one activation row per (N,K) of the
+    rowwise workload, extrapolated linearly in M."""
+    import oracle
+    est, sample_s = 0.0, 0.0
+    for (N, K) in synth.DECODE_NK:
+        wb = synth.weight_bf16_blocked(N, K)
+        xb = synth.act_decode(1, K)
+        if code == "int8block":
+            qw, sw = oracle.quant_weight_int8(wb, oracle.BF16)
+            t0 = time.perf_counter()
+            qa, sa = oracle.quant_act_int8(xb, oracle.BF16)
+            oracle.gemm_int8_block(qa, sa, qw, sw)
+        else:
+            i8 = code == "int8"
+            qw, sw = oracle.quant_rows(wb, oracle.BF16, int8=i8)
+            t0 = time.perf_counter()
+            qa, sa = oracle.quant_rows(xb, oracle.BF16, int8=i8)
+            oracle.gemm_rowcol(qa, sa, qw, sw, i8)
+        dt = time.perf_counter() - t0
+        sample_s += dt
+        est += dt * sum(synth.DECODE_M)
+    return est, sample_s, ("one activation row per (N,K) through the oracle's quant and GEMM, "
+                           "single thread; extrapolated linearly in M")
+
+
 def run_gpu_rowwise(args, rank, world):
     import torch
 
@@ -649,10 +1424,11 @@ def run_gpu_rowwise(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    probs = problems()
+    probs = rowwise_problems()
     w_q, w_s = {}, {}
     for (N, K) in synth.DECODE_NK:
-        wd = torch.from_numpy(synth.weight_bf16(N, K).view(np.int16)).view(torch.bfloat16).to(dev)
+        wd = torch.from_numpy(synth.weight_bf16_blocked(N, K).view(np.int16)).view(
+            torch.bfloat16).to(dev)
         q, s = fc.quant_w(wd)
         del wd
         for M in synth.DECODE_M:
@@ -668,9 +1444,7 @@ def run_gpu_rowwise(args, rank, world):
     ws_bytes = max(fc.linear_ws(*p) for p in probs)
     ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
     variants = {p: fc.select(*p) for p in probs}
-    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-    ev = [(mk(), mk()) for _ in probs]
-    ev_s, ev_e, ev2_s, ev2_e = mk(), mk(), mk(), mk()
+    ev = _events(torch, len(probs), True)
 
     def step():
         for p in probs:
@@ -686,42 +1460,14 @@ def run_gpu_rowwise(args, rank, world):
     step()
     step_split()
     torch.cuda.synchronize()
-    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g1, stream=side):
-            ev_s.record()
-            step()
-            ev_e.record()
-        with torch.cuda.graph(g2, stream=side):
-            ev2_s.record()
-            step_split()
-            ev2_e.record()
-    torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        g1.replay()
-        g2.replay()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    step_ms = []
-    t_wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        g1.replay()
-        ev_e.synchronize()
-        step_ms.append(ev_s.elapsed_time(ev_e))
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
-    step_s = float(np.mean(step_ms)) / 1e3
-    n_instr = max(1, min(args.steps, args.instr_steps))
+    g1, g2 = capture(torch, step), capture(torch, step_split)
+    step_s, passes, clk, wall = timed_steps(torch, g1, args, 1, dev, local, rank)
     gemm_ms = np.zeros(len(probs))
-    for _ in range(n_instr):
+    for _ in range(args.instr_passes):
         g2.replay()
-        ev2_e.synchronize()
+        torch.cuda.synchronize()
         gemm_ms += np.array([a.elapsed_time(b) for a, b in ev])
-    gemm_us = gemm_ms / n_instr * 1e3
+    gemm_us = gemm_ms / args.instr_passes * 1e3
     assert fp8bq.fp8bq_device_status() == 0
 
     # large M: the GEMM alone, two weight copies alternating (each > L2 / 2)
@@ -731,7 +1477,7 @@ def run_gpu_rowwise(args, rank, world):
     for (N, K) in synth.DECODE_NK:
         wq2 = [w_q[(1, N, K)], w_q[(2, N, K)]]
         for M in ROWWISE_PREFILL_M:
-            xa = torch.from_numpy(synth.act_prefill(M, K).view(np.int16)).view(
+            xa = torch.from_numpy(synth.act_prefill_blocked(M, K).view(np.int16)).view(
                 torch.bfloat16).to(dev)
             aq, as_ = fc.quant_a(xa)
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -740,8 +1486,7 @@ def run_gpu_rowwise(args, rank, world):
             for i in range(3):
                 fc.gemm(aq, as_, wq2[i % 2], w_s[(N, K)], o, wsp)
             reps = 10
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(reps)]
+            evs = _events(torch, reps, False)
             for i in range(reps):
                 evs[i][0].record()
                 fc.gemm(aq, as_, wq2[i % 2], w_s[(N, K)], o, wsp)
@@ -749,11 +1494,10 @@ def run_gpu_rowwise(args, rank, world):
             torch.cuda.synchronize()
             us = float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
             fl = gemm_flops(M, N, K)
-            entry = {"m": M, "n": N, "k": K, "us": round(us, 2),
-                     "tflops": round(fl / us / 1e6, 1),
+            entry = {"m": M, "n": N, "k": K, "us": us, "tflops": fl / us / 1e6,
                      "variant": variant_name(fc.select(M, N, K))}
             if code == "e4m3":
-                entry["frac_of_fp8_peak"] = round(fl / us / 1e6 / fp8_peak, 3)
+                entry["frac_of_fp8_peak"] = fl / us / 1e6 / fp8_peak
             prefill.append(entry)
             del xa, aq, as_, o
     assert fp8bq.fp8bq_device_status() == 0
@@ -762,10 +1506,9 @@ def run_gpu_rowwise(args, rank, world):
     for i, (M, N, K) in enumerate(probs):
         t = gemm_us[i] * 1e-6
         b = fc.gemm_bytes(M, N, K)
-        per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
-                    "tflops": round(gemm_flops(M, N, K) / t / 1e12, 2),
-                    "gbs_alg": round(b / t / 1e9, 1),
-                    "roofline_frac": round(b / (peaks["hbm_gbs"] * 1e9) / t, 3),
+        per.append({"m": M, "n": N, "k": K, "us": gemm_us[i],
+                    "tflops": gemm_flops(M, N, K) / t / 1e12, "gbs_alg": b / t / 1e9,
+                    "roofline_frac": b / (peaks["hbm_gbs"] * 1e9) / t,
                     "variant": variant_name(variants[(M, N, K)])})
     tot = sum(fc.gemm_bytes(*p) for p in probs)
     achieved = tot / (gemm_us.sum() * 1e-6) / 1e9
@@ -775,408 +1518,146 @@ def run_gpu_rowwise(args, rank, world):
                     "e4m3 planes, per shape from the measured table",
             "int8block": "gemm_i8_kernel (block promotion per K slab, mma.sync m16n8k32 s8) or "
                          "gemm_mx_kernel on two e4m3 planes, per shape from the measured table"}[code]
+    cpu = None
+    if not args.no_cpu_baseline:
+        est, sample_s, desc = rowwise_oracle_sample(code)
+        cpu = {"value": step_total / est / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "extrapolated": True, "sample": desc + f" (sample took {sample_s:.1f} s)"}
     line = {
-        "metric": METRIC, "value": round(step_total / step_s / 1e9, 2), "unit": "GB/s",
+        "metric": METRIC, "value": step_total * passes / step_s / 1e9, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": code, "data": "synthetic",
         "config": {"workload": ROWWISE_WORKLOAD.format(
                        code=code, aq=ROWWISE_QUANT[code][0], wq=ROWWISE_QUANT[code][1],
                        api=ROWWISE_QUANT[code][2]),
-                   "problems_per_step": len(probs),
+                   "problems_per_pass": len(probs),
                    "l2": "inputs larger than L2: each GEMM reads its own weight copy",
-                   "timing": "graph: step = fp8bq_linear_rowwise per problem, CUDA events on "
-                             "the launching stream; per-GEMM durations from an instrumented "
-                             "pass (quant and GEMM as separate calls)",
                    "parallelism": "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+        "passes_per_step": passes,
+        "timing": "graph: a pass = one linear call per problem; a step = passes_per_step "
+                  "passes; per-GEMM durations from an instrumented pass",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": None, "kernel": kern,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 2 * len(probs),
-        "clocks": clk, "per_shape": per, "prefill_gemm": prefill,
-        "wall_timed_s": round(t_wall, 3), "gemm_source_sha256_16": gemm_source_hash(),
+        "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": args.steps * passes * 2 * len(probs), "clocks": clk, "per_shape": per,
+        "prefill_gemm": prefill, "wall_timed_s": wall, "gemm_source_sha256_16": gemm_source_hash(),
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(_round(line)), flush=True)
     return 0
 
 
-# ------------------------------------------------------------- GPU arm
+# ------------------------------------------------------------- reference arm
 
-def run_gpu(args, rank, world):
-    import torch
-    import torch.distributed as dist
-
-    from block_scaled_fp8_group_gb300 import build
-    build.build()
-    from block_scaled_fp8_group_gb300 import fp8bq
-
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    probs = problems()
-    stream = torch.cuda.current_stream()
-
-    # ---- setup (untimed): weights quantised once, one copy per M point
-    w_q, w_s = {}, {}
-    for (N, K) in synth.DECODE_NK:
-        wb = synth.weight_bf16(N, K)
-        wd = torch.from_numpy(wb.view(np.int16)).view(torch.bfloat16).to(dev)
-        q, s = fp8bq.fp8bq_quant_weight(wd, "ue8m0")
-        del wd
-        for M in synth.DECODE_M:
-            w_q[(M, N, K)] = q.clone()
-        w_s[(N, K)] = s
-        del q
-    torch.cuda.synchronize()
-    xs, aqs, ass, outs = {}, {}, {}, {}
-    for (M, N, K) in probs:
-        xb = synth.act_decode(M, K)
-        xs[(M, N, K)] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
-        aqs[(M, N, K)], ass[(M, N, K)] = (
-            torch.empty((M, K), dtype=torch.uint8, device=dev),
-            torch.empty(fp8bq.act_scale_shape(M, K, 128, "ue8m0")[0], dtype=torch.int32,
-                        device=dev))
-        outs[(M, N, K)] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws_bytes = max(fp8bq.fp8bq_linear_workspace_bytes(M, N, K, "ue8m0", torch.bfloat16)
-                   for (M, N, K) in probs)
-    ws = torch.zeros(ws_bytes + (1 << 20), dtype=torch.uint8, device=dev)
-    variants = {p: fp8bq.fp8bq_select_variant(*p, "ue8m0", torch.bfloat16) for p in probs}
-
-    def step_linear():
-        # the timed step: one fp8bq_linear call (quant + GEMM, PDL) per problem
-        for p in probs:
-            M, N, K = p
-            fp8bq.fp8bq_linear(xs[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
-                               out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
-
-    def step_split(ev_pairs):
-        # the instrumented step: quant and GEMM as separate calls, with timing
-        # events around every GEMM launch
-        for i, p in enumerate(probs):
-            M, N, K = p
-            fp8bq.fp8bq_quant_act(xs[p], "ue8m0", q=aqs[p], s=ass[p])
-            ev_pairs[i][0].record()
-            fp8bq.fp8bq_gemm(aqs[p], ass[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
-                             out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
-            ev_pairs[i][1].record()
-
-    def step_gemms():
-        # the 33 GEMMs alone, launched back to back as in the step (PDL
-        # between them), on the codes the instrumented pass wrote
-        for p in probs:
-            M, N, K = p
-            fp8bq.fp8bq_gemm(aqs[p], ass[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
-                             out_dtype=torch.bfloat16, out=outs[p], workspace=ws)
-
-    # ---- timing instruments: CUDA graphs with external timing events, else eager
-    mode = args.mode
-    ext_ok = True
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        ext_ok = False
-    if mode == "graph" and not ext_ok:
-        mode = "eager"
-    mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if mode == "graph" else \
-        (lambda: torch.cuda.Event(enable_timing=True))
-    ev_pairs = [(mk(), mk()) for _ in probs]
-    ev_start, ev_end = mk(), mk()
-    ev2_start, ev2_end = mk(), mk()
-    ev3_start, ev3_end = mk(), mk()
-
-    # first launches: load the table, set kernel attributes
-    step_linear()
-    step_split(ev_pairs)
-    torch.cuda.synchronize()
-    graphs = None
-    if mode == "graph":
-        g_lin, g_split, g_gemm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g_lin, stream=side):
-                ev_start.record()
-                step_linear()
-                ev_end.record()
-            with torch.cuda.graph(g_split, stream=side):
-                ev2_start.record()
-                step_split(ev_pairs)
-                ev2_end.record()
-            with torch.cuda.graph(g_gemm, stream=side):
-                ev3_start.record()
-                step_gemms()
-                ev3_end.record()
-        torch.cuda.synchronize()
-        graphs = (g_lin, g_split, g_gemm)
-
-    def run_timed():
-        if graphs is not None:
-            graphs[0].replay()
-        else:
-            ev_start.record()
-            step_linear()
-            ev_end.record()
-
-    def run_instr():
-        if graphs is not None:
-            graphs[1].replay()
-        else:
-            ev2_start.record()
-            step_split(ev_pairs)
-            ev2_end.record()
-
-    def run_gemms():
-        if graphs is not None:
-            graphs[2].replay()
-        else:
-            ev3_start.record()
-            step_gemms()
-            ev3_end.record()
-
-    for _ in range(args.warmup):
-        run_timed()
-        run_instr()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    if rank == 0:
-        clocks.start()
-    step_ms = []
-    t_wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        run_timed()
-        ev_end.synchronize()
-        step_ms.append(ev_start.elapsed_time(ev_end))
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop() if rank == 0 else None
-    step_s = float(np.mean(step_ms)) / 1e3
-    if world > 1:
-        step_s = max_over_ranks(step_s, dev)
-    # instrumented pass (same problems, same cold weights): per-GEMM durations
-    n_instr = max(1, min(args.steps, args.instr_steps))
-    gemm_ms, split_ms = np.zeros(len(probs)), []
-    for _ in range(n_instr):
-        run_instr()
-        ev2_end.synchronize()
-        split_ms.append(ev2_start.elapsed_time(ev2_end))
-        gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_pairs])
-    gemm_us = gemm_ms / n_instr * 1e3
-    # the GEMM launches as the step runs them: back to back, PDL between them
-    chain_ms = []
-    for _ in range(n_instr):
-        run_gemms()
-        ev3_end.synchronize()
-        chain_ms.append(ev3_start.elapsed_time(ev3_end))
-    chain_s = float(np.mean(chain_ms)) / 1e3
-    assert fp8bq.fp8bq_device_status() == 0
-    launches = args.steps * 2 * len(probs)
-
-    # ---- end to end through the public fp8bq_linear call with host buffers
-    e2e = None
-    if not args.no_e2e:
-        # all inputs of a step in one pinned host buffer and all outputs in
-        # another, one slice per problem (16-byte aligned: M*K and M*N are
-        # multiples of 64 elements)
-        x_off, o_off, xo, oo = {}, {}, 0, 0
-        for (M, N, K) in probs:
-            x_off[(M, N, K)], o_off[(M, N, K)] = xo, oo
-            xo += M * K
-            oo += M * N
-        hx_all = torch.empty(xo, dtype=torch.bfloat16).pin_memory()
-        hout_all = torch.empty(oo, dtype=torch.bfloat16).pin_memory()
-        for (M, N, K) in probs:
-            hx_all[x_off[(M, N, K)]:x_off[(M, N, K)] + M * K].copy_(xs[(M, N, K)].reshape(-1).cpu())
-        xd_all = torch.empty(xo, dtype=torch.bfloat16, device=dev)
-        od_all = torch.empty(oo, dtype=torch.bfloat16, device=dev)
-        xd = {p: xd_all[x_off[p]:x_off[p] + p[0] * p[2]].view(p[0], p[2]) for p in probs}
-        od = {p: od_all[o_off[p]:o_off[p] + p[0] * p[1]].view(p[0], p[1]) for p in probs}
-        h2d, d2h = 2 * xo, 2 * oo
-
-        hx = {p: hx_all[x_off[p]:x_off[p] + p[0] * p[2]].view(p[0], p[2]) for p in probs}
-        ho = {p: hout_all[o_off[p]:o_off[p] + p[0] * p[1]].view(p[0], p[1]) for p in probs}
-        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-
-        wait_every = 6  # measured on GB300: 1 -> 3152, 6 -> 3379, 33 -> 2886 GB/s
-
-        def e2e_step():
-            # copies overlap the compute: every problem's input goes up on
-            # one side stream ahead of its linear layer, and its output comes
-            # back on another while the next problems run.  The compute
-            # stream waits once per `wait_every` problems (for the inputs of
-            # the next ones): each cross-stream wait cuts the chain of
-            # programmatic launches between consecutive layers
-            cur = torch.cuda.current_stream()
-            h2d_s.wait_stream(cur)
-            d2h_s.wait_stream(cur)
-            ready = []
-            with torch.cuda.stream(h2d_s):
-                for p in probs:
-                    xd[p].copy_(hx[p], non_blocking=True)
-                    e = torch.cuda.Event()
-                    e.record(h2d_s)
-                    ready.append(e)
-            for i, p in enumerate(probs):
-                M, N, K = p
-                if i % wait_every == 0:
-                    cur.wait_event(ready[min(i + wait_every, len(probs)) - 1])
-                fp8bq.fp8bq_linear(xd[p], w_q[p], w_s[(N, K)], fmt="ue8m0",
-                                   out_dtype=torch.bfloat16, out=od[p], workspace=ws)
-                done = torch.cuda.Event()
-                done.record(cur)
-                d2h_s.wait_event(done)
-                with torch.cuda.stream(d2h_s):
-                    ho[p].copy_(od[p], non_blocking=True)
-            cur.wait_stream(h2d_s)
-            cur.wait_stream(d2h_s)
-
-        e2e_step()
-        torch.cuda.synchronize()
-        g_e2e = None
-        if mode == "graph":
-            g_e2e = torch.cuda.CUDAGraph()
-            side2 = torch.cuda.Stream()
-            side2.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(side2):
-                with torch.cuda.graph(g_e2e, stream=side2):
-                    e2e_step()
-            torch.cuda.synchronize()
-        run_e2e = g_e2e.replay if g_e2e is not None else e2e_step
-        for _ in range(args.warmup):
-            run_e2e()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, args.e2e_steps))
-        a.record()
-        for _ in range(n_e2e):
-            run_e2e()
-        b.record()
-        b.synchronize()
-        e2e_s = a.elapsed_time(b) / 1e3 / n_e2e
-        if world > 1:
-            e2e_s = max_over_ranks(e2e_s, dev)
-        e2e = {"value": job_value(total_step_bytes(), world, e2e_s), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
-               "api": f"fp8bq_linear (quant + GEMM, PDL) per problem ({mode}); every step copies "
-                      "each problem's input from pinned host memory on a side stream ahead of its "
-                      "linear layer (the compute waits once per 6 problems) and its output back on "
-                      "another side stream after it, overlapping the compute of the other problems"}
-
+def run_reference(args, rank, world):
+    """The oracle (the CPU reference of this path) on the host cores, on the
+    GPU arm's workload, config, metric and unit: every step times a bounded
+    sample of the workload and extrapolates it to the whole step."""
     if rank != 0:
         return 0
-
-    peaks = load_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_TO_BF16_NOMINAL
-    per = []
-    for i, (M, N, K) in enumerate(probs):
-        t = gemm_us[i] * 1e-6
-        b = gemm_bytes(M, N, K)
-        fl = gemm_flops(M, N, K)
-        t_roof = max(b / (peaks["hbm_gbs"] * 1e9), fl / (fp8_peak * 1e12))
-        per.append({"m": M, "n": N, "k": K, "us": round(gemm_us[i], 3),
-                    "tflops": round(fl / t / 1e12, 2),
-                    "gbs_pages": round(pages_gbs_bytes(M, N, K) / t / 1e9, 1),
-                    "gbs_alg": round(b / t / 1e9, 1), "roofline_frac": round(t_roof / t, 3),
-                    "variant": variant_name(variants[(M, N, K)]),
-                    "h100_deepgemm_us": H100_DEEPGEMM_US.get((M, N, K))})
-    n_mx = sum(1 for p in probs if variants[p]["mma_scale"])
-    tot_gemm_bytes = sum(gemm_bytes(*p) for p in probs)
-    achieved = tot_gemm_bytes / chain_s / 1e9
-    achieved_iso = tot_gemm_bytes / (gemm_us.sum() * 1e-6) / 1e9
-    traffic = profile_traffic()
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": traffic,
-            "method": "achieved = the 33 GEMMs' algorithmic bytes / the average time of the 33 "
-                      "GEMM launches run back to back as the step launches them (PDL between "
-                      "them; CUDA events around the chain on the launching stream); "
-                      "achieved_isolated = the same bytes / the sum of the GEMMs timed one by "
-                      "one between events (each pays its own launch, ramp and tail)",
-            "achieved_isolated": round(achieved_iso, 1),
-            "frac_isolated": round(achieved_iso / peaks["hbm_gbs"], 4),
-            "gemm_chain_ms": round(chain_s * 1e3, 4),
-            "kernel": f"block-scaled FP8 GEMM, decode sweep: {len(probs)} launches per step "
-                      f"({n_mx} gemm_mx_kernel, {len(probs) - n_mx} gemm_kernel, as the "
-                      "table selects)",
-            "algorithmic_bytes_per_launch_avg": tot_gemm_bytes / len(probs),
-            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        est, sample_s, desc = oracle_time_sample(rows_per_shape=args.oracle_rows)
-        cpu = {"value": total_step_bytes() / est / 1e9, "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "sample": desc + f" (sample took {sample_s:.1f} s)"}
-        est_all, nthr, desc_all = oracle_time_all_cores()
-        cpu["all_cores"] = {"value": total_step_bytes() / est_all / 1e9, "unit": "GB/s",
-                            "cores": nthr, "sample": desc_all}
-    value = job_value(total_step_bytes(), world, step_s)
+    w = args.workload
+    if w in ("grid", "decode", "prefill", "small"):
+        sweep = make_sweep(w)
+        host_w = {(N, K): sweep.weight(N, K) for (N, K) in sorted({(p.N, p.K)
+                                                                   for p in sweep.problems})}
+        qws = oracle_weights(sweep, host_w)
+        one = lambda: oracle_sample(sweep, qws, rows=1)  # noqa: E731
+        units = sum(sweep.units(p) for p in sweep.problems)
+        unit, scale, config = sweep.unit, sweep.unit_scale, sweep.config(world)
+    elif w == "quant":
+        one = lambda: quant_oracle_sample(16)  # noqa: E731
+        units = sum(quant_bytes(*p) for p in quant_problems())
+        unit, scale, config = "GB/s", 1e9, quant_config(world)
+    elif w == "moe":
+        one = moe_oracle_sample
+        units = sum(moe_bytes(p[1], p[2], p[3], True) for p in moe_problems())
+        unit, scale = "GB/s", 1e9
+        config = {"workload": MOE_WORKLOAD, "problems_per_pass": len(moe_problems()),
+                  "l2": "inputs larger than L2: every problem reads its own weight copy "
+                        "(0.47-0.94 GB each)", "parallelism": "single GPU"}
+    else:
+        one = lambda: rowwise_oracle_sample(args.code)  # noqa: E731
+        probs = rowwise_problems()
+        fc_bytes = block_int8_step_bytes if args.code == "int8block" else rowwise_step_bytes
+        units = sum(fc_bytes(*p) for p in probs)
+        unit, scale = "GB/s", 1e9
+        config = {"workload": ROWWISE_WORKLOAD.format(
+                      code=args.code, aq=ROWWISE_QUANT[args.code][0],
+                      wq=ROWWISE_QUANT[args.code][1], api=ROWWISE_QUANT[args.code][2]),
+                  "problems_per_pass": len(probs),
+                  "l2": "inputs larger than L2: each GEMM reads its own weight copy",
+                  "parallelism": "single GPU"}
+    for _ in range(args.warmup):
+        one()
+    ests, samples = [], []
+    desc = ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        est, sample_s, desc = one()
+        ests.append(est)
+        samples.append(sample_s)
+    wall = time.perf_counter() - t0
+    est = float(np.mean(ests))
+    value = units / est / scale
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "problems_per_step": len(probs),
-                   "l2": "inputs larger than L2: each GEMM reads its own weight copy "
-                         "(3.2 GB of weights per step)",
-                   "timing": f"{mode}: step = fp8bq_linear per problem (PDL between "
-                             "kernels), CUDA events on the launching stream around each step; "
-                             "per-GEMM durations (per_shape) from an instrumented pass of the "
-                             "same step (quant and GEMM as separate calls, events around every "
-                             "GEMM); the roofline from the same GEMMs launched back to back",
-                   "instrumented_step_ms": round(float(np.mean(split_ms)), 4),
-                   "instrumented_steps": n_instr,
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clk, "per_shape": per, "wall_timed_s": round(t_wall, 3),
-        "gemm_source_sha256_16": gemm_source_hash(),
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3,
+        "extrapolated": True, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": config, "passes_per_step": 1,
+        "timing": "every step times the oracle on a bounded sample of the workload (one "
+                  "activation row per (N,K), single thread) and extrapolates linearly in M to "
+                  "one pass; ms_per_step is that extrapolation, wall_s the time the samples "
+                  "took",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "sample_s_per_step": float(np.mean(samples)), "wall_s": wall,
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(_round(line)), flush=True)
     return 0
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("fp8bq", "reference"), default="fp8bq")
-    ap.add_argument("--mode", choices=("graph", "eager"), default="graph")
-    ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--instr-steps", type=int, default=200)
-    ap.add_argument("--oracle-rows", type=int, default=4)
-    ap.add_argument("--steps-ref", type=int, default=None)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("decode", "moe", "rowwise"), default="decode")
+    ap.add_argument("--workload", choices=("grid", "decode", "prefill", "small", "quant", "moe",
+                                           "rowwise"), default="grid")
     ap.add_argument("--code", choices=("e4m3", "int8", "int8block"), default="e4m3",
                     help="rowwise workload: FP8_Dynamic (e4m3), W8A8_INT8 (int8) or block "
                          "INT8 (int8block) codes")
+    ap.add_argument("--min-timed-s", type=float, default=20.0,
+                    help="passes per step are chosen so the K timed steps last at least this")
+    ap.add_argument("--instr-passes", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--oracle-rows", type=int, default=24)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    if args.steps_ref is None:
-        args.steps_ref = max(1, min(args.steps, 10))
     if args.impl == "reference":
         return run_reference(args, rank, world)
-    if args.workload == "moe":
+    if args.workload in ("moe", "rowwise"):
         if world > 1 and rank != 0:
             return 0
-        return run_gpu_moe(args, rank, world)
-    if args.workload == "rowwise":
-        if world > 1 and rank != 0:
-            return 0
-        return run_gpu_rowwise(args, rank, world)
+        return (run_gpu_moe if args.workload == "moe" else run_gpu_rowwise)(args, rank, 1)
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    rc = run_gpu(args, rank, world)
+    if args.workload == "quant":
+        rc = run_quant(args, rank, world)
+    else:
+        rc = run_sweep(args, rank, world, make_sweep(args.workload))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -634,7 +634,7 @@ size_t fp8bq_variant_workspace_bytes(int64_t M, int64_t N, int64_t K, const fp8b
     if (!v || check_gemm_args(M, N, K, FP8BQ_SCALE_FP32, FP8BQ_BF16) != FP8BQ_OK) return 0;
     if (M == 0 || N == 0) return 0;
     GemmPlan plan;
-    if (!make_gemm_plan(M, N, K, *v, 152, &plan)) return 0;
+    if (!make_gemm_plan(M, N, K, *v, host_sms(), &plan)) return 0;
     return plan.ws_bytes;
 }
 
@@ -794,7 +794,7 @@ size_t fp8bq_grouped_variant_workspace_bytes(int64_t E, int64_t M_max, int64_t N
         return 0;
     if (M_max == 0 || N == 0) return 0;
     GemmPlan plan;
-    if (!make_gemm_plan(M_max, N, K, *v, 152, &plan, E)) return 0;
+    if (!make_gemm_plan(M_max, N, K, *v, host_sms(), &plan, E)) return 0;
     return plan.ws_bytes;
 }
 
@@ -873,6 +873,7 @@ fp8bq_status fp8bq_grouped_linear(const void* x, fp8bq_dtype x_dtype, int64_t E,
     if (st != FP8BQ_OK) return st;
     if (group != kGroup || block_n != kGroup || block_k != kGroup) return FP8BQ_ERR_UNSUPPORTED;
     if (x_dtype != FP8BQ_BF16 && x_dtype != FP8BQ_FP16) return FP8BQ_ERR_UNSUPPORTED;
+    if (E > 65535) return FP8BQ_ERR_UNSUPPORTED;  // the quant grid's expert dimension
     if (M_max == 0 || N == 0) return FP8BQ_OK;
     if (!x || !counts) return FP8BQ_ERR_INVALID_ARG;
     st = check_gemm_ptrs(x, x, w_q, w_s, out);

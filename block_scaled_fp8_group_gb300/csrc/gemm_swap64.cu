@@ -1,0 +1,10 @@
+// gemm_swap64.cu -- instantiates the GEMM launchers of: launch_bn<true, 64>.
+#include "gemm_impl.cuh"
+
+namespace fp8bq {
+
+cudaError_t launch_gemm_swap64(const GemmPlan& p, const GemmLaunch& g, cudaStream_t stream) {
+    return launch_bn<true, 64>(p, g, stream);
+}
+
+}  // namespace fp8bq

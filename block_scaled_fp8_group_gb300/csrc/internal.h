@@ -36,9 +36,10 @@ struct QuantActArgs {
     int ue8m0;
     int fp16;    // input is fp16 (else bf16)
     int int8 = 0;  // int8 codes, s = max(amax, eps) / 127 (fp32 scales; block INT8)
-    // Grouped rows (optional): row r belongs to expert r / m_max and is
-    // quantised only if r % m_max < counts[expert] (device array, clamped to
-    // [0, m_max]); other rows are neither read nor written.
+    // Grouped rows (optional): M = E * m_max rows, expert e owning rows
+    // [e * m_max, (e + 1) * m_max), of which the first counts[e] (device
+    // array, clamped to [0, m_max]) are quantised; other rows are neither
+    // read nor written.  The launch gives every expert its own grid layer.
     const int* counts = nullptr;
     int64_t m_max = 0;
 };

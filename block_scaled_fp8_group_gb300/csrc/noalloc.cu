@@ -7,9 +7,12 @@
 // allocation could block or synchronise the device, or a plug-in that only
 // receives tensors and a stream.  fp8bq_gemm needs a caller-provided
 // workspace when the chosen kernel splits K; this entry point instead uses a
-// scratch array that lives in the library itself (allocated once, when the
-// library is loaded, on every GPU that loads it) and keeps it until the
-// process exits.
+// scratch array that lives in the library itself.  The CUDA runtime loads
+// the array's module on a device lazily, at the first lookup of its address
+// (the first call of this entry point on that device): that is when the
+// device's copy is reserved, and it is kept until the process exits.  That
+// first call may synchronise the device, so it belongs at start-up, before
+// any stream capture and outside any no-allocation region.
 #include <mutex>
 
 #include "internal.h"

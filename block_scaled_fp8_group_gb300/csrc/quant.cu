@@ -24,15 +24,17 @@ namespace {
 // and the 4 UE8M0 exponents of the warp form exactly one packed u32 word, so
 // packing needs no traffic between warps.
 //
-// 2D grid without runtime division: blockIdx.x picks kRows rows (one per
-// warp), blockIdx.y picks the 4-group column; every index below is a product
-// or sum of those with compile-time constants.
+// Grid without runtime division: blockIdx.x picks kRows rows (one per warp),
+// blockIdx.y the 4-group column and, for grouped rows, blockIdx.z the expert
+// (rows then counted within it); every index below is a product or sum of
+// those with compile-time constants or kernel arguments.
 constexpr int kQuantRows = 8;  // warps per CTA = rows per CTA
 
 template <bool kFp16, bool kGrouped>
 __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantActArgs a) {
     const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantRows + (threadIdx.x >> 5);
+    const int64_t wrow = static_cast<int64_t>(blockIdx.x) * kQuantRows + (threadIdx.x >> 5);
+    const int64_t row = kGrouped ? static_cast<int64_t>(blockIdx.z) * a.m_max + wrow : wrow;
     const int quad = blockIdx.y;             // 4-group column index
     const int g = quad * 4 + (lane >> 3);    // this lane's group
     const bool active = row < a.M && g < a.G;
@@ -42,11 +44,11 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
     pdl_wait_prior_grid();
     pdl_launch_dependents();
     if (row >= a.Mp) return;
-    if (kGrouped && row < a.M) {
+    if (kGrouped) {
         // grouped rows: skip the rows past the expert's count (warp-uniform)
-        const int64_t e = row / a.m_max;
-        const int c = __ldg(a.counts + e);
-        if (row - e * a.m_max >= (c < 0 ? 0 : c)) return;
+        if (wrow >= a.m_max) return;
+        const int c = __ldg(a.counts + blockIdx.z);
+        if (wrow >= (c < 0 ? 0 : c)) return;
     }
 
     const int64_t off = row * a.K + static_cast<int64_t>(quad) * 512 + lane * 16;
@@ -86,9 +88,24 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
 #pragma unroll
             for (int i = 0; i < 8; ++i) c[i] = cvt2_e4m3(f[2 * i] * r, f[2 * i + 1] * r);
         } else {
+            // fp32 scales: the code of fp32(x / s), computed as y = x * r with
+            // r = fp32(1 / s).  Two roundings of relative size <= 2^-24 put y
+            // within 2 fp32 ulps of x / s, so y and fp32(x / s) give the same
+            // e4m3 code unless a rounding boundary of e4m3 (the midpoint of
+            // two adjacent codes) lies that close to y.  For |y| >= 2^-6
+            // (normal e4m3: 3 mantissa bits kept) such a midpoint has the 20
+            // mantissa bits e4m3 drops equal to 0x80000; y within 8 ulps of
+            // one, or in the e4m3 subnormal range, takes the exact quotient.
+            const float r = __fdiv_rn(1.0f, s);
+            float y[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                c[i] = cvt2_e4m3(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+            for (int i = 0; i < 16; ++i) {
+                y[i] = f[i] * r;
+                const uint32_t d = (__float_as_uint(y[i]) & 0xFFFFFu) - 0x80000u + 8u;
+                if (fabsf(y[i]) < 0.015625f || d <= 16u) y[i] = __fdiv_rn(f[i], s);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] = cvt2_e4m3(y[2 * i], y[2 * i + 1]);
         }
         uint4 out;
         out.x = c[0] | (c[1] << 16);
@@ -357,8 +374,16 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 cudaError_t launch_quant_act(const QuantActArgs& a, cudaStream_t stream) {
     const int quads = (a.G + 3) / 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((a.Mp + kQuantRows - 1) / kQuantRows),
-                       static_cast<unsigned>(quads));
+    if (a.counts != nullptr) {
+        // one grid layer per expert (M = E * m_max rows, m_max a multiple of 4)
+        const int64_t E = a.m_max > 0 ? a.M / a.m_max : 0;
+        if (E <= 0 || E > 65535) return cudaErrorInvalidConfiguration;
+        cfg.gridDim = dim3(static_cast<unsigned>((a.m_max + kQuantRows - 1) / kQuantRows),
+                           static_cast<unsigned>(quads), static_cast<unsigned>(E));
+    } else {
+        cfg.gridDim = dim3(static_cast<unsigned>((a.Mp + kQuantRows - 1) / kQuantRows),
+                           static_cast<unsigned>(quads));
+    }
     cfg.blockDim = dim3(kQuantRows * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -54,6 +54,50 @@ def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
+def _row_blocks(shape, block_rows):
+    rows = shape[0]
+    return [(b, slice(r, min(rows, r + block_rows)))
+            for b, r in enumerate(range(0, rows, block_rows))]
+
+
+def _par_map(fn, items, threads=None):
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    with ThreadPoolExecutor(max_workers=threads or min(16, os.cpu_count() or 1)) as ex:
+        return list(ex.map(fn, items))
+
+
+def normal_blocked(shape, seed: int, std: float = 1.0, block_rows: int = 1024) -> np.ndarray:
+    """N(0, std^2) fp32 drawn in blocks of `block_rows` rows, block b from its
+    own PCG64 stream seeded with SeedSequence([seed, b]), filled by parallel
+    threads.  A different (but equally seeded and reproducible) recipe from
+    `normal`, for the benchmark's multi-GB inputs; the values of a row depend
+    only on (seed, row), not on the number of rows drawn."""
+    x = np.empty(shape, dtype=np.float32)
+
+    def fill(item):
+        b, rows = item
+        np.random.default_rng([seed, b]).standard_normal(size=x[rows].shape, dtype=np.float32,
+                                                         out=x[rows])
+        if std != 1.0:
+            x[rows] *= np.float32(std)
+
+    _par_map(fill, _row_blocks(shape, block_rows))
+    return x
+
+
+def f32_to_bf16_bits_par(x: np.ndarray, block_rows: int = 1024) -> np.ndarray:
+    """`f32_to_bf16_bits` over row blocks in parallel threads (same bits)."""
+    out = np.empty(x.shape, dtype=np.uint16)
+
+    def conv(item):
+        _, rows = item
+        out[rows] = f32_to_bf16_bits(x[rows])
+
+    _par_map(conv, _row_blocks(x.shape, block_rows))
+    return out
+
+
 def normal(shape, seed: int, std: float = 1.0) -> np.ndarray:
     x = _rng(seed).standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
@@ -129,6 +173,53 @@ def weight_f32(N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
 
 def weight_bf16(N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
     return f32_to_bf16_bits(weight_f32(N, K, seed))
+
+
+# Benchmark-sized inputs (row-blocked parallel draws, see normal_blocked).
+
+def weight_bf16_blocked(N: int, K: int, seed: int = SEED_WEIGHT) -> np.ndarray:
+    return f32_to_bf16_bits_par(normal_blocked((N, K), seed, std=0.02))
+
+
+def act_full_grid_blocked(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal_blocked((M, K), seed)
+    scale_channels(x, outlier_channels(K, 0.005, SEED_STRUCT), 50.0)
+    return f32_to_bf16_bits_par(x)
+
+
+def act_decode_blocked(M: int, K: int, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal_blocked((M, K), seed)
+    scale_channels(x, outlier_channels(K, 0.01, SEED_STRUCT), 30.0)
+    return f32_to_bf16_bits_par(x)
+
+
+def act_prefill_blocked(M: int, K: int, seed: int = SEED_ACT, nu: float = 3.0,
+                        block_rows: int = 1024) -> np.ndarray:
+    """Student-t(nu) rows drawn per row block (stream SeedSequence([seed, b])),
+    scaled to unit empirical RMS over the whole matrix (fp64)."""
+    t = np.empty((M, K), dtype=np.float64)
+
+    def fill(item):
+        b, rows = item
+        t[rows] = np.random.default_rng([seed, b]).standard_t(nu, size=t[rows].shape)
+
+    blocks = _row_blocks((M, K), block_rows)
+    _par_map(fill, blocks)
+    rms = np.sqrt(np.mean(np.square(t)))
+    x = np.empty((M, K), dtype=np.float32)
+
+    def norm(item):
+        _, rows = item
+        x[rows] = t[rows] / rms
+
+    _par_map(norm, blocks)
+    return f32_to_bf16_bits_par(x)
+
+
+def act_quant_blocked(M: int, K: int, group: int = 128, seed: int = SEED_ACT) -> np.ndarray:
+    x = normal_blocked((M, K), seed)
+    group_spikes(x, group, SEED_STRUCT)
+    return f32_to_bf16_bits_par(x)
 
 
 # The pages' M grid ("vLLM 量化 Kernel 配置机制" §2) and the workload shape sets.

@@ -82,9 +82,9 @@ typedef struct {
     int32_t from_table; /* output of fp8bq_select_variant: 1 = measured table, 0 = default */
     int32_t mma_scale;  /* 0: each K slab's fp32 product is promoted by sa*sw on the CUDA
                          * cores; 1: the tensor core applies the scales (block-scaled MMA,
-                         * E8M0 factors in TMEM) and accumulates all slabs itself -- swap-AB
-                         * only, UE8M0 scales only, K a multiple of 512 (FP8BQ_ERR_UNSUPPORTED
-                         * otherwise) */
+                         * E8M0 factors in TMEM) and accumulates all slabs itself -- either
+                         * orientation (kinds 0 and 1; not kind 2), UE8M0 scales only, K a
+                         * multiple of 512 (FP8BQ_ERR_UNSUPPORTED otherwise) */
 } fp8bq_variant;
 
 /* ------------------------------------------------------------ size queries */
@@ -152,9 +152,13 @@ fp8bq_status fp8bq_quant_weight(const void* w, fp8bq_dtype w_dtype, int64_t N, i
 /* out[m,n] = sum_kb sa[m,kb] * sw[n/128,kb] * sum_{k in slab kb} a_q[m,k]*w_q[n,k]
  * ("vLLM DeepGEMM FP8 Block GEMM 基准测试" §4.2: fp8_gemm_nt, A [M,K] and W
  * [N,K] both K-major; the per-K-block scale multiply into the accumulator).
- * Each slab's FP8 products are summed by the tensor cores in fp32 and the
- * slab sum is promoted into an fp32 register accumulator; the result is
- * rounded to nearest even into out_dtype.
+ * Each slab's FP8 products are summed by the tensor cores in fp32.  With
+ * mma_scale = 0 (every fp32-scale shape, and the UE8M0 shapes the table
+ * picks so) the slab sum is promoted by sa*sw into an fp32 register
+ * accumulator; with mma_scale = 1 (UE8M0 only) the tensor core multiplies
+ * every 32-wide K block's products by the power-of-two factors as it
+ * accumulates, and all slabs build up in one fp32 TMEM accumulator.  The
+ * result is rounded to nearest even into out_dtype.
  * a_q: [M,K] e4m3 row-major, 16-byte aligned.
  * a_s: activation scales in the fp8bq_quant_act layout for `fmt`.
  * w_q: [N,K] e4m3 row-major, 16-byte aligned.  w_s: fp32 [ceil(N/128)][K/128].
@@ -227,7 +231,9 @@ fp8bq_status fp8bq_grouped_gemm_variant(int64_t E, int64_t M_max, int64_t N, int
  * counts[e] are not read.  The codes and scales go to the front of
  * `workspace` (fp8bq_grouped_linear_workspace_bytes; counter prefix, codes,
  * scales, split-K partials, as fp8bq_linear); their padding rows are not
- * written.  Other arguments and preconditions as fp8bq_grouped_gemm. */
+ * written.  E at most 65535 (FP8BQ_ERR_UNSUPPORTED otherwise: the quant
+ * kernel's grid has one layer per expert).  Other arguments and
+ * preconditions as fp8bq_grouped_gemm. */
 fp8bq_status fp8bq_grouped_linear(const void* x, fp8bq_dtype x_dtype, int64_t E, int64_t M_max,
                                   int64_t N, int64_t K, const int32_t* counts, const void* w_q,
                                   const float* w_s, int group, int block_n, int block_k,
@@ -266,14 +272,18 @@ fp8bq_status fp8bq_linear(const void* x, fp8bq_dtype x_dtype, int64_t M, int64_t
  * they cannot provide the split-K workspace fp8bq_gemm may need.  This entry
  * point takes the same arguments minus the workspace and allocates nothing:
  * no cudaMalloc, no cudaFree, no allocating library call.  Its scratch is one
- * array of 32 MiB (33554432 bytes) built into the library; every GPU that
- * loads the library holds it until the process exits.
+ * array of 32 MiB (33554432 bytes) built into the library; every GPU on which
+ * it is first used holds it from then until the process exits.
  *   - Problems whose chosen kernel needs more split-K scratch than 32 MiB are
  *     rejected with FP8BQ_ERR_WORKSPACE (nothing is launched); use fp8bq_gemm
  *     with a workspace for those.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current.  Under the CUDA
+ *     runtime's default lazy module loading, that lookup is also what loads
+ *     the array's module on the device: it reserves the 32 MiB there and may
+ *     synchronise the device.  So make that first call once at start-up,
+ *     outside any region where allocation or synchronisation is not allowed,
+ *     and before any stream capture.
  *   - All calls share the one array, and each call clears the counters at its
  *     start (cudaMemsetAsync on `stream`): calls that overlap on the GPU
  *     (different streams without ordering) race and give wrong results. */

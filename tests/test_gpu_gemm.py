@@ -198,29 +198,58 @@ def test_prefill_full_size_sampled(fp8bq, N, K, M):
         check_gemm(o.float().cpu().numpy()[rows], ref, out, f"prefill {M}x{N}x{K} {out}")
 
 
-@functools.lru_cache(maxsize=2)
-def _full_grid_weights(N, K):
-    wb = synth.weight_bf16(N, K)
-    qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
-    return wb, qw, sw
+_GRID_W = {}   # (N, K) -> (oracle codes, oracle scales, device codes, device scales)
+_GRID_REF = {}  # (N, K) -> {row: fp64 oracle row}
 
 
+def _grid_weights(fp8bq, N, K):
+    if (N, K) not in _GRID_W:
+        wb = synth.weight_bf16_blocked(N, K)
+        qw, sw = oracle.quant_weight(wb, oracle.BF16, 128, 128, True)
+        wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
+        _GRID_W[(N, K)] = (qw, sw, wq, ws)
+    return _GRID_W[(N, K)]
+
+
+@functools.lru_cache(maxsize=3)
+def _grid_act(K):
+    # rows of the blocked generator depend only on (seed, row): the M-row
+    # input of every grid point is the first M rows of this one
+    return synth.act_full_grid_blocked(max(synth.M_GRID), K)
+
+
+def _grid_ref(N, K, qw, sw, rows):
+    """Oracle rows of the full-grid problem (N, K), cached across M."""
+    cache = _GRID_REF.setdefault((N, K), {})
+    need = [r for r in rows if r not in cache]
+    if need:
+        xb = np.ascontiguousarray(_grid_act(K)[need])
+        qa, sa = oracle.quant_act(xb, oracle.BF16, 128, True)
+        ref = oracle_full(qa, sa, qw, sw, True)
+        for i, r in enumerate(need):
+            cache[r] = ref[i]
+    return np.stack([cache[r] for r in rows])
+
+
+@pytest.mark.parametrize("M", synth.M_GRID)
 @pytest.mark.parametrize("N,K", synth.FULL_NK)
-@pytest.mark.parametrize("M", [1, 24, 128, 512, 4096])
 def test_linear_full_grid(fp8bq, N, K, M):
-    """Fused quant + GEMM (UE8M0, fp16 and bf16 out) on the full-grid shapes;
-    the reference quantises with the oracle on the host.  Every element for
-    M <= 128, else all columns of 64 seeded rows plus the tile-boundary rows."""
-    wb, qw, sw = _full_grid_weights(N, K)
-    xb = synth.act_full_grid(M, K)
-    wq, ws = fp8bq.fp8bq_quant_weight(to_dev_bits(wb), "ue8m0")
+    """The full grid through the fused linear entry point (UE8M0, fp16 and
+    bf16 out), at every M point and (N,K), in the kernels the table selects
+    for each; the reference quantises with the oracle on the host.  Every
+    element for M <= 128, else all columns of 64 seeded rows plus the
+    tile-boundary rows."""
+    qw, sw, wq, ws = _grid_weights(fp8bq, N, K)
+    xb = _grid_act(K)[:M]
     rows = list(range(M)) if M <= 128 else sample_rows(M, 64)
-    qa, sa = oracle.quant_act(np.ascontiguousarray(xb[rows]), oracle.BF16, 128, True)
-    ref = oracle_full(qa, sa, qw, sw, True)
+    ref = _grid_ref(N, K, qw, sw, rows)
+    x = to_dev_bits(xb)
     for out in ("fp16", "bf16"):
-        o = fp8bq.fp8bq_linear(to_dev_bits(xb), wq, ws, fmt="ue8m0", out_dtype=TORCH_OUT[out])
+        o = fp8bq.fp8bq_linear(x, wq, ws, fmt="ue8m0", out_dtype=TORCH_OUT[out])
         torch.cuda.synchronize()
-        check_gemm(o.float().cpu().numpy()[rows], ref, out, f"linear {M}x{N}x{K} {out}")
+        sel = fp8bq.fp8bq_select_variant(M, N, K, "ue8m0", out)
+        check_gemm(o.float().cpu().numpy()[rows], ref, out,
+                   f"linear {M}x{N}x{K} {out} {sel}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (5, 384, 1024), (16, 1024, 2048),

@@ -225,3 +225,55 @@ def test_act_quant_every_bf16_value_per_scale(fp8bq, amax, ue):
     rq, rs = oracle.quant_act(xb, oracle.BF16, 128, ue)
     np.testing.assert_array_equal(q, rq)
     np.testing.assert_array_equal(s, rs.view(np.uint32))
+
+
+def _near_midpoint_pairs(n_scales=2000, seed=21, ulps=8):
+    """(A, x) bf16 pairs whose quotient fp32(x / fp32(A/448)) lies within
+    `ulps` fp32 ulps of an e4m3 rounding boundary (the midpoint of two
+    adjacent normal e4m3 values: the 20 mantissa bits e4m3 drops equal
+    0x80000), found by scanning every positive bf16 x <= A for seeded A."""
+    rng = np.random.default_rng(seed)
+    bits = np.arange(0x0080, 0x7F80, dtype=np.uint32).astype(np.uint16)  # positive normals
+    vals = synth.bf16_bits_to_f32(bits)
+    a_bits = rng.choice(bits[(vals >= 1e-3) & (vals <= 1e4)], size=n_scales, replace=False)
+    pairs = []
+    for ab in a_bits:
+        a = synth.bf16_bits_to_f32(np.array([ab], dtype=np.uint16))[0]
+        s = np.float32(a) / np.float32(448.0)  # IEEE fp32 division
+        xs = bits[vals <= a]
+        q = synth.bf16_bits_to_f32(xs) / s
+        u = q.view(np.uint32)
+        d = np.abs((u & np.uint32(0xFFFFF)).astype(np.int64) - 0x80000)
+        hit = (d <= ulps) & (q >= np.float32(2.0 ** -6))
+        pairs += [(int(ab), int(x)) for x in xs[hit]]
+    return pairs
+
+
+def test_act_quant_fp32_scale_near_rounding_boundaries(fp8bq):
+    """fp32 scales: inputs whose quotient x/s falls within a few fp32 ulps of
+    an e4m3 rounding boundary (including exact ties) -- where a product by
+    the reciprocal would round to another code than the IEEE quotient -- each
+    in a group whose amax A sets s, with both signs; codes and scales
+    bit-exact against the oracle."""
+    pairs = _near_midpoint_pairs()
+    assert len(pairs) > 500
+    by_a = {}
+    for ab, x in pairs:
+        by_a.setdefault(ab, []).append(x)
+    groups = []
+    for ab, xs in by_a.items():
+        for i in range(0, len(xs), 63):
+            g = np.zeros(128, dtype=np.uint16)
+            g[0] = ab
+            chunk = np.array(xs[i:i + 63], dtype=np.uint16)
+            g[1:1 + chunk.size] = chunk
+            g[64:64 + chunk.size] = chunk | np.uint16(0x8000)  # negatives
+            groups.append(g)
+    rows = (len(groups) + 7) // 8
+    xb = np.zeros((rows * 8, 128), dtype=np.uint16)
+    xb[:len(groups)] = np.stack(groups)
+    xb = xb.reshape(rows, 1024)
+    q, s = run_act(fp8bq, xb, False, False)
+    rq, rs = oracle.quant_act(xb, oracle.BF16, 128, False)
+    np.testing.assert_array_equal(q, rq)
+    np.testing.assert_array_equal(s, rs.view(np.uint32))

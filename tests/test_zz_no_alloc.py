@@ -54,7 +54,9 @@ def call_noalloc(fp8bq, aq, as_, wq, ws, fmt, out):
 def test_noalloc_matches_gemm_twice(fp8bq, M, N, K, fmt):
     aq, as_, wq, ws = problem(fp8bq, M, N, K, fmt)
     need = fp8bq.fp8bq_gemm_workspace_bytes(M, N, K, fmt, torch.bfloat16)
-    assert need <= SCRATCH_BYTES
+    # the selected kernel splits K, so the shared array is really used (and
+    # the second call finds it as the first one left it)
+    assert 0 < need <= SCRATCH_BYTES
     ref = fp8bq.fp8bq_gemm(aq, as_, wq, ws, fmt=fmt, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     ref64 = ref.float().cpu().numpy().astype(np.float64)
@@ -62,19 +64,34 @@ def test_noalloc_matches_gemm_twice(fp8bq, M, N, K, fmt):
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         assert call_noalloc(fp8bq, aq, as_, wq, ws, fmt, out) == 0
         torch.cuda.synchronize()
+        # the same kernel on the same inputs with a fixed-order split
+        # reduction: the result equals fp8bq_gemm's bit for bit (and so lies
+        # within the GEMM tolerance of the oracle that fp8bq_gemm's own tests
+        # check)
+        assert torch.equal(out, ref), f"noalloc call {call} differs from fp8bq_gemm"
         check_gemm(out.float().cpu().numpy(), ref64, "bf16", f"noalloc call {call}")
     assert fp8bq.fp8bq_device_status() == 0
 
 
+# Shapes whose table-selected kernel (a stream-K schedule over 256-wide tiles)
+# needs more than the 32 MiB array; the test uses the first that does.
+OVERSIZED = [(1536, 4096, 7168, "fp32"), (2048, 4096, 7168, "fp32"), (4096, 4096, 7168, "fp32"),
+             (1536, 4096, 7168, "ue8m0"), (1024, 7168, 18432, "fp32"),
+             (2048, 7168, 18432, "ue8m0"), (256, 4096, 7168, "fp32")]
+
+
 def test_noalloc_rejects_problems_beyond_the_scratch(fp8bq):
-    # a large split problem (default variant: stream-K over 256-wide tiles)
-    M, N, K = 256, 4096, 7168
-    need = fp8bq.fp8bq_gemm_workspace_bytes(M, N, K, "fp32", torch.bfloat16)
-    if need <= SCRATCH_BYTES:
-        pytest.skip("the selected kernel for this shape fits the scratch")
+    found = [(M, N, K, fmt) for (M, N, K, fmt) in OVERSIZED
+             if fp8bq.fp8bq_gemm_workspace_bytes(M, N, K, fmt, torch.bfloat16) > SCRATCH_BYTES]
+    assert found, "no candidate shape needs more than 32 MiB under the current table"
+    M, N, K, fmt = found[0]
     aq = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
-    as_ = torch.ones((K // 128, M), dtype=torch.float32, device="cuda")
+    shape, dt = fp8bq.act_scale_shape(M, K, 128, fmt)
+    as_ = torch.zeros(shape, dtype=dt, device="cuda")
     wq = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
     ws = torch.ones((N // 128, K // 128), dtype=torch.float32, device="cuda")
-    out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
-    assert call_noalloc(fp8bq, aq, as_, wq, ws, "fp32", out) == 5  # FP8BQ_ERR_WORKSPACE
+    out = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert call_noalloc(fp8bq, aq, as_, wq, ws, fmt, out) == 5  # FP8BQ_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    # rejected on the host before any launch: the output is untouched
+    assert bool((out == 7.0).all())
