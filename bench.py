@@ -617,7 +617,37 @@ def run_sweep(args, rank, world, sweep):
                                out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
 
     ev_i = _events(torch, len(probs), True)
+    ev_b = _events(torch, len(probs), True)
     ev_h = _events(torch, len(probs), True)
+    # every weight copy of each (N, K): back-to-back calls rotate over them
+    copies = {}
+    for k in keys:
+        copies.setdefault((k[1], k[2]), []).append(w_q[k])
+    R = args.b2b
+
+    def gemm_w(p, w):
+        fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w, w_s[(p.N, p.K)], fmt=fmt,
+                         out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
+
+    def step_b2b():
+        # the pages' per-shape method: R calls of the GEMM back to back (each
+        # launch overlaps the previous one's tail), events around the R calls;
+        # cold: the calls rotate over the problem's weight copies
+        for i, p in enumerate(probs):
+            cs = copies[(p.N, p.K)]
+            j0 = next(j for j, c in enumerate(cs) if c is w_q[p.key])
+            ev_b[i][0].record()
+            for j in range(R):
+                gemm_w(p, cs[(j0 + j) % len(cs)])
+            ev_b[i][1].record()
+
+    def step_hot():
+        # the same with one weight copy: operands in L2 as far as they fit
+        for i, p in enumerate(probs):
+            ev_h[i][0].record()
+            for j in range(R):
+                gemm_w(p, w_q[p.key])
+            ev_h[i][1].record()
 
     def step_instr():
         # quant and GEMM as separate calls, events around every GEMM launch
@@ -627,18 +657,6 @@ def run_sweep(args, rank, world, sweep):
             fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w_q[p.key], w_s[(p.N, p.K)], fmt=fmt,
                              out_dtype=out_of(p).dtype, out=out_of(p), workspace=ws)
             ev_i[i][1].record()
-
-    def step_hot():
-        # every GEMM twice in a row; the second one is timed (operands in L2
-        # as far as they fit)
-        for i, p in enumerate(probs):
-            g = lambda: fp8bq.fp8bq_gemm(aqs[p.key], ass[p.key], w_q[p.key],  # noqa: E731
-                                         w_s[(p.N, p.K)], fmt=fmt, out_dtype=out_of(p).dtype,
-                                         out=out_of(p), workspace=ws)
-            g()
-            ev_h[i][0].record()
-            g()
-            ev_h[i][1].record()
 
     chain_sets = {"all": list(range(len(probs)))}
     low = [i for i, p in enumerate(probs) if p.M <= 64]
@@ -660,6 +678,7 @@ def run_sweep(args, rank, world, sweep):
     g_step = capture(torch, step)
     g_instr = capture(torch, step_instr)
     g_hot = capture(torch, step_hot)
+    g_b2b = capture(torch, step_b2b)
     g_chain = {name: capture(torch, chain_fn(idx)) for name, idx in chain_sets.items()}
 
     step_s, passes, clk, wall = timed_steps(torch, g_step, args, world, dev, local, rank)
@@ -681,13 +700,17 @@ def run_sweep(args, rank, world, sweep):
         torch.cuda.synchronize()
         gemm_ms += np.array([a.elapsed_time(b) for a, b in ev_i])
         n_instr += 1
-    gemm_us = gemm_ms / n_instr * 1e3
-    hot_ms = np.zeros(len(probs))
+    event_us = gemm_ms / n_instr * 1e3
+    hot_ms, b2b_ms = np.zeros(len(probs)), np.zeros(len(probs))
     for _ in range(args.instr_passes):
+        g_b2b.replay()
+        torch.cuda.synchronize()
+        b2b_ms += np.array([a.elapsed_time(b) for a, b in ev_b])
         g_hot.replay()
         torch.cuda.synchronize()
         hot_ms += np.array([a.elapsed_time(b) for a, b in ev_h])
-    hot_us = hot_ms / args.instr_passes * 1e3
+    gemm_us = b2b_ms / (args.instr_passes * R) * 1e3  # per call, back to back, cold
+    hot_us = hot_ms / (args.instr_passes * R) * 1e3
     chain_s = {}
     for name, g in g_chain.items():
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -716,7 +739,8 @@ def run_sweep(args, rank, world, sweep):
         fl = gemm_flops(p.M, p.N, p.K)
         tr, bound = roof_time(byt, fl, peaks)
         per.append({"m": p.M, "n": p.N, "k": p.K, "out": p.odt, "copy": p.copy,
-                    "us": gemm_us[i], "us_hot": hot_us[i], "tflops": fl / t / 1e12,
+                    "us": gemm_us[i], "us_hot": hot_us[i], "us_event": event_us[i],
+                    "tflops": fl / t / 1e12,
                     "gbs_pages": pages_gbs_bytes(p.M, p.N, p.K) / t / 1e9,
                     "gbs_alg": byt / t / 1e9, "roofline_frac": tr / t, "bound": bound,
                     "variant": variant_name(variants[p.shape]),
@@ -787,10 +811,11 @@ def run_sweep(args, rank, world, sweep):
     roof.update({"kernel": kern, "launches_per_pass": len(idx),
                  "algorithmic_bytes_per_launch": alg_bytes_dom / len(idx),
                  "method": "achieved = the class's algorithmic flops (or bytes) over the sum "
-                           "of its launches' durations, each GEMM timed alone between CUDA "
-                           "events in a graph replay of the pass (cold: every GEMM reads its "
-                           "own weight copy); traffic = the ncu DRAM bytes per algorithmic "
-                           "byte of the committed summary x the class's bytes per launch"})
+                           "of its launches' durations, each GEMM timed per call over "
+                           f"{R} back-to-back calls in a graph that rotate over the "
+                           "problem's weight copies (cold), CUDA events on the launching "
+                           "stream; traffic = the ncu DRAM bytes per algorithmic byte of the "
+                           "committed summary x the class's bytes per launch"})
 
     cpu = None
     if cpu_job is not None:
@@ -815,8 +840,11 @@ def run_sweep(args, rank, world, sweep):
         "timing": "graph replays; a step = passes_per_step passes over the problems (the "
                   "smallest count that makes the timed region >= --min-timed-s); CUDA events "
                   "on the launching stream around every step; 3 untimed calibration passes "
-                  "before the warm-up; per_shape from an instrumented graph (quant and GEMM "
-                  "as separate calls, events around every GEMM launch)",
+                  "before the warm-up.  per_shape: us = per call over back-to-back calls of "
+                  "the GEMM rotating over the problem's weight copies (the pages' per-shape "
+                  "method: warm-up, then the mean of many calls), us_hot = the same on one "
+                  "weight copy, us_event = the GEMM alone between CUDA events after its quant "
+                  "(includes the launch gap a graph node pays)",
         "step_roofline_frac": t_roof_pass * passes / step_s,
         "roofline": roof, "targets": targets, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "clocks": clk,
@@ -841,7 +869,7 @@ def merge_copies(per):
     for key, es in groups.items():
         e = dict(es[0])
         e.pop("copy")
-        for f in ("us", "us_hot", "tflops", "gbs_pages", "gbs_alg", "roofline_frac"):
+        for f in ("us", "us_hot", "us_event", "tflops", "gbs_pages", "gbs_alg", "roofline_frac"):
             e[f] = float(np.mean([x[f] for x in es]))
         if len(es) > 1:
             e["copies"] = len(es)
@@ -949,9 +977,17 @@ def run_quant(args, rank, world):
         qs[(M, K, fmt)] = torch.empty((M, K), dtype=torch.uint8, device=dev)
         ss[(M, K, fmt)] = torch.empty(shape, dtype=dt, device=dev)
 
-    def call(p):
+    # extra input copies for the back-to-back per-shape measurement (cold:
+    # calls rotate over copies that together exceed the L2)
+    xcopies = {}
+    for (M, K) in xs:
+        n = min(8, max(2, -(-(400 << 20) // (2 * M * K))))
+        xcopies[(M, K)] = [xs[(M, K)]] + [xs[(M, K)].clone() for _ in range(n - 1)]
+    R = args.b2b
+
+    def call(p, x=None):
         M, K, fmt = p
-        fp8bq.fp8bq_quant_act(xs[(M, K)], fmt, q=qs[p], s=ss[p])
+        fp8bq.fp8bq_quant_act(xs[(M, K)] if x is None else x, fmt, q=qs[p], s=ss[p])
 
     def step():
         for p in probs:
@@ -966,35 +1002,49 @@ def run_quant(args, rank, world):
             call(p)
             ev_i[i][1].record()
 
+    ev_b = _events(torch, len(probs), True)
+
+    def step_b2b():
+        for i, p in enumerate(probs):
+            cs = xcopies[(p[0], p[1])]
+            ev_b[i][0].record()
+            for j in range(R):
+                call(p, cs[j % len(cs)])
+            ev_b[i][1].record()
+
     def step_hot():
         for i, p in enumerate(probs):
-            call(p)
             ev_h[i][0].record()
-            call(p)
+            for j in range(R):
+                call(p)
             ev_h[i][1].record()
 
     step()
     torch.cuda.synchronize()
-    g_step, g_instr, g_hot = capture(torch, step), capture(torch, step_instr), capture(torch,
-                                                                                       step_hot)
+    g_step, g_instr = capture(torch, step), capture(torch, step_instr)
+    g_hot, g_b2b = capture(torch, step_hot), capture(torch, step_b2b)
     step_s, passes, clk, wall = timed_steps(torch, g_step, args, world, dev, local, rank)
     cpu_job = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_job = Background(lambda: quant_oracle_sample(args.oracle_rows * 16))
-    us = np.zeros(len(probs))
+    ev_us = np.zeros(len(probs))
     n_instr = 0
     while n_instr < args.instr_passes or (cpu_job is not None and not cpu_job.done()):
         g_instr.replay()
         torch.cuda.synchronize()
-        us += np.array([a.elapsed_time(b) for a, b in ev_i]) * 1e3
+        ev_us += np.array([a.elapsed_time(b) for a, b in ev_i]) * 1e3
         n_instr += 1
-    us /= n_instr
-    hot = np.zeros(len(probs))
+    ev_us /= n_instr
+    us, hot = np.zeros(len(probs)), np.zeros(len(probs))
     for _ in range(args.instr_passes):
+        g_b2b.replay()
+        torch.cuda.synchronize()
+        us += np.array([a.elapsed_time(b) for a, b in ev_b]) * 1e3
         g_hot.replay()
         torch.cuda.synchronize()
         hot += np.array([a.elapsed_time(b) for a, b in ev_h]) * 1e3
-    hot /= args.instr_passes
+    us /= args.instr_passes * R
+    hot /= args.instr_passes * R
     assert fp8bq.fp8bq_device_status() == 0
 
     e2e = None
@@ -1042,6 +1092,7 @@ def run_quant(args, rank, world):
     for i, (M, K, fmt) in enumerate(probs):
         b = quant_bytes(M, K, fmt)
         per.append({"m": M, "k": K, "scale_fmt": fmt, "us": us[i], "us_hot": hot[i],
+                    "us_event": ev_us[i],
                     "gbs_alg": b / (us[i] * 1e-6) / 1e9,
                     "roofline_frac": b / (peaks["hbm_gbs"] * 1e9) / (us[i] * 1e-6)})
     tot = sum(quant_bytes(*p) for p in probs)
@@ -1053,7 +1104,8 @@ def run_quant(args, rank, world):
             "kernel": f"quant_act_kernel, {len(probs)} launches per pass",
             "algorithmic_bytes_per_launch": tot / len(probs),
             "method": "achieved = the pass's algorithmic bytes over the sum of the launches' "
-                      "durations, each timed alone between CUDA events in a graph replay",
+                      "durations, each timed per call over back-to-back calls in a graph "
+                      "that rotate over input copies larger than the L2 together",
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy)"}
     by_fmt = {}
     for fmt in ("fp32", "ue8m0"):
@@ -1073,7 +1125,9 @@ def run_quant(args, rank, world):
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": quant_config(world),
         "passes_per_step": passes,
         "timing": "graph replays; a step = passes_per_step passes over the 30 quant calls; "
-                  "CUDA events on the launching stream around every step",
+                  "CUDA events on the launching stream around every step.  per_shape: us = "
+                  "per call over back-to-back calls rotating over input copies (cold), "
+                  "us_hot = on one copy, us_event = one call between CUDA events",
         "roofline": roof, "targets": by_fmt, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * passes * len(probs), "clocks": clk, "per_shape": per,
         "wall_timed_s": wall, "quant_source_sha256_16": quant_source_hash(),
@@ -1634,6 +1688,8 @@ def main():
     ap.add_argument("--min-timed-s", type=float, default=20.0,
                     help="passes per step are chosen so the K timed steps last at least this")
     ap.add_argument("--instr-passes", type=int, default=10)
+    ap.add_argument("--b2b", type=int, default=8,
+                    help="back-to-back calls per problem in the per-shape measurement")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--oracle-rows", type=int, default=24)
     ap.add_argument("--no-e2e", action="store_true")

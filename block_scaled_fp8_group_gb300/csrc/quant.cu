@@ -75,10 +75,12 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
 
     if (active && a.int8) {
         // block INT8: 16 int8 codes
+        const float r = __fdiv_rn(1.0f, s);
         *reinterpret_cast<uint4*>(a.q + off) =
-            make_uint4(cvt4_int8(f[0], f[1], f[2], f[3], s), cvt4_int8(f[4], f[5], f[6], f[7], s),
-                       cvt4_int8(f[8], f[9], f[10], f[11], s),
-                       cvt4_int8(f[12], f[13], f[14], f[15], s));
+            make_uint4(cvt4_int8_act(f[0], f[1], f[2], f[3], s, r),
+                       cvt4_int8_act(f[4], f[5], f[6], f[7], s, r),
+                       cvt4_int8_act(f[8], f[9], f[10], f[11], s, r),
+                       cvt4_int8_act(f[12], f[13], f[14], f[15], s, r));
     } else if (active) {
         uint32_t c[8];
         if (a.ue8m0) {
@@ -88,24 +90,12 @@ __global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantA
 #pragma unroll
             for (int i = 0; i < 8; ++i) c[i] = cvt2_e4m3(f[2 * i] * r, f[2 * i + 1] * r);
         } else {
-            // fp32 scales: the code of fp32(x / s), computed as y = x * r with
-            // r = fp32(1 / s).  Two roundings of relative size <= 2^-24 put y
-            // within 2 fp32 ulps of x / s, so y and fp32(x / s) give the same
-            // e4m3 code unless a rounding boundary of e4m3 (the midpoint of
-            // two adjacent codes) lies that close to y.  For |y| >= 2^-6
-            // (normal e4m3: 3 mantissa bits kept) such a midpoint has the 20
-            // mantissa bits e4m3 drops equal to 0x80000; y within 8 ulps of
-            // one, or in the e4m3 subnormal range, takes the exact quotient.
+            // fp32 scales: fp32(x / s) from the reciprocal and one residual
+            // correction (act_quotient: exact for these inputs)
             const float r = __fdiv_rn(1.0f, s);
-            float y[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                y[i] = f[i] * r;
-                const uint32_t d = (__float_as_uint(y[i]) & 0xFFFFFu) - 0x80000u + 8u;
-                if (fabsf(y[i]) < 0.015625f || d <= 16u) y[i] = __fdiv_rn(f[i], s);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) c[i] = cvt2_e4m3(y[2 * i], y[2 * i + 1]);
+            for (int i = 0; i < 8; ++i)
+                c[i] = cvt2_e4m3(act_quotient(f[2 * i], s, r), act_quotient(f[2 * i + 1], s, r));
         }
         uint4 out;
         out.x = c[0] | (c[1] << 16);

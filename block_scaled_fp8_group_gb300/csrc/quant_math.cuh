@@ -36,6 +36,39 @@ __device__ __forceinline__ uint32_t cvt2_e4m3(float a, float b) {
                                                           __NV_E4M3));
 }
 
+// fp32(x / s) for an activation value x (bf16 or fp16: at most 11 significant
+// bits) and its group or row scale s = fp32(max(amax, eps) / Q) (amax of the
+// same format, Q = 448 or 127), from r = fp32(1 / s): the product
+// q0 = fp32(x * r), its exact residual x - q0 * s (one FMA) and one
+// correction fp32(q0 + residual * r) -- the division step of P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990.  For every pair of input and
+// scale significands these formats allow, the result is the correctly
+// rounded quotient (the scaling by powers of two commutes with each step
+// while the values stay normal, and quotients below 2^-126 give a zero code
+// either way); a zero quotient takes the sign of x, as the division gives it.
+// It costs three FP operations where the IEEE division needs a reciprocal
+// iteration and a range check per value.
+__device__ __forceinline__ float act_quotient(float x, float s, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, s, x);
+    return copysignf(__fmaf_rn(e, r, q0), x);
+}
+
+// Four activation values -> four int8 codes, as cvt4_int8 with the quotient
+// of act_quotient (r = fp32(1 / s)).
+__device__ __forceinline__ uint32_t cvt4_int8_act(float a, float b, float c, float d, float s,
+                                                  float r) {
+    const float v[4] = {a, b, c, d};
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float y = fminf(fmaxf(act_quotient(v[j], s, r), -kInt8Max), kInt8Max);
+        w |= (static_cast<uint32_t>(__float2int_rn(y)) & 0xFFu) << (8 * j);
+    }
+    return w;
+}
+
 // Four fp32 values -> four int8 codes (byte j = value j): round half to even
 // of clamp(v / s, -127, 127), with the IEEE division.
 __device__ __forceinline__ uint32_t cvt4_int8(float a, float b, float c, float d, float s) {
