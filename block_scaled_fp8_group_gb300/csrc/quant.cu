@@ -30,8 +30,12 @@ namespace {
 // those with compile-time constants or kernel arguments.
 constexpr int kQuantRows = 8;  // warps per CTA = rows per CTA
 
+// Eight resident CTAs per SM (at most 32 registers a thread): the kernel is a
+// load-latency-bound stream, and the full 64 warps keep more loads in flight
+// than the 48 that 40 registers allow (16384 x 18432: 0.84 -> 0.89 of the
+// measured copy bandwidth with UE8M0 scales, 0.78 -> 0.82 with fp32 scales).
 template <bool kFp16, bool kGrouped>
-__global__ void __launch_bounds__(kQuantRows * 32) quant_act_kernel(const QuantActArgs a) {
+__global__ void __launch_bounds__(kQuantRows * 32, 8) quant_act_kernel(const QuantActArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t wrow = static_cast<int64_t>(blockIdx.x) * kQuantRows + (threadIdx.x >> 5);
     const int64_t row = kGrouped ? static_cast<int64_t>(blockIdx.z) * a.m_max + wrow : wrow;

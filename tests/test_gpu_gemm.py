@@ -187,15 +187,20 @@ def test_decode_every_element(fp8bq, N, K, M):
 @pytest.mark.parametrize("M", synth.PREFILL_M)
 def test_prefill_full_size_sampled(fp8bq, N, K, M):
     """Prefill sweep at full size (fp32 scales, bf16 and fp32 out): all N
-    columns of 64 seeded rows plus the tile-boundary rows."""
+    columns of 64 seeded rows plus the tile-boundary rows, through the GEMM
+    on oracle-quantised inputs and through the fused linear entry point (GPU
+    quant of the same bf16 input, then the GEMM with its weight prefetch)."""
     xb, qa, sa, qw, sw = quantised_problem(M, N, K, False, synth.act_prefill, weight="bf16")
     d = upload(qa, sa, qw, sw)
     rows = sample_rows(M, 64)
     ref = oracle_rows(qa, sa, qw, sw, False, rows)
+    x = to_dev_bits(xb)
     for out in ("bf16", "fp32"):
         o = fp8bq.fp8bq_gemm(*d, fmt="fp32", out_dtype=TORCH_OUT[out])
+        lin = fp8bq.fp8bq_linear(x, d[2], d[3], fmt="fp32", out_dtype=TORCH_OUT[out])
         torch.cuda.synchronize()
         check_gemm(o.float().cpu().numpy()[rows], ref, out, f"prefill {M}x{N}x{K} {out}")
+        check_gemm(lin.float().cpu().numpy()[rows], ref, out, f"prefill linear {M}x{N}x{K} {out}")
 
 
 _GRID_W = {}   # (N, K) -> (oracle codes, oracle scales, device codes, device scales)
